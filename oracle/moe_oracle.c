@@ -1,0 +1,373 @@
+/*
+ * Plain CPU oracle of the fused Mixture-of-Experts layer forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or call
+ * this file: only the test suite, the smoke check and the benchmark's CPU
+ * baseline leg use it.  It shares no code, header, table or constant with the
+ * CUDA library; both sides only see the same seeded inputs.
+ *
+ * Every step is written the slow, obvious way, in double precision, one token
+ * at a time, in the order the pages describe the layer:
+ *
+ *   route -> process the token with each of its top-k experts -> weighted sum
+ *   ("FusedMoE vs MegaMoE" (zwxr.cn), section 2: the router produces a weight
+ *   distribution, the k best experts process the token, their results are
+ *   summed with the weights; section 3.1: routing, sorting by expert, index
+ *   construction, fused expert computation, reorder + weighted sum).
+ *
+ * Readings of points the pages leave open (each one is a named choice):
+ *   - softmax over all E experts, then top-k; renormalisation optional;
+ *   - ranking by probability == ranking by logit (softmax is strictly
+ *     monotone); equal logits rank the lower expert index first;
+ *   - w13[e] holds the gate rows [0, I) above the up rows [I, 2I);
+ *     SiLU(z) = z / (1 + exp(-z)); the routing weight is applied after the
+ *     down projection;
+ *   - the permutation lists, expert by expert in ascending order, the flat
+ *     pair indices f = t*k + j in ascending order, pads each expert to a
+ *     multiple of the block size with the sentinel T*k, and gives empty
+ *     experts no block;
+ *   - FP8 (e4m3, OCP 8-bit floating point spec): one fp32 scale per expert
+ *     weight tensor, one dynamic scale for the layer input and one for the
+ *     intermediate activation, scale = amax / 448 (1 when amax is 0), codes by
+ *     round-to-nearest-even with saturation to +-448.  The code decision is
+ *     taken in fp32 (x / scale in fp32), the precision a kernel takes it in.
+ *
+ * Build: gcc -O2 -fPIC -shared -fopenmp (OpenMP only splits independent
+ * tokens across threads; each token's arithmetic is unchanged).
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_E4M3 = 2 };
+
+/* ------------------------------------------------------------------------ */
+/* Number formats                                                            */
+/* ------------------------------------------------------------------------ */
+
+/* bfloat16: the top 16 bits of an IEEE binary32. */
+double oracle_bf16_to_f64(uint16_t v) {
+  uint32_t bits = (uint32_t)v << 16;
+  float f;
+  memcpy(&f, &bits, sizeof f);
+  return (double)f;
+}
+
+/* binary32 -> bfloat16, round to nearest, ties to even (NaN stays NaN). */
+uint16_t oracle_f32_to_bf16(float f) {
+  uint32_t bits;
+  memcpy(&bits, &f, sizeof bits);
+  if ((bits & 0x7f800000u) == 0x7f800000u && (bits & 0x007fffffu)) return (uint16_t)((bits >> 16) | 0x40u);
+  uint32_t upper = bits >> 16;
+  uint32_t lower = bits & 0xffffu;
+  if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) upper += 1u;
+  return (uint16_t)upper;
+}
+
+/* E4M3 (OCP FP8): 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits,
+ * no infinities, S.1111.111 is NaN, largest finite magnitude 448.
+ * exponent field 0 is subnormal: value = mantissa/8 * 2^-6. */
+double oracle_e4m3_to_f64(uint8_t c) {
+  int sign = (c >> 7) & 1;
+  int ex = (c >> 3) & 0xf;
+  int man = c & 0x7;
+  double mag;
+  if (ex == 0xf && man == 0x7) return NAN;
+  if (ex == 0)
+    mag = ldexp((double)man / 8.0, -6);
+  else
+    mag = ldexp(1.0 + (double)man / 8.0, ex - 7);
+  return sign ? -mag : mag;
+}
+
+/* float -> E4M3, round to nearest with ties to even, saturating to +-448.
+ * Written as a search over the 127 non-negative finite codes, which are in
+ * increasing order of value: find the two neighbours and pick the nearer,
+ * the even code on a tie. */
+uint8_t oracle_f32_to_e4m3_satfinite(float f) {
+  if (isnan(f)) return 0x7f;
+  uint8_t sign = signbit(f) ? 0x80 : 0x00;
+  double a = fabs((double)f);
+  if (a >= 448.0) return (uint8_t)(sign | 0x7e);
+  int lo = 0; /* largest code with value <= a */
+  for (int c = 0; c <= 0x7e; ++c) {
+    if (oracle_e4m3_to_f64((uint8_t)c) <= a) lo = c;
+  }
+  int hi = lo + 1;
+  double vlo = oracle_e4m3_to_f64((uint8_t)lo);
+  double vhi = oracle_e4m3_to_f64((uint8_t)hi);
+  int pick;
+  if (a - vlo < vhi - a) pick = lo;
+  else if (a - vlo > vhi - a) pick = hi;
+  else pick = (lo & 1) ? hi : lo;
+  if (a == vlo) pick = lo;
+  return (uint8_t)(sign | pick);
+}
+
+static double load_elem(const void* p, int dtype, size_t i) {
+  switch (dtype) {
+    case ORC_F32: return (double)((const float*)p)[i];
+    case ORC_BF16: return oracle_bf16_to_f64(((const uint16_t*)p)[i]);
+    case ORC_E4M3: return oracle_e4m3_to_f64(((const uint8_t*)p)[i]);
+  }
+  return NAN;
+}
+
+static float load_f32(const void* p, int dtype, size_t i) { return (float)load_elem(p, dtype, i); }
+
+double oracle_silu(double z) { return z / (1.0 + exp(-z)); }
+
+/* ------------------------------------------------------------------------ */
+/* Step 1: router gate GEMM, logits[t][e] = sum_h X[t][h] * Wr[e][h]         */
+/* ("FusedMoE vs MegaMoE", section 2: the router computes, per token, a      */
+/*  weight distribution over the experts.)                                   */
+/* ------------------------------------------------------------------------ */
+void oracle_router_logits(const void* X, const void* Wr, int dtype, int T, int H, int E, double* logits) {
+#pragma omp parallel for schedule(static)
+  for (int t = 0; t < T; ++t) {
+    for (int e = 0; e < E; ++e) {
+      double s = 0.0;
+      for (int h = 0; h < H; ++h) s += load_elem(X, dtype, (size_t)t * H + h) * load_elem(Wr, dtype, (size_t)e * H + h);
+      logits[(size_t)t * E + e] = s;
+    }
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step 2: softmax over all experts, top-k, optional renormalisation         */
+/* ("FusedMoE vs MegaMoE", section 2: the k highest-weight experts are       */
+/*  chosen; section 5 names this Top-k gating.)                              */
+/* ------------------------------------------------------------------------ */
+int oracle_topk(const double* logits, int T, int E, int k, int renorm, int32_t* ids, double* w) {
+  if (k < 1 || k > E) return -1;
+  char* taken = (char*)malloc((size_t)E);
+  double* p = (double*)malloc(sizeof(double) * (size_t)E);
+  if (!taken || !p) { free(taken); free(p); return -2; }
+  for (int t = 0; t < T; ++t) {
+    const double* l = logits + (size_t)t * E;
+    double m = l[0];
+    for (int e = 1; e < E; ++e) if (l[e] > m) m = l[e];
+    double z = 0.0;
+    for (int e = 0; e < E; ++e) { p[e] = exp(l[e] - m); z += p[e]; }
+    for (int e = 0; e < E; ++e) p[e] /= z;
+    memset(taken, 0, (size_t)E);
+    /* k rounds of "pick the largest not yet taken"; the strict > keeps the
+     * lower index on equal logits.  The ranking uses the logit itself, which
+     * orders exactly like p (exp is strictly increasing). */
+    for (int j = 0; j < k; ++j) {
+      int best = -1;
+      for (int e = 0; e < E; ++e) {
+        if (taken[e]) continue;
+        if (best < 0 || l[e] > l[best]) best = e;
+      }
+      taken[best] = 1;
+      ids[(size_t)t * k + j] = best;
+      w[(size_t)t * k + j] = p[best];
+    }
+    if (renorm) {
+      double s = 0.0;
+      for (int j = 0; j < k; ++j) s += w[(size_t)t * k + j];
+      for (int j = 0; j < k; ++j) w[(size_t)t * k + j] /= s;
+    }
+  }
+  free(taken);
+  free(p);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step 3: token-to-expert permutation                                       */
+/* ("FusedMoE vs MegaMoE", section 3.1: sort the routed tokens by expert and */
+/*  build the index that says which rows belong to which expert; page 1,     */
+/*  "Routage backend...": variable token bucketing onto expert tiles.)       */
+/* sorted capacity: T*k + min(E, T*k)*(B-1); expert_ids capacity: that / B.  */
+/* ------------------------------------------------------------------------ */
+int oracle_align(const int32_t* ids, int T, int k, int E, int B, int32_t* sorted, int32_t* expert_ids,
+                 int32_t* num_post_pad, int32_t* counts) {
+  if (B < 1) return -1;
+  const int64_t n = (int64_t)T * k;
+  const int32_t sentinel = (int32_t)n;
+  int64_t pos = 0, blk = 0;
+  for (int e = 0; e < E; ++e) {
+    int64_t c = 0;
+    for (int64_t f = 0; f < n; ++f) {
+      if (ids[f] == e) { sorted[pos++] = (int32_t)f; ++c; }
+    }
+    if (counts) counts[e] = (int32_t)c;
+    if (c == 0) continue;
+    int64_t padded = (c + B - 1) / B * B;
+    for (int64_t q = c; q < padded; ++q) sorted[pos++] = sentinel;
+    for (int64_t b = 0; b < padded / B; ++b) expert_ids[blk++] = e;
+  }
+  *num_post_pad = (int32_t)pos;
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Dynamic per-tensor e4m3 quantisation of one tensor (page 1, "Routage      */
+/* backend pour la quantisation des tenseurs FP8": per-tensor FP8 with the   */
+/* scale applied where the data is used, read from HBM once).               */
+/* ------------------------------------------------------------------------ */
+float oracle_e4m3_scale(float amax) { return amax > 0.0f ? amax / 448.0f : 1.0f; }
+
+uint8_t oracle_e4m3_quant(float v, float scale) { return oracle_f32_to_e4m3_satfinite(v / scale); }
+
+/* ------------------------------------------------------------------------ */
+/* Steps 4-7: per-token expert FFNs and the routing-weighted combine.        */
+/* out[i][:] is the output of token tokens[i] (or i when tokens is NULL).    */
+/* The router is step 1-2 above, run on the stored inputs.                   */
+/* ids_out / w_out (nullable) receive the routing of every one of the T      */
+/* tokens.  In FP8 mode the two activation scales are layer-wide: the input  */
+/* scale is taken over all T tokens, the intermediate one over every routed  */
+/* (token, expert) pair of all T tokens, so the intermediate is formed for   */
+/* all T tokens even when only a subset of outputs is asked for.             */
+/* Returns 0, or a negative value on bad arguments.                          */
+/* ------------------------------------------------------------------------ */
+int oracle_moe_forward(const void* X, const void* Wr, const void* W13, const void* W2, int act_dtype, int w_dtype,
+                       int T, int H, int I, int E, int k, int renorm, const float* w13_scale, const float* w2_scale,
+                       const int32_t* tokens, int n_tokens, double* out, int32_t* ids_out, double* w_out,
+                       float* act_scales_out) {
+  if (T < 0 || H < 1 || I < 1 || E < 1 || k < 1 || k > E) return -1;
+  if (act_dtype != ORC_F32 && act_dtype != ORC_BF16) return -1;
+  const int fp8 = (w_dtype == ORC_E4M3);
+  if (fp8 && (!w13_scale || !w2_scale || act_dtype != ORC_BF16)) return -1;
+  if (!tokens) n_tokens = T;
+  if (T == 0) return 0;
+
+  double* logits = (double*)malloc(sizeof(double) * (size_t)T * E);
+  int32_t* ids = (int32_t*)malloc(sizeof(int32_t) * (size_t)T * k);
+  double* w = (double*)malloc(sizeof(double) * (size_t)T * k);
+  if (!logits || !ids || !w) { free(logits); free(ids); free(w); return -2; }
+  oracle_router_logits(X, Wr, act_dtype, T, H, E, logits);
+  oracle_topk(logits, T, E, k, renorm, ids, w);
+  free(logits);
+  if (ids_out) memcpy(ids_out, ids, sizeof(int32_t) * (size_t)T * k);
+  if (w_out) memcpy(w_out, w, sizeof(double) * (size_t)T * k);
+
+  if (!fp8) {
+#pragma omp parallel
+    {
+      double* x = (double*)malloc(sizeof(double) * (size_t)H);
+      double* a = (double*)malloc(sizeof(double) * (size_t)I);
+#pragma omp for schedule(dynamic, 1)
+      for (int q = 0; q < n_tokens; ++q) {
+        const int t = tokens ? tokens[q] : q;
+        double* o = out + (size_t)q * H;
+        for (int h = 0; h < H; ++h) { x[h] = load_elem(X, act_dtype, (size_t)t * H + h); o[h] = 0.0; }
+        for (int j = 0; j < k; ++j) {
+          const int e = ids[(size_t)t * k + j];
+          const size_t w13_base = (size_t)e * 2 * I * H;
+          for (int i = 0; i < I; ++i) {
+            double g = 0.0, u = 0.0;
+            for (int h = 0; h < H; ++h) {
+              g += load_elem(W13, w_dtype, w13_base + (size_t)i * H + h) * x[h];
+              u += load_elem(W13, w_dtype, w13_base + (size_t)(I + i) * H + h) * x[h];
+            }
+            a[i] = oracle_silu(g) * u;
+          }
+          const size_t w2_base = (size_t)e * H * I;
+          const double wj = w[(size_t)t * k + j];
+          for (int h = 0; h < H; ++h) {
+            double y = 0.0;
+            for (int i = 0; i < I; ++i) y += load_elem(W2, w_dtype, w2_base + (size_t)h * I + i) * a[i];
+            o[h] += wj * y;
+          }
+        }
+      }
+      free(x);
+      free(a);
+    }
+    free(ids);
+    free(w);
+    return 0;
+  }
+
+  /* FP8: quantise the layer input with one dynamic scale. */
+  float amax_x = 0.0f;
+  for (size_t i = 0; i < (size_t)T * H; ++i) {
+    float v = fabsf(load_f32(X, act_dtype, i));
+    if (v > amax_x) amax_x = v;
+  }
+  const float s_a1 = oracle_e4m3_scale(amax_x);
+  /* Intermediate activation of every routed pair, kept to find its scale. */
+  double* A = (double*)malloc(sizeof(double) * (size_t)T * k * I);
+  if (!A) { free(ids); free(w); return -2; }
+#pragma omp parallel
+  {
+    double* xq = (double*)malloc(sizeof(double) * (size_t)H);
+#pragma omp for schedule(dynamic, 1)
+    for (int t = 0; t < T; ++t) {
+      for (int h = 0; h < H; ++h)
+        xq[h] = oracle_e4m3_to_f64(oracle_e4m3_quant(load_f32(X, act_dtype, (size_t)t * H + h), s_a1));
+      for (int j = 0; j < k; ++j) {
+        const int e = ids[(size_t)t * k + j];
+        const size_t w13_base = (size_t)e * 2 * I * H;
+        for (int i = 0; i < I; ++i) {
+          double g = 0.0, u = 0.0;
+          for (int h = 0; h < H; ++h) {
+            g += oracle_e4m3_to_f64(((const uint8_t*)W13)[w13_base + (size_t)i * H + h]) * xq[h];
+            u += oracle_e4m3_to_f64(((const uint8_t*)W13)[w13_base + (size_t)(I + i) * H + h]) * xq[h];
+          }
+          g = g * (double)s_a1 * (double)w13_scale[e];
+          u = u * (double)s_a1 * (double)w13_scale[e];
+          A[((size_t)t * k + j) * I + i] = oracle_silu(g) * u;
+        }
+      }
+    }
+    free(xq);
+  }
+  double amax_a = 0.0;
+  for (size_t i = 0; i < (size_t)T * k * I; ++i) if (fabs(A[i]) > amax_a) amax_a = fabs(A[i]);
+  const float s_a2 = oracle_e4m3_scale((float)amax_a);
+  if (act_scales_out) { act_scales_out[0] = s_a1; act_scales_out[1] = s_a2; }
+#pragma omp parallel
+  {
+    double* aq = (double*)malloc(sizeof(double) * (size_t)I);
+#pragma omp for schedule(dynamic, 1)
+    for (int q = 0; q < n_tokens; ++q) {
+      const int t = tokens ? tokens[q] : q;
+      double* o = out + (size_t)q * H;
+      for (int h = 0; h < H; ++h) o[h] = 0.0;
+      for (int j = 0; j < k; ++j) {
+        const int e = ids[(size_t)t * k + j];
+        for (int i = 0; i < I; ++i)
+          aq[i] = oracle_e4m3_to_f64(oracle_e4m3_quant((float)A[((size_t)t * k + j) * I + i], s_a2));
+        const size_t w2_base = (size_t)e * H * I;
+        const double wj = w[(size_t)t * k + j];
+        for (int h = 0; h < H; ++h) {
+          double y = 0.0;
+          for (int i = 0; i < I; ++i) y += oracle_e4m3_to_f64(((const uint8_t*)W2)[w2_base + (size_t)h * I + i]) * aq[i];
+          y = y * (double)s_a2 * (double)w2_scale[e];
+          o[h] += wj * y;
+        }
+      }
+    }
+    free(aq);
+  }
+  free(A);
+  free(ids);
+  free(w);
+  return 0;
+}
+
+/* Thread control for timing the oracle single-threaded and on all cores. */
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
+int oracle_get_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
