@@ -1,0 +1,194 @@
+/*
+ * moe_api.h -- C ABI of the GB300 (sm_103a) fused Mixture-of-Experts layer forward.
+ *
+ * The layer (one call of moe_forward) is the fused MoE operation the pages
+ * describe: token routing, the data shuffle that groups tokens by expert, the
+ * expert networks and the routing-weighted sum back to token order, run as one
+ * batched GPU operation instead of a loop over experts
+ *   ("Mixture-of-Experts kernel engineering on Amazon SageMaker AI", intro;
+ *    "FusedMoE vs MegaMoE" (zwxr.cn), sections 2 and 3.1).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Pointers named *hidden*, *router_w*, *w13*, *w2*, *out*, *logits*,
+ *    *topk_*, *sorted_ids*, *expert_ids*, *num_post_pad*, *expert_counts*,
+ *    *workspace* and the FP8 scales are DEVICE pointers of the current CUDA
+ *    device.  The caller owns all of them; the library never allocates,
+ *    frees or retains device memory across calls (it keeps one status word
+ *    per device, see moe_get_status).
+ *  - All arrays are dense row-major with no padding between rows.  Device
+ *    pointers must be 16-byte aligned (MOE_ERR_ALIGNMENT otherwise).
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream).  A return of MOE_OK means "validated and
+ *    enqueued"; faults found by the kernels themselves (an expert id out of
+ *    range, a bounded wait that ran out) are reported by moe_get_status.
+ *  - Results are deterministic: the same inputs give bitwise-identical outputs
+ *    on every call (fixed reduction orders, no floating-point atomics).
+ *  - Shapes are runtime arguments; no call compiles or specialises code for a
+ *    new token count (page 1, section "Élimination de la recompilation JIT de
+ *    Triton": recompiling per num_tokens cost 9 % TTFT at 8-way TP).
+ *  - T = 0 is a valid, empty call (nothing is enqueued, MOE_OK).
+ *
+ * Notation: T tokens, H hidden size, I expert intermediate size, E experts,
+ * k = topk experts per token, B = block (token-tile) size of the permutation.
+ */
+#ifndef MOE_API_H
+#define MOE_API_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(MOE_BUILD_LIBRARY) && defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t */
+typedef struct CUevent_st* moe_event_t;   /* same type as cudaEvent_t */
+
+/* Element types.  BF16 is stored as 16-bit bfloat16, E4M3 as 8-bit OCP E4M3
+ * codes (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, max 448). */
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2 } moe_dtype;
+
+/* Return codes (0 or negative). */
+enum {
+  MOE_OK = 0,
+  MOE_ERR_ARG = -1,            /* bad size, null pointer, bad enum */
+  MOE_ERR_UNSUPPORTED = -2,    /* valid but not implemented (dtype pair, shape rule) */
+  MOE_ERR_WORKSPACE = -3,      /* workspace smaller than moe_workspace_size() */
+  MOE_ERR_CUDA = -4,           /* a CUDA runtime call failed (launch, no device ...) */
+  MOE_ERR_DEVICE_TIMEOUT = -5, /* a kernel's bounded wait ran out (from moe_get_status) */
+  MOE_ERR_DEVICE_INDEX = -6,   /* a kernel met an expert id outside [0, E) (moe_get_status) */
+  MOE_ERR_ALIGNMENT = -7       /* a device pointer is not 16-byte aligned */
+};
+
+/* Orientation of the grouped expert GEMMs.
+ * SWAP_AB computes C^T[N,M] = B^T[N,K] * A^T[K,M]: the expert weight rows fill
+ * the tensor core's fixed 128-row M slot and the few tokens of an expert
+ * take the flexible N slot (page 1, section "Swap-AB pour l'utilisation de
+ * WGMMA", Figure 1; re-derived here for tcgen05, whose M slot is 128).
+ * TOKEN_MAJOR puts 128 sorted token rows in the M slot (prefill).
+ * AUTO picks SWAP_AB for T <= 64 and TOKEN_MAJOR above. */
+typedef enum { MOE_ORIENT_AUTO = 0, MOE_ORIENT_SWAP_AB = 1, MOE_ORIENT_TOKEN_MAJOR = 2 } moe_orientation;
+
+/* Stages of moe_forward, for the optional timing events below. */
+typedef enum {
+  MOE_STAGE_ROUTE = 0,   /* router GEMM + softmax/top-k (+ renorm) */
+  MOE_STAGE_ALIGN = 1,   /* histogram / scan / stable scatter */
+  MOE_STAGE_GATHER = 2,  /* activation rows in expert order (+ FP8 input quantisation) */
+  MOE_STAGE_GEMM1 = 3,   /* grouped GEMM on w13 with the SiLU(gate)*up epilogue */
+  MOE_STAGE_ACT = 4,     /* split-K reduction / FP8 intermediate quantisation (may be empty) */
+  MOE_STAGE_GEMM2 = 5,   /* grouped GEMM on w2 */
+  MOE_STAGE_COMBINE = 6, /* routing-weighted sum back to token order */
+  MOE_NUM_STAGES = 7
+} moe_stage;
+
+/* Optional knobs of moe_forward / moe_workspace_size.  Pass NULL for defaults
+ * (all-zero struct == defaults).  The same options must be given to
+ * moe_workspace_size and to the moe_forward calls that use that workspace. */
+typedef struct {
+  int orientation;    /* moe_orientation; SWAP_AB needs T <= 256 */
+  int split_k;        /* 0 = automatic; n > 0 forces n K-splits in SWAP_AB mode */
+  int inject_timeout; /* test hook: 1 makes the first kernel wait on a device flag that
+                         nothing sets, with a ~1 ms bound; the call then reports
+                         MOE_ERR_DEVICE_TIMEOUT through moe_get_status and writes
+                         nothing else.  0 in normal use. */
+  int reserved;
+  /* Nullable CUDA events recorded on `stream` right before / after the
+   * kernels of each stage (the caller creates and owns them). */
+  moe_event_t stage_begin[MOE_NUM_STAGES];
+  moe_event_t stage_end[MOE_NUM_STAGES];
+} moe_options;
+
+/* Human-readable text of a return code (static storage). */
+MOE_API const char* moe_strerror(int code);
+
+/* Bytes of device workspace moe_forward needs for this shape, dtype pair and
+ * options (written to *bytes).  Depends only on its arguments. */
+MOE_API int moe_workspace_size(int T, int H, int I, int E, int topk, moe_dtype act_dtype, moe_dtype w_dtype,
+                       const moe_options* opts, size_t* bytes);
+
+/* Capacities of the permutation outputs for (T, topk, E, block):
+ *   sorted_cap = T*topk + min(E, T*topk)*(block-1)     (int32 entries)
+ *   blocks_cap = sorted_cap / block                     (int32 entries) */
+MOE_API int moe_align_capacity(int T, int topk, int E, int block, size_t* sorted_cap, size_t* blocks_cap);
+
+/* Router: steps 1-2 of the layer
+ *   ("FusedMoE vs MegaMoE", section 2: the router gives every token a weight
+ *    distribution over experts and the k highest experts are chosen).
+ *   logits_out[T][E] (fp32, required) = hidden[T][H] . router_w[E][H]^T, fp32 accumulation;
+ *   p = softmax over all E; topk_ids[T][topk] (int32) = the topk largest p in
+ *   descending order, equal values ranked by lower expert index (ranking is on
+ *   the fp32 logit, which orders like p); topk_w[T][topk] (fp32) = p of those
+ *   experts, divided by their sum when renorm != 0.
+ * hidden and router_w have type act_dtype (MOE_F32 or MOE_BF16).
+ * Limits: 1 <= topk <= min(E, 32), E <= 1024. */
+MOE_API int moe_route(const void* hidden, const void* router_w, int T, int H, int E, int topk, int renorm,
+              moe_dtype act_dtype, float* logits_out, float* topk_w, int32_t* topk_ids, moe_stream_t stream);
+
+/* Step 2 alone, from given fp32 logits[T][E] (same ranking and weights as
+ * moe_route).  Lets routing be compared exactly on identical logits. */
+MOE_API int moe_topk_from_logits(const float* logits, int T, int E, int topk, int renorm, float* topk_w,
+                         int32_t* topk_ids, moe_stream_t stream);
+
+/* Step 3: token-to-expert permutation
+ *   ("FusedMoE vs MegaMoE", section 3.1: sort routed tokens by expert and
+ *    build the index of which rows belong to which expert; page 1, section
+ *    "Routage backend...": variable token bucketing onto expert tiles).
+ * For every (token t, slot j) pair the flat index f = t*topk + j.  Experts are
+ * laid out in ascending order; inside an expert its f values ascend (stable);
+ * each expert's run is padded with the sentinel T*topk to a multiple of
+ * `block`; experts without tokens get no block.
+ *   sorted_ids[sorted_cap]   int32, entries [0, *num_post_pad) written
+ *   expert_ids[blocks_cap]   int32, expert of each block, [0, *num_post_pad/block) written
+ *   num_post_pad[1]          int32, total padded length
+ *   expert_counts[E]         int32, tokens per expert (nullable)
+ * Ids outside [0, E) are dropped and flagged as MOE_ERR_DEVICE_INDEX (moe_get_status).
+ * Limits: E <= 1024, 1 <= block <= 1024, T*topk < 2^31. */
+MOE_API int moe_align(const int32_t* topk_ids, int T, int topk, int E, int block, int32_t* sorted_ids, int32_t* expert_ids,
+              int32_t* num_post_pad, int32_t* expert_counts, moe_stream_t stream);
+
+/* The whole layer forward, steps 1-7, on `stream`:
+ *   route -> align -> gather -> GEMM1 (w13) + SiLU(gate)*up -> GEMM2 (w2) -> combine
+ *   out[t] = sum_j topk_w[t][j] * W2[e_j] . (SiLU(W13[e_j][0:I] . x_t) * (W13[e_j][I:2I] . x_t))
+ *   ("FusedMoE vs MegaMoE", sections 2 and 3.1; page 1, sections on Swap-AB and FP8).
+ * Arguments:
+ *   hidden   [T][H]      act_dtype (MOE_F32 or MOE_BF16)
+ *   router_w [E][H]      act_dtype
+ *   w13      [E][2I][H]  w_dtype; rows [0, I) are the gate, rows [I, 2I) the up projection
+ *   w2       [E][H][I]   w_dtype
+ *   w13_scale, w2_scale  [E] fp32 per-expert dequantisation scales, required iff w_dtype == MOE_E4M3
+ *   out      [T][H]      act_dtype
+ *   workspace            >= moe_workspace_size(...) bytes, 256-byte aligned, contents ignored
+ * Supported dtype pairs:
+ *   (F32, F32)   fp32 CUDA-core path, any H, I >= 1
+ *   (BF16, BF16) tcgen05 tensor-core path (kind::f16, fp32 accumulation in TMEM)
+ *   (BF16, E4M3) tcgen05 kind::f8f6f4 path: the input is quantised to e4m3 with one
+ *                dynamic scale amax/448, the intermediate likewise; the scales are applied
+ *                in the GEMM epilogues (page 1, section "Routage backend pour la
+ *                quantisation des tenseurs FP8": scaling fused where the data is used)
+ *   tensor-core paths need H % 128 == 0 and I % 128 == 0.
+ * The intermediate SiLU(gate)*up is stored in bf16 (fp32 on the fp32 path, e4m3 on
+ * the FP8 path); accumulation is fp32 throughout; out is rounded once. */
+MOE_API int moe_forward(const void* hidden, const void* router_w, const void* w13, const void* w2, int T, int H, int I, int E,
+                int topk, int renorm, moe_dtype act_dtype, moe_dtype w_dtype, const float* w13_scale,
+                const float* w2_scale, void* out, void* workspace, size_t workspace_bytes, const moe_options* opts,
+                moe_stream_t stream);
+
+/* Synchronises `stream`, then reads and clears this device's status word.
+ * Returns MOE_OK, MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_DEVICE_INDEX or MOE_ERR_CUDA. */
+MOE_API int moe_get_status(moe_stream_t stream);
+
+/* Library version as major*10000 + minor*100 + patch. */
+MOE_API int moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_API_H */

@@ -1,0 +1,197 @@
+"""Python binding of the GB300 fused MoE layer library (ctypes over include/moe_api.h).
+
+Argument marshalling only: every step of the layer runs in the CUDA kernels of
+libmoe_gb300.so.  PyTorch supplies device memory and streams.  The names
+mirror the C entry points; each raises MoeError on a nonzero return code.
+If the shared library is missing this module fails at import, loudly: there is
+no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe_gb300.so")
+
+MOE_F32, MOE_BF16, MOE_E4M3 = 0, 1, 2
+MOE_OK, MOE_ERR_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE = 0, -1, -2, -3
+MOE_ERR_CUDA, MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_DEVICE_INDEX, MOE_ERR_ALIGNMENT = -4, -5, -6, -7
+ORIENT_AUTO, ORIENT_SWAP_AB, ORIENT_TOKEN_MAJOR = 0, 1, 2
+STAGES = ("route", "align", "gather", "gemm1", "act", "gemm2", "combine")
+NUM_STAGES = len(STAGES)
+
+# every entry point include/moe_api.h declares
+EXPORTS = ("moe_strerror", "moe_workspace_size", "moe_align_capacity", "moe_route", "moe_topk_from_logits",
+           "moe_align", "moe_forward", "moe_get_status", "moe_version")
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {strerror(code)} ({code})")
+
+
+class moe_options(ctypes.Structure):
+    _fields_ = [("orientation", ctypes.c_int), ("split_k", ctypes.c_int), ("inject_timeout", ctypes.c_int),
+                ("reserved", ctypes.c_int), ("stage_begin", ctypes.c_void_p * NUM_STAGES),
+                ("stage_end", ctypes.c_void_p * NUM_STAGES)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built; run __graft_entry__.build() (nvcc, sm_103a)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.moe_strerror.restype = ctypes.c_char_p
+    lib.moe_strerror.argtypes = [i]
+    lib.moe_version.restype = i
+    lib.moe_version.argtypes = []
+    lib.moe_workspace_size.restype = i
+    lib.moe_workspace_size.argtypes = [i, i, i, i, i, i, i, P, ctypes.POINTER(sz)]
+    lib.moe_align_capacity.restype = i
+    lib.moe_align_capacity.argtypes = [i, i, i, i, ctypes.POINTER(sz), ctypes.POINTER(sz)]
+    lib.moe_route.restype = i
+    lib.moe_route.argtypes = [P, P, i, i, i, i, i, i, P, P, P, P]
+    lib.moe_topk_from_logits.restype = i
+    lib.moe_topk_from_logits.argtypes = [P, i, i, i, i, P, P, P]
+    lib.moe_align.restype = i
+    lib.moe_align.argtypes = [P, i, i, i, i, P, P, P, P, P]
+    lib.moe_forward.restype = i
+    lib.moe_forward.argtypes = [P, P, P, P, i, i, i, i, i, i, i, i, P, P, P, P, sz, P, P]
+    lib.moe_get_status.restype = i
+    lib.moe_get_status.argtypes = [P]
+    return lib
+
+
+_lib = _load()
+
+
+def lib():
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return _lib.moe_strerror(int(code)).decode()
+
+
+def version() -> int:
+    return int(_lib.moe_version())
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != 0:
+        raise MoeError(rc, where)
+
+
+def _dt(t: torch.Tensor) -> int:
+    return {torch.float32: MOE_F32, torch.bfloat16: MOE_BF16, torch.float8_e4m3fn: MOE_E4M3,
+            torch.uint8: MOE_E4M3}[t.dtype]
+
+
+def _p(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _opts(options) -> Optional[ctypes.POINTER(moe_options)]:
+    if options is None:
+        return None
+    if isinstance(options, moe_options):
+        return ctypes.byref(options)
+    o = moe_options()
+    o.orientation = int(options.get("orientation", 0))
+    o.split_k = int(options.get("split_k", 0))
+    o.inject_timeout = int(options.get("inject_timeout", 0))
+    for name, ev in (options.get("stage_begin") or {}).items():
+        o.stage_begin[STAGES.index(name)] = ctypes.c_void_p(ev.cuda_event)
+    for name, ev in (options.get("stage_end") or {}).items():
+        o.stage_end[STAGES.index(name)] = ctypes.c_void_p(ev.cuda_event)
+    return ctypes.byref(o)
+
+
+def moe_workspace_size(T: int, H: int, I: int, E: int, topk: int, act_dtype: int, w_dtype: int, options=None) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_lib.moe_workspace_size(T, H, I, E, topk, act_dtype, w_dtype, _opts(options), ctypes.byref(n)),
+           "moe_workspace_size")
+    return int(n.value)
+
+
+def moe_align_capacity(T: int, topk: int, E: int, block: int):
+    a, b = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check(_lib.moe_align_capacity(T, topk, E, block, ctypes.byref(a), ctypes.byref(b)), "moe_align_capacity")
+    return int(a.value), int(b.value)
+
+
+def moe_route(hidden: torch.Tensor, router_w: torch.Tensor, topk: int, renorm: bool, logits=None, topk_w=None,
+              topk_ids=None, stream=None):
+    """Router logits [T,E] fp32, top-k weights [T,k] fp32 and ids [T,k] int32."""
+    T, H = hidden.shape
+    E = router_w.shape[0]
+    dev = hidden.device
+    logits = torch.empty(T, E, dtype=torch.float32, device=dev) if logits is None else logits
+    topk_w = torch.empty(T, topk, dtype=torch.float32, device=dev) if topk_w is None else topk_w
+    topk_ids = torch.empty(T, topk, dtype=torch.int32, device=dev) if topk_ids is None else topk_ids
+    _check(_lib.moe_route(_p(hidden), _p(router_w), T, H, E, topk, int(bool(renorm)), _dt(hidden), _p(logits),
+                          _p(topk_w), _p(topk_ids), _stream(stream)), "moe_route")
+    return logits, topk_w, topk_ids
+
+
+def moe_topk_from_logits(logits: torch.Tensor, topk: int, renorm: bool, topk_w=None, topk_ids=None, stream=None):
+    T, E = logits.shape
+    dev = logits.device
+    topk_w = torch.empty(T, topk, dtype=torch.float32, device=dev) if topk_w is None else topk_w
+    topk_ids = torch.empty(T, topk, dtype=torch.int32, device=dev) if topk_ids is None else topk_ids
+    _check(_lib.moe_topk_from_logits(_p(logits), T, E, topk, int(bool(renorm)), _p(topk_w), _p(topk_ids),
+                                     _stream(stream)), "moe_topk_from_logits")
+    return topk_w, topk_ids
+
+
+def moe_align(topk_ids: torch.Tensor, E: int, block: int, stream=None, with_counts: bool = True):
+    """(sorted_ids, expert_ids, num_post_pad[1], expert_counts) as full-capacity int32 device tensors."""
+    T, k = topk_ids.shape
+    cap, bcap = moe_align_capacity(T, k, E, block)
+    dev = topk_ids.device
+    sorted_ids = torch.empty(max(cap, 1), dtype=torch.int32, device=dev)
+    expert_ids = torch.empty(max(bcap, 1), dtype=torch.int32, device=dev)
+    npp = torch.zeros(4, dtype=torch.int32, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev) if with_counts else None
+    _check(_lib.moe_align(_p(topk_ids), T, k, E, block, _p(sorted_ids), _p(expert_ids), _p(npp), _p(counts),
+                          _stream(stream)), "moe_align")
+    return sorted_ids, expert_ids, npp[:1], counts
+
+
+def moe_forward(hidden: torch.Tensor, router_w: torch.Tensor, w13: torch.Tensor, w2: torch.Tensor, topk: int,
+                renorm: bool, w13_scale=None, w2_scale=None, out=None, workspace=None, options=None, stream=None):
+    """One fused MoE layer forward; returns out [T,H] in the activation dtype."""
+    T, H = hidden.shape
+    E, twoI, H2 = w13.shape
+    I = twoI // 2
+    if H2 != H or w2.shape != (E, H, I) or router_w.shape != (E, H):
+        raise ValueError("inconsistent shapes")
+    act, wdt = _dt(hidden), _dt(w13)
+    opts = _opts(options)
+    need = moe_workspace_size(T, H, I, E, topk, act, wdt, options)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=hidden.device)
+    out = torch.empty_like(hidden) if out is None else out
+    _check(_lib.moe_forward(_p(hidden), _p(router_w), _p(w13), _p(w2), T, H, I, E, topk, int(bool(renorm)), act, wdt,
+                            _p(w13_scale), _p(w2_scale), _p(out), _p(workspace), workspace.numel(), opts,
+                            _stream(stream)), "moe_forward")
+    return out
+
+
+def moe_get_status(stream=None) -> int:
+    return int(_lib.moe_get_status(_stream(stream)))

@@ -1,0 +1,436 @@
+// C ABI of the fused MoE layer forward: argument checks, workspace layout,
+// choice of kernels, and the launch sequence of one layer call.
+//
+// Declared in include/moe_api.h; every entry point is extern "C", takes plain
+// pointers and sizes, and enqueues work on the caller's stream.
+#include <algorithm>
+#include <mutex>
+
+#include "moe_device.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+// One status word per device: kernels record the first fault they see here
+// (MOE_ERR_DEVICE_TIMEOUT / MOE_ERR_DEVICE_INDEX); moe_get_status reads and
+// clears it.
+static __device__ int g_status_word;
+
+constexpr int kMaxDevices = 64;
+
+int* status_word() {
+  static int* ptr[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    ptr[dev] = static_cast<int*>(p);
+  }
+  return ptr[dev];
+}
+
+static int num_sms() {
+  static int sms[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  if (!sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+  return sms[dev];
+}
+
+// Target CTA count used to choose K splits.  A fixed constant (twice the 152
+// SMs of a GB300) so that the workspace size depends only on the arguments.
+constexpr int kSplitTargetCtas = 2 * 152;
+
+enum Path { PATH_F32 = 0, PATH_BF16 = 1, PATH_FP8 = 2 };
+
+struct Plan {
+  int path = 0;
+  bool swap = false;
+  int B = 16;
+  long cap = 0, nblk_cap = 0;
+  int xbox = 128;
+  int s1 = 1, kb1 = 1, s2 = 1, kb2 = 1;
+  int wbox2 = 128;  // token-major GEMM2 weight rows per load (N = 2 * wbox2)
+  bool y_bf16 = false;
+  size_t o_logits = 0, o_tw = 0, o_tid = 0, o_meta = 0, o_sorted = 0, o_eids = 0, o_xs = 0, o_aint = 0, o_af32 = 0,
+         o_p1 = 0, o_y = 0, o_misc = 0, total = 0;
+  size_t p1_stride = 0, y_stride = 0;
+};
+
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+static int choose_splits(long base_tiles, int kb_total, int forced) {
+  int s;
+  if (forced > 0) {
+    s = forced;
+  } else {
+    s = (int)((kSplitTargetCtas + base_tiles - 1) / std::max<long>(base_tiles, 1));
+    s = std::min(s, std::max(1, kb_total / 4));
+  }
+  s = std::max(1, std::min(s, kb_total));
+  return s;
+}
+
+static int check_shape(int T, int H, int I, int E, int topk) {
+  if (T < 0 || H < 1 || I < 1 || E < 1 || E > 1024 || topk < 1 || topk > E || topk > 32) return MOE_ERR_ARG;
+  const long long n = (long long)T * topk;
+  if (n + (long long)std::min<long long>(E, n) * 127 >= (1ll << 31)) return MOE_ERR_ARG;
+  return MOE_OK;
+}
+
+static int make_plan(int T, int H, int I, int E, int topk, moe_dtype act, moe_dtype w, const moe_options* opts,
+                     Plan* pl) {
+  int rc = check_shape(T, H, I, E, topk);
+  if (rc) return rc;
+  Plan p;
+  if (act == MOE_F32 && w == MOE_F32) {
+    p.path = PATH_F32;
+    if (H % 4) return MOE_ERR_UNSUPPORTED;
+  } else if (act == MOE_BF16 && w == MOE_BF16) {
+    p.path = PATH_BF16;
+  } else if (act == MOE_BF16 && w == MOE_E4M3) {
+    p.path = PATH_FP8;
+  } else {
+    return (act > MOE_E4M3 || w > MOE_E4M3 || act < 0 || w < 0) ? MOE_ERR_ARG : MOE_ERR_UNSUPPORTED;
+  }
+  const int orient = opts ? opts->orientation : MOE_ORIENT_AUTO;
+  if (orient < 0 || orient > 2) return MOE_ERR_ARG;
+  const long n = (long)T * topk;
+  if (p.path != PATH_F32) {
+    if (H % 128 || I % 128) return MOE_ERR_UNSUPPORTED;
+    p.swap = orient == MOE_ORIENT_SWAP_AB || (orient == MOE_ORIENT_AUTO && T <= 64);
+    if (p.swap && T > 256) return MOE_ERR_UNSUPPORTED;
+    const int eb = p.path == PATH_FP8 ? 1 : 2;
+    if (p.swap) {
+      p.B = 16;
+      p.xbox = std::max(16, (T + 15) / 16 * 16);
+      const long act_upper = std::min<long>(E, n);
+      const int forced = opts ? opts->split_k : 0;
+      if (forced < 0) return MOE_ERR_ARG;
+      const int kbt1 = H * eb / 128, kbt2 = I * eb / 128;
+      p.s1 = choose_splits(act_upper * (I / 64), kbt1, forced);
+      p.kb1 = (kbt1 + p.s1 - 1) / p.s1;
+      p.s1 = (kbt1 + p.kb1 - 1) / p.kb1;
+      p.s2 = choose_splits(act_upper * (H / 128), kbt2, forced);
+      p.kb2 = (kbt2 + p.s2 - 1) / p.s2;
+      p.s2 = (kbt2 + p.kb2 - 1) / p.kb2;
+      p.y_bf16 = false;
+    } else {
+      p.B = 128;
+      p.xbox = 128;
+      p.s1 = p.s2 = 1;
+      p.kb1 = H * eb / 128;
+      p.kb2 = I * eb / 128;
+      p.wbox2 = (H % 256 == 0) ? 128 : 64;
+      p.y_bf16 = true;
+    }
+  } else {
+    p.B = 16;
+    p.swap = false;
+  }
+  p.cap = n + std::min<long>(E, n) * (p.B - 1);
+  p.nblk_cap = p.cap / p.B;
+
+  const size_t A = 256;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align_up(o + std::max<size_t>(bytes, 1), A);
+    return at;
+  };
+  const size_t xb = p.path == PATH_F32 ? 4 : (p.path == PATH_BF16 ? 2 : 1);
+  p.o_logits = take((size_t)T * E * 4);
+  p.o_tw = take((size_t)n * 4);
+  p.o_tid = take((size_t)n * 4);
+  p.o_meta = take((size_t)meta_words(E) * 4);
+  p.o_sorted = take((size_t)p.cap * 4);
+  p.o_eids = take((size_t)std::max<long>(p.nblk_cap, 1) * 4);
+  p.o_xs = take((size_t)p.cap * H * xb);
+  p.o_aint = take((size_t)p.cap * I * xb);
+  if (p.path == PATH_FP8) p.o_af32 = take((size_t)p.cap * I * 4);
+  if (p.s1 > 1) {
+    p.p1_stride = (size_t)p.cap * 2 * I;
+    p.o_p1 = take(p.p1_stride * p.s1 * 4);
+  }
+  p.y_stride = (size_t)n * H;
+  p.o_y = take(p.y_stride * p.s2 * (p.y_bf16 ? 2 : 4));
+  p.o_misc = take(256);
+  p.total = o;
+  *pl = p;
+  return MOE_OK;
+}
+
+static bool misaligned(const void* p, uintptr_t a = 16) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; }
+
+static int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+static void record(moe_event_t ev, cudaStream_t s) {
+  if (ev) cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev), s);
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_strerror(int code) {
+  switch (code) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported dtype pair or shape";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait timed out";
+    case MOE_ERR_DEVICE_INDEX: return "expert id out of range";
+    case MOE_ERR_ALIGNMENT: return "device pointer not 16-byte aligned";
+    default: return "unknown error";
+  }
+}
+
+int moe_version(void) { return 100; }
+
+int moe_workspace_size(int T, int H, int I, int E, int topk, moe_dtype act_dtype, moe_dtype w_dtype,
+                       const moe_options* opts, size_t* bytes) {
+  if (!bytes) return MOE_ERR_ARG;
+  Plan p;
+  const int rc = make_plan(T, H, I, E, topk, act_dtype, w_dtype, opts, &p);
+  if (rc) return rc;
+  *bytes = p.total;
+  return MOE_OK;
+}
+
+int moe_align_capacity(int T, int topk, int E, int block, size_t* sorted_cap, size_t* blocks_cap) {
+  if (T < 0 || topk < 1 || E < 1 || block < 1 || !sorted_cap || !blocks_cap) return MOE_ERR_ARG;
+  const long long n = (long long)T * topk;
+  const long long cap = n + std::min<long long>(E, n) * (block - 1);
+  if (cap >= (1ll << 31)) return MOE_ERR_ARG;
+  *sorted_cap = (size_t)cap;
+  *blocks_cap = (size_t)(cap / block);
+  return MOE_OK;
+}
+
+int moe_route(const void* hidden, const void* router_w, int T, int H, int E, int topk, int renorm,
+              moe_dtype act_dtype, float* logits_out, float* topk_w, int32_t* topk_ids, moe_stream_t stream) {
+  if (T < 0 || H < 1 || E < 1 || E > 1024 || topk < 1 || topk > E || topk > 32) return MOE_ERR_ARG;
+  if (act_dtype != MOE_F32 && act_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!hidden || !router_w || !logits_out || !topk_w || !topk_ids) return MOE_ERR_ARG;
+  if (misaligned(hidden) || misaligned(router_w) || misaligned(logits_out) || misaligned(topk_w) ||
+      misaligned(topk_ids))
+    return MOE_ERR_ALIGNMENT;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_router_logits(hidden, router_w, T, H, E, act_dtype == MOE_BF16, logits_out, s);
+  if (e == cudaSuccess) e = launch_topk(logits_out, T, E, topk, renorm != 0, topk_w, topk_ids, s);
+  return cuda_rc(e);
+}
+
+int moe_topk_from_logits(const float* logits, int T, int E, int topk, int renorm, float* topk_w, int32_t* topk_ids,
+                         moe_stream_t stream) {
+  if (T < 0 || E < 1 || E > 1024 || topk < 1 || topk > E || topk > 32) return MOE_ERR_ARG;
+  if (T == 0) return MOE_OK;
+  if (!logits || !topk_w || !topk_ids) return MOE_ERR_ARG;
+  if (misaligned(logits) || misaligned(topk_w) || misaligned(topk_ids)) return MOE_ERR_ALIGNMENT;
+  return cuda_rc(launch_topk(logits, T, E, topk, renorm != 0, topk_w, topk_ids, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_align(const int32_t* topk_ids, int T, int topk, int E, int block, int32_t* sorted_ids, int32_t* expert_ids,
+              int32_t* num_post_pad, int32_t* expert_counts, moe_stream_t stream) {
+  if (T < 0 || topk < 1 || E < 1 || E > 1024 || block < 1 || block > 1024) return MOE_ERR_ARG;
+  size_t cap = 0, bcap = 0;
+  if (moe_align_capacity(T, topk, E, block, &cap, &bcap) != MOE_OK) return MOE_ERR_ARG;
+  if (T == 0) return MOE_OK;
+  if (!topk_ids || !sorted_ids || !expert_ids || !num_post_pad) return MOE_ERR_ARG;
+  if (misaligned(topk_ids) || misaligned(sorted_ids) || misaligned(expert_ids) || misaligned(num_post_pad) ||
+      (expert_counts && misaligned(expert_counts)))
+    return MOE_ERR_ALIGNMENT;
+  int* st = status_word();
+  if (!st) return MOE_ERR_CUDA;
+  return cuda_rc(launch_align(topk_ids, T, topk, E, block, sorted_ids, expert_ids, num_post_pad, expert_counts,
+                              nullptr, st, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_forward(const void* hidden, const void* router_w, const void* w13, const void* w2, int T, int H, int I, int E,
+                int topk, int renorm, moe_dtype act_dtype, moe_dtype w_dtype, const float* w13_scale,
+                const float* w2_scale, void* out, void* workspace, size_t workspace_bytes, const moe_options* opts,
+                moe_stream_t stream) {
+  Plan pl;
+  int rc = make_plan(T, H, I, E, topk, act_dtype, w_dtype, opts, &pl);
+  if (rc) return rc;
+  if (T == 0) return MOE_OK;
+  if (!hidden || !router_w || !w13 || !w2 || !out || !workspace) return MOE_ERR_ARG;
+  if (pl.path == PATH_FP8 && (!w13_scale || !w2_scale)) return MOE_ERR_ARG;
+  if (misaligned(hidden) || misaligned(router_w) || misaligned(w13) || misaligned(w2) || misaligned(out) ||
+      misaligned(workspace, 256) || (w13_scale && misaligned(w13_scale, 4)) || (w2_scale && misaligned(w2_scale, 4)))
+    return MOE_ERR_ALIGNMENT;
+  if (workspace_bytes < pl.total) return MOE_ERR_WORKSPACE;
+  int* st = status_word();
+  const int sms = num_sms();
+  if (!st || sms <= 0) return MOE_ERR_CUDA;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* logits = reinterpret_cast<float*>(ws + pl.o_logits);
+  float* tw = reinterpret_cast<float*>(ws + pl.o_tw);
+  int32_t* tid = reinterpret_cast<int32_t*>(ws + pl.o_tid);
+  int32_t* meta = reinterpret_cast<int32_t*>(ws + pl.o_meta);
+  int32_t* sorted = reinterpret_cast<int32_t*>(ws + pl.o_sorted);
+  int32_t* eids = reinterpret_cast<int32_t*>(ws + pl.o_eids);
+  void* xs = ws + pl.o_xs;
+  void* aint = ws + pl.o_aint;
+  float* af32 = reinterpret_cast<float*>(ws + pl.o_af32);
+  float* p1 = reinterpret_cast<float*>(ws + pl.o_p1);
+  void* y = ws + pl.o_y;
+  unsigned* amax = reinterpret_cast<unsigned*>(ws + pl.o_misc);  // [0] input amax, [1] intermediate amax
+  int* flag = reinterpret_cast<int*>(ws + pl.o_misc + 64);
+  const moe_options* o = opts;
+  const int cap = (int)pl.cap;
+  const int n = T * topk;
+  cudaError_t e = cudaSuccess;
+#define MOE_TRY(x)                 \
+  do {                             \
+    e = (x);                       \
+    if (e != cudaSuccess) return MOE_ERR_CUDA; \
+  } while (0)
+
+  if (o && o->inject_timeout) {
+    MOE_TRY(cudaMemsetAsync(flag, 0, sizeof(int), s));
+    MOE_TRY(launch_inject_timeout(flag, st, s));
+    return MOE_OK;
+  }
+
+  // 1-2. router
+  if (o) record(o->stage_begin[MOE_STAGE_ROUTE], s);
+  MOE_TRY(launch_router_logits(hidden, router_w, T, H, E, act_dtype == MOE_BF16, logits, s));
+  MOE_TRY(launch_topk(logits, T, E, topk, renorm != 0, tw, tid, s));
+  if (o) record(o->stage_end[MOE_STAGE_ROUTE], s);
+
+  // 3. permutation
+  if (o) record(o->stage_begin[MOE_STAGE_ALIGN], s);
+  MOE_TRY(launch_align(tid, T, topk, E, pl.B, sorted, eids, meta + META_NPP, nullptr, meta, st, s));
+  if (o) record(o->stage_end[MOE_STAGE_ALIGN], s);
+
+  // 4. gather (+ FP8 input quantisation)
+  if (o) record(o->stage_begin[MOE_STAGE_GATHER], s);
+  if (pl.path == PATH_FP8) {
+    MOE_TRY(cudaMemsetAsync(amax, 0, 2 * sizeof(unsigned), s));
+    MOE_TRY(launch_amax_bf16(hidden, (size_t)T * H, amax, s));
+    MOE_TRY(launch_gather(hidden, T, H, topk, 2, 1, amax, sorted, meta, cap, xs, s));
+  } else {
+    MOE_TRY(launch_gather(hidden, T, H, topk, pl.path == PATH_F32 ? 4 : 2, 0, nullptr, sorted, meta, cap, xs, s));
+  }
+  if (o) record(o->stage_end[MOE_STAGE_GATHER], s);
+
+  if (pl.path == PATH_F32) {
+    if (o) record(o->stage_begin[MOE_STAGE_GEMM1], s);
+    MOE_TRY(launch_gemm1_simt((const float*)xs, (const float*)w13, H, I, pl.B, eids, meta, cap, (float*)aint, s));
+    if (o) record(o->stage_end[MOE_STAGE_GEMM1], s);
+    if (o) record(o->stage_begin[MOE_STAGE_ACT], s);
+    if (o) record(o->stage_end[MOE_STAGE_ACT], s);
+    if (o) record(o->stage_begin[MOE_STAGE_GEMM2], s);
+    MOE_TRY(launch_gemm2_simt((const float*)aint, (const float*)w2, H, I, pl.B, T, topk, sorted, eids, meta, cap,
+                              (float*)y, s));
+    if (o) record(o->stage_end[MOE_STAGE_GEMM2], s);
+  } else {
+    const bool fp8 = pl.path == PATH_FP8;
+    TcGemmArgs g = {};
+    g.swap = pl.swap;
+    g.fp8 = fp8;
+    g.T = T;
+    g.k = topk;
+    g.E = E;
+    g.I = I;
+    g.H = H;
+    g.cap = cap;
+    g.sorted = sorted;
+    g.eids = eids;
+    g.meta = meta;
+    g.status = st;
+    g.num_sms = sms;
+
+    // 5. GEMM1 on w13 (+ SiLU(gate)*up)
+    TcGemmArgs g1 = g;
+    g1.K = H;
+    g1.W = w13;
+    g1.X = xs;
+    g1.w_rows_per_expert = 2 * I;
+    g1.w_pair_off = I;
+    g1.wbox = pl.swap ? 64 : 128;
+    g1.w_tile_rows = g1.wbox;
+    g1.xbox = pl.xbox;
+    g1.n_tiles = I / g1.wbox;
+    g1.splits = pl.s1;
+    g1.kb_per_split = pl.kb1;
+    g1.w_scale = w13_scale;
+    g1.a_amax = amax;
+    g1.amax_out = amax + 1;
+    if (pl.s1 > 1) {
+      g1.epi = TC_EPI_G1_PART;
+      g1.out = p1;
+      g1.out_split_stride = pl.p1_stride;
+    } else {
+      g1.epi = fp8 ? TC_EPI_G1_F32AMAX : TC_EPI_G1_BF16;
+      g1.out = fp8 ? (void*)af32 : aint;
+    }
+    if (o) record(o->stage_begin[MOE_STAGE_GEMM1], s);
+    MOE_TRY(launch_gemm_tc(g1, s));
+    if (o) record(o->stage_end[MOE_STAGE_GEMM1], s);
+
+    // split-K reduction / FP8 quantisation of the intermediate
+    if (o) record(o->stage_begin[MOE_STAGE_ACT], s);
+    if (pl.s1 > 1)
+      MOE_TRY(launch_reduce_act(p1, pl.s1, pl.p1_stride, I, pl.B, eids, meta, cap, fp8 ? w13_scale : nullptr, amax,
+                                fp8 ? 1 : 0, fp8 ? (void*)af32 : aint, amax + 1, s));
+    if (fp8) MOE_TRY(launch_quant_act(af32, I, meta, cap, amax + 1, (uint8_t*)aint, s));
+    if (o) record(o->stage_end[MOE_STAGE_ACT], s);
+
+    // 6. GEMM2 on w2
+    TcGemmArgs g2 = g;
+    g2.K = I;
+    g2.W = w2;
+    g2.X = aint;
+    g2.w_rows_per_expert = H;
+    g2.wbox = pl.swap ? 64 : pl.wbox2;
+    g2.w_pair_off = g2.wbox;
+    g2.w_tile_rows = 2 * g2.wbox;
+    g2.xbox = pl.xbox;
+    g2.n_tiles = H / g2.w_tile_rows;
+    g2.splits = pl.s2;
+    g2.kb_per_split = pl.kb2;
+    g2.w_scale = w2_scale;
+    g2.a_amax = amax + 1;
+    g2.out = y;
+    g2.out_split_stride = pl.y_stride;
+    g2.epi = pl.y_bf16 ? TC_EPI_G2_BF16 : TC_EPI_G2_F32;
+    if (o) record(o->stage_begin[MOE_STAGE_GEMM2], s);
+    MOE_TRY(launch_gemm_tc(g2, s));
+    if (o) record(o->stage_end[MOE_STAGE_GEMM2], s);
+  }
+
+  // 7. combine
+  if (o) record(o->stage_begin[MOE_STAGE_COMBINE], s);
+  MOE_TRY(launch_combine(y, pl.y_bf16 ? 1 : 0, pl.s2, pl.y_stride, tw, T, topk, H, out, act_dtype == MOE_BF16 ? 1 : 0,
+                         s));
+  if (o) record(o->stage_end[MOE_STAGE_COMBINE], s);
+#undef MOE_TRY
+  (void)n;
+  return MOE_OK;
+}
+
+int moe_get_status(moe_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  int* st = status_word();
+  if (!st) return MOE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, st, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(st, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return v;
+}
+
+}  // extern "C"

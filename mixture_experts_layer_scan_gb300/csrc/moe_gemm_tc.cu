@@ -1,0 +1,522 @@
+// Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05, sm_103a).
+//
+// One persistent kernel covers every active expert of the layer in a single
+// launch ("Mixture-of-Experts kernel engineering on Amazon SageMaker AI",
+// intro: routing, data shuffle and expert networks as one batched GPU
+// operation; "FusedMoE vs MegaMoE", section 3.2: the fused kernel must keep
+// every SM busy although experts receive different token counts).
+//
+// Roles (192 threads):
+//   warp 0      TMA producer: weight tile + sorted activation tile per
+//               128-byte K block into a ring of shared-memory stages
+//   warp 1      MMA issuer: tcgen05.mma into a tensor-memory accumulator
+//               (two accumulators, so the epilogue of one tile overlaps the
+//               main loop of the next)
+//   warps 2-5   epilogue: tcgen05.ld -> registers -> scale / SiLU(gate)*up ->
+//               global stores
+//
+// Orientation.  In swap-AB mode (thin decode batches) the MMA computes
+// C^T[N,M] = B^T[N,K] A^T[K,M]: 128 expert weight rows occupy the M slot and
+// the expert's few tokens (padded to 16) the N slot, so no tensor-core row is
+// spent on empty token rows (page 1, section "Swap-AB pour l'utilisation de
+// WGMMA", Figure 1: the large expert N dimension moved into the fixed-size
+// operand slot; Hopper's slot is 64 rows, tcgen05's is 128).  In token-major
+// mode (prefill) 128 sorted token rows fill M and 256 weight rows N.
+//
+// The weight tile is two TMA loads of `wbox` rows.  For GEMM1 they are the
+// gate rows and the matching up rows, so SiLU(gate)*up pairs values of one
+// tile: in token-major mode inside one thread (columns c and wbox+c), in
+// swap-AB mode across TMEM lanes i and 64+i through shared memory.
+#include <mutex>
+
+#include "moe_device.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kTcThreads = 192;
+constexpr int kMaxStages = 8;
+constexpr int kXchgStride = 17;                           // floats per exchange row (16 + 1 pad)
+constexpr uint32_t kXchgBytes = 2 * 64 * kXchgStride * 4; // double-buffered 64 x 16 fp32
+constexpr uint32_t kTmemCols = 512;                       // two 256-column accumulators
+
+struct TcDev {
+  int epi;
+  int T, k, E, I, H;
+  int kb_total, kb_per_split, splits, n_tiles;
+  int w_rows_per_expert, w_pair_off, w_tile_rows, wbox, xbox;
+  int stages;
+  uint32_t stage_bytes, w_bytes, xchg_off, bar_off;
+  const int32_t* sorted;
+  const int32_t* eids;
+  const int32_t* meta;
+  void* out;
+  size_t out_split_stride;
+  const float* w_scale;
+  const unsigned* a_amax;
+  unsigned* amax_out;
+  int* status;
+};
+
+struct Tile {
+  int e, xrow, ntok, npad, wr0, kb0, kb1, n, s;
+};
+
+template <bool SWAP>
+__device__ __forceinline__ int tile_count(const TcDev& p) {
+  if constexpr (SWAP)
+    return p.meta[META_NACT] * p.n_tiles * p.splits;
+  else
+    return (p.meta[META_NPP] / 128) * p.n_tiles;
+}
+
+template <bool SWAP>
+__device__ __forceinline__ Tile tile_at(const TcDev& p, int t) {
+  Tile d;
+  if constexpr (SWAP) {
+    const int per_e = p.n_tiles * p.splits;
+    const int a = t / per_e;
+    const int rem = t - a * per_e;
+    d.n = rem / p.splits;
+    d.s = rem - d.n * p.splits;
+    d.e = p.meta[meta_active(p.E) + a];
+    d.xrow = p.meta[meta_offsets(p.E) + d.e];
+    d.ntok = p.meta[meta_counts(p.E) + d.e];
+    d.npad = (d.ntok + 15) & ~15;
+    d.kb0 = d.s * p.kb_per_split;
+    d.kb1 = min(d.kb0 + p.kb_per_split, p.kb_total);
+  } else {
+    const int m = t / p.n_tiles;
+    d.n = t - m * p.n_tiles;
+    d.s = 0;
+    d.e = p.eids[m];
+    d.xrow = m * 128;
+    d.ntok = 128;
+    d.npad = 128;
+    d.kb0 = 0;
+    d.kb1 = p.kb_total;
+  }
+  d.wr0 = d.e * p.w_rows_per_expert + d.n * p.w_tile_rows;
+  return d;
+}
+
+// OR of a flag over the 128 epilogue threads (named barrier 1).
+__device__ __forceinline__ bool epi_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\tbar.red.or.pred po, 1, 128, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+
+template <bool SWAP, bool FP8, int EPI>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const TcDev p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar_full = sbase + p.bar_off;
+  const uint32_t bar_empty = bar_full + 8 * kMaxStages;
+  const uint32_t bar_tfull = bar_empty + 8 * kMaxStages;
+  const uint32_t bar_tempty = bar_tfull + 16;
+  const uint32_t bar_drain = bar_tempty + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + p.bar_off + 8 * (2 * kMaxStages + 5));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* xchg = reinterpret_cast<float*>(smem + p.xchg_off);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_tfull + 8 * b, 1);
+      mbar_init(bar_tempty + 8 * b, 128);
+    }
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  // Everything below reads the routing results of the preceding kernels.
+  pdl_wait();
+  const int ntiles = tile_count<SWAP>(p);
+  constexpr int KBLK = FP8 ? 128 : 64;  // elements per 128-byte K block
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      int stage = 0;
+      uint32_t phase = 0, issued = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        const Tile d = tile_at<SWAP>(p, t);
+        for (int kb = d.kb0; kb < d.kb1; ++kb) {
+          if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sw = sbase + stage * p.stage_bytes;
+          const uint32_t fb = bar_full + 8 * stage;
+          mbar_arrive_expect_tx(fb, p.stage_bytes);
+          tma_load_2d(sw, &tmW, kb * KBLK, d.wr0, fb);
+          tma_load_2d(sw + p.wbox * 128, &tmW, kb * KBLK, d.wr0 + p.w_pair_off, fb);
+          tma_load_2d(sw + p.w_bytes, &tmX, kb * KBLK, d.xrow, fb);
+          ++issued;
+          if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {  // let the copies already in flight land before the CTA exits
+        const uint32_t first = issued > (uint32_t)p.stages ? issued - p.stages : 0u;
+        for (uint32_t i = first; i < issued; ++i)
+          mbar_wait_drain(bar_full + 8 * (i % p.stages), (i / p.stages) & 1u, 100000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true, any = false;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        const Tile d = tile_at<SWAP>(p, t);
+        const int N = SWAP ? d.npad : 2 * p.wbox;
+        const uint32_t idesc = idesc_make(128, N, FP8);
+        if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t dt = tmem_base + (uint32_t)acc * 256u;
+        for (int kb = d.kb0; kb < d.kb1; ++kb) {
+          if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sw = sbase + stage * p.stage_bytes;
+          const uint32_t sx = sw + p.w_bytes;
+          const uint32_t a_base = SWAP ? sw : sx;
+          const uint32_t b_base = SWAP ? sx : sw;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma<FP8>(dt, sdesc_k_sw128(a_base + kk * 32), sdesc_k_sw128(b_base + kk * 32), idesc,
+                        (kb > d.kb0 || kk > 0) ? 1u : 0u);
+          tc_commit(bar_empty + 8 * stage);
+          any = true;
+          if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(bar_tfull + 8 * acc);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok && any) {  // the tensor core must be idle before tensor memory is freed
+        tc_commit(bar_drain);
+        mbar_wait_drain(bar_drain, 0, 100000000ull);
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int q = warp & 3;        // tensor-memory lane quadrant this warp may read
+    const int lrow = q * 32 + lane; // accumulator row of this thread
+    float a_scale = 1.0f;
+    if constexpr (FP8) a_scale = e4m3_scale_from_amax(__uint_as_float(*p.a_amax));
+    float amax = 0.0f;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    const int n_pairs = p.T * p.k;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+      const Tile d = tile_at<SWAP>(p, t);
+      const bool ok = mbar_wait(bar_tfull + 8 * acc, acc_phase, abort_flag, p.status);
+      if (epi_any(!ok)) break;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * 256u;
+      const float scale = FP8 ? a_scale * p.w_scale[d.e] : 1.0f;
+
+      if constexpr (SWAP && (EPI == TC_EPI_G1_BF16 || EPI == TC_EPI_G1_F32AMAX)) {
+        // lanes 0..63: gate of column i = n*64 + lrow; lanes 64..127: up of i = n*64 + lrow - 64
+        const bool is_up = lrow >= 64;
+        const int il = is_up ? lrow - 64 : lrow;
+        const int i = d.n * 64 + il;
+        for (int c0 = 0, buf = 0; c0 < d.npad; c0 += 16, buf ^= 1) {
+          float v[16];
+          tmem_ld16(tb + (uint32_t)c0, v);
+          float* xb = xchg + (buf * 64 + il) * kXchgStride;
+          if (is_up) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) xb[j] = v[j];
+          }
+          named_bar_sync(1, 128);
+          if (!is_up) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int c = c0 + j;
+              if (c < d.ntok) {
+                const float a = silu(v[j] * scale) * (xb[j] * scale);
+                const size_t o = (size_t)(d.xrow + c) * p.I + i;
+                if constexpr (EPI == TC_EPI_G1_BF16) {
+                  reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(a);
+                } else {
+                  reinterpret_cast<float*>(p.out)[o] = a;
+                  amax = fmaxf(amax, fabsf(a));
+                }
+              }
+            }
+          }
+        }
+        named_bar_sync(1, 128);  // exchange buffers free for the next tile
+      } else if constexpr (SWAP && EPI == TC_EPI_G1_PART) {
+        // raw fp32 split partial: P[s][row][col], col = i (gate) or I + i (up)
+        const int col = (lrow < 64) ? d.n * 64 + lrow : p.I + d.n * 64 + (lrow - 64);
+        float* P = reinterpret_cast<float*>(p.out) + (size_t)d.s * p.out_split_stride;
+        for (int c0 = 0; c0 < d.npad; c0 += 16) {
+          float v[16];
+          tmem_ld16(tb + (uint32_t)c0, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (c0 + j < d.ntok) P[(size_t)(d.xrow + c0 + j) * (2 * p.I) + col] = v[j];
+        }
+      } else if constexpr (SWAP && EPI == TC_EPI_G2_F32) {
+        // Y[s][pair][h], h = n*128 + lrow, pair = sorted[xrow + c]
+        const int h = d.n * 128 + lrow;
+        float* Y = reinterpret_cast<float*>(p.out) + (size_t)d.s * p.out_split_stride;
+        for (int c0 = 0; c0 < d.npad; c0 += 16) {
+          float v[16];
+          tmem_ld16(tb + (uint32_t)c0, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int c = c0 + j;
+            if (c < d.ntok) {
+              const int f = p.sorted[d.xrow + c];
+              if (f < n_pairs) Y[(size_t)f * p.H + h] = v[j] * scale;
+            }
+          }
+        }
+      } else if constexpr (!SWAP && (EPI == TC_EPI_G1_BF16 || EPI == TC_EPI_G1_F32AMAX)) {
+        // row = xrow + lrow; columns [0, wbox) gate, [wbox, 2 wbox) up of i = n*wbox + c
+        const size_t row = (size_t)(d.xrow + lrow);
+        for (int c0 = 0; c0 < p.wbox; c0 += 16) {
+          float g[16], u[16];
+          tmem_ld16(tb + (uint32_t)c0, g);
+          tmem_ld16(tb + (uint32_t)(p.wbox + c0), u);
+          float a[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) a[j] = silu(g[j] * scale) * (u[j] * scale);
+          const size_t o = row * p.I + (size_t)d.n * p.wbox + c0;
+          if constexpr (EPI == TC_EPI_G1_BF16) {
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + o);
+            dst[0] = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
+                                pack_bf16x2(a[6], a[7]));
+            dst[1] = make_uint4(pack_bf16x2(a[8], a[9]), pack_bf16x2(a[10], a[11]), pack_bf16x2(a[12], a[13]),
+                                pack_bf16x2(a[14], a[15]));
+          } else {
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + o);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) dst[j] = make_float4(a[4 * j], a[4 * j + 1], a[4 * j + 2], a[4 * j + 3]);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(a[j]));
+          }
+        }
+      } else if constexpr (!SWAP && (EPI == TC_EPI_G2_BF16 || EPI == TC_EPI_G2_F32)) {
+        const int f = p.sorted[d.xrow + lrow];
+        const int ncols = 2 * p.wbox;
+        for (int c0 = 0; c0 < ncols; c0 += 16) {
+          float v[16];
+          tmem_ld16(tb + (uint32_t)c0, v);
+          if (f < n_pairs) {
+            const size_t o = (size_t)f * p.H + (size_t)d.n * ncols + c0;
+            if constexpr (EPI == TC_EPI_G2_BF16) {
+              uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + o);
+              dst[0] = make_uint4(pack_bf16x2(v[0] * scale, v[1] * scale), pack_bf16x2(v[2] * scale, v[3] * scale),
+                                  pack_bf16x2(v[4] * scale, v[5] * scale), pack_bf16x2(v[6] * scale, v[7] * scale));
+              dst[1] =
+                  make_uint4(pack_bf16x2(v[8] * scale, v[9] * scale), pack_bf16x2(v[10] * scale, v[11] * scale),
+                             pack_bf16x2(v[12] * scale, v[13] * scale), pack_bf16x2(v[14] * scale, v[15] * scale));
+            } else {
+              float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + o);
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                dst[j] = make_float4(v[4 * j] * scale, v[4 * j + 1] * scale, v[4 * j + 2] * scale,
+                                     v[4 * j + 3] * scale);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar_tempty + 8 * acc);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if constexpr (EPI == TC_EPI_G1_F32AMAX) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+      if (lane == 0 && amax > 0.0f) atomicMax(p.amax_out, __float_as_uint(amax));
+    }
+  }
+
+  pdl_launch_dependents();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D K-major tensor [rows][K] of 1- or 2-byte elements, box = 128 bytes of K x box_rows, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int elem_bytes, uint64_t K, uint64_t rows, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {K, rows};
+  const cuuint64_t strides[1] = {K * (uint64_t)elem_bytes};
+  const cuuint32_t box[2] = {(cuuint32_t)(128 / elem_bytes), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType dt = elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool SWAP, bool FP8, int EPI>
+cudaError_t launch_inst(const CUtensorMap& mw, const CUtensorMap& mx, const TcDev& p, int grid, size_t smem,
+                        cudaStream_t s) {
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  auto kern = k_gemm_tc<SWAP, FP8, EPI>;
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, mw, mx, p);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s) {
+  const int eb = a.fp8 ? 1 : 2;
+  CUtensorMap mw, mx;
+  if (!make_map(&mw, a.W, eb, (uint64_t)a.K, (uint64_t)a.E * a.w_rows_per_expert, (uint32_t)a.wbox))
+    return cudaErrorInvalidValue;
+  if (!make_map(&mx, a.X, eb, (uint64_t)a.K, (uint64_t)a.cap, (uint32_t)a.xbox)) return cudaErrorInvalidValue;
+
+  TcDev p = {};
+  p.epi = a.epi;
+  p.T = a.T;
+  p.k = a.k;
+  p.E = a.E;
+  p.I = a.I;
+  p.H = a.H;
+  p.kb_total = a.K * eb / 128;
+  p.kb_per_split = a.kb_per_split;
+  p.splits = a.splits;
+  p.n_tiles = a.n_tiles;
+  p.w_rows_per_expert = a.w_rows_per_expert;
+  p.w_pair_off = a.w_pair_off;
+  p.w_tile_rows = a.w_tile_rows;
+  p.wbox = a.wbox;
+  p.xbox = a.xbox;
+  p.sorted = a.sorted;
+  p.eids = a.eids;
+  p.meta = a.meta;
+  p.out = a.out;
+  p.out_split_stride = a.out_split_stride;
+  p.w_scale = a.w_scale;
+  p.a_amax = a.a_amax;
+  p.amax_out = a.amax_out;
+  p.status = a.status;
+
+  const bool xchg = a.swap && (a.epi == TC_EPI_G1_BF16 || a.epi == TC_EPI_G1_F32AMAX);
+  p.w_bytes = (uint32_t)(2 * a.wbox * 128);
+  p.stage_bytes = p.w_bytes + (uint32_t)(a.xbox * 128);
+  const uint32_t bar_bytes = 8 * (2 * kMaxStages + 5) + 16;
+  const uint32_t budget = 227 * 1024 - 1024 - (xchg ? kXchgBytes : 0) - bar_bytes;
+  int stages = (int)(budget / p.stage_bytes);
+  if (stages > kMaxStages) stages = kMaxStages;
+  if (stages < 2) return cudaErrorInvalidValue;
+  p.stages = stages;
+  p.xchg_off = (uint32_t)stages * p.stage_bytes;
+  p.bar_off = p.xchg_off + (xchg ? kXchgBytes : 0);
+  const size_t smem = 1024 + (size_t)p.bar_off + bar_bytes;
+
+  long upper;
+  if (a.swap)
+    upper = (long)std::min(a.E, a.T * a.k) * a.n_tiles * a.splits;
+  else
+    upper = (long)(a.cap / 128) * a.n_tiles;
+  int grid = (int)std::min<long>(upper, a.num_sms);
+  if (grid < 1) grid = 1;
+
+#define MOE_TC_CASE(SW, F8, EP)                      \
+  if (a.swap == SW && a.fp8 == F8 && a.epi == EP) \
+    return launch_inst<SW, F8, EP>(mw, mx, p, grid, smem, s);
+  MOE_TC_CASE(true, false, TC_EPI_G1_BF16)
+  MOE_TC_CASE(true, false, TC_EPI_G1_PART)
+  MOE_TC_CASE(true, false, TC_EPI_G2_F32)
+  MOE_TC_CASE(true, true, TC_EPI_G1_F32AMAX)
+  MOE_TC_CASE(true, true, TC_EPI_G1_PART)
+  MOE_TC_CASE(true, true, TC_EPI_G2_F32)
+  MOE_TC_CASE(false, false, TC_EPI_G1_BF16)
+  MOE_TC_CASE(false, false, TC_EPI_G2_BF16)
+  MOE_TC_CASE(false, true, TC_EPI_G1_F32AMAX)
+  MOE_TC_CASE(false, true, TC_EPI_G2_BF16)
+#undef MOE_TC_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

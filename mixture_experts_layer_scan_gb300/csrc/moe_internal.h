@@ -1,0 +1,103 @@
+// Internal host-side interface between the C ABI layer and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "moe_api.h"
+
+namespace moe {
+
+// Per-call routing metadata written by the permutation kernel (int32 words):
+//   [0] num_post_pad  [1] number of blocks  [2] number of active experts  [3] unused
+//   [4, 4+E)          active experts, ascending
+//   [4+E, 5+2E)       padded start offset of every expert (E+1 entries, last = num_post_pad)
+//   [5+2E, 5+3E)      tokens per expert
+enum { META_NPP = 0, META_NBLK = 1, META_NACT = 2, META_HDR = 4 };
+inline int meta_words(int E) { return META_HDR + 3 * E + 1; }
+__host__ __device__ inline int meta_active(int E) { (void)E; return META_HDR; }
+__host__ __device__ inline int meta_offsets(int E) { return META_HDR + E; }
+__host__ __device__ inline int meta_counts(int E) { return META_HDR + 2 * E + 1; }
+
+// ---- routing ----------------------------------------------------------------
+cudaError_t launch_router_logits(const void* X, const void* Wr, int T, int H, int E, bool bf16, float* logits,
+                                 cudaStream_t s);
+cudaError_t launch_topk(const float* logits, int T, int E, int k, int renorm, float* w, int32_t* ids,
+                        cudaStream_t s);
+cudaError_t launch_inject_timeout(const int* flag, int* status, cudaStream_t s);
+
+// ---- permutation / data movement ----------------------------------------------
+cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int B, int32_t* sorted, int32_t* eids,
+                         int32_t* npp, int32_t* counts, int32_t* meta, int* status, cudaStream_t s);
+// amax over n bf16 values -> *amax_bits (float bits, must be zeroed before)
+cudaError_t launch_amax_bf16(const void* X, size_t n, unsigned* amax_bits, cudaStream_t s);
+// Xs[r] = X[sorted[r]/k] (zero rows for the sentinel) for r < num_post_pad;
+// mode 0: copy elements of elem_bytes; mode 1: bf16 -> e4m3 with scale amax/448
+cudaError_t launch_gather(const void* X, int T, int H, int k, int elem_bytes, int mode, const unsigned* amax_bits,
+                          const int32_t* sorted, const int32_t* meta, int cap, void* Xs, cudaStream_t s);
+// split-K reduction of the GEMM1 partials + scale + SiLU(gate)*up.
+//   out_mode 0: bf16 A_int   1: fp32 A (+ amax into amax_bits)
+cudaError_t launch_reduce_act(const float* P, int splits, size_t split_stride, int I, int B, const int32_t* eids,
+                              const int32_t* meta, int cap, const float* w_scale, const unsigned* a_amax_bits,
+                              int out_mode, void* A_out, unsigned* amax_bits, cudaStream_t s);
+// A_q[r][i] = e4m3(A[r][i] / (amax/448)) for r < num_post_pad
+cudaError_t launch_quant_act(const float* A, int I, const int32_t* meta, int cap, const unsigned* amax_bits,
+                             uint8_t* Aq, cudaStream_t s);
+// out[t] = sum_j w[t][j] * sum_s Y[s][t*k+j]   (Y fp32 or bf16, out fp32 or bf16)
+cudaError_t launch_combine(const void* Y, int y_bf16, int splits, size_t split_stride, const float* w, int T, int k,
+                           int H, void* out, int out_bf16, cudaStream_t s);
+
+// ---- fp32 CUDA-core grouped GEMMs ---------------------------------------------
+cudaError_t launch_gemm1_simt(const float* Xs, const float* W13, int H, int I, int B, const int32_t* eids,
+                              const int32_t* meta, int cap, float* A, cudaStream_t s);
+cudaError_t launch_gemm2_simt(const float* A, const float* W2, int H, int I, int B, int T, int k,
+                              const int32_t* sorted, const int32_t* eids, const int32_t* meta, int cap, float* Y,
+                              cudaStream_t s);
+
+// ---- tcgen05 grouped GEMM --------------------------------------------------------
+enum TcEpilogue {
+  TC_EPI_G1_BF16 = 0,    // GEMM1: SiLU(gate)*up -> bf16 A_int
+  TC_EPI_G1_PART = 1,    // GEMM1: raw fp32 partials [split][row][2I] (gate cols [0,I), up [I,2I))
+  TC_EPI_G1_F32AMAX = 2, // GEMM1: scaled SiLU(gate)*up -> fp32 A + amax (FP8 path)
+  TC_EPI_G2_F32 = 3,     // GEMM2: fp32 Y[split][pair][H]
+  TC_EPI_G2_BF16 = 4     // GEMM2: bf16 Y[pair][H]
+};
+
+struct TcGemmArgs {
+  bool swap;        // swap-AB orientation (weights in the M slot)
+  bool fp8;         // e4m3 operands (kind::f8f6f4), else bf16 (kind::f16)
+  int epi;          // TcEpilogue
+  // problem
+  int T, k, E, I, H;
+  int K;            // reduction length in elements
+  int w_rows_per_expert;
+  int w_pair_off;   // row offset of the second weight load from the first
+  int w_tile_rows;  // weight rows advanced per output tile
+  int wbox;         // rows per weight load (tile = two loads)
+  int xbox;         // token rows per activation load
+  int n_tiles;      // output tiles per expert (or per 128-row block)
+  int splits;       // K splits (swap mode)
+  int kb_per_split; // k-blocks (128 bytes of K) per split
+  int cap;          // rows of the sorted activation buffer
+  // tensors
+  const void* W;    // weights viewed as [E * w_rows_per_expert][K]
+  const void* X;    // sorted activations [cap][K]
+  const int32_t* sorted;
+  const int32_t* eids;
+  const int32_t* meta;
+  void* out;
+  size_t out_split_stride;  // elements between split partial buffers
+  const float* w_scale;     // [E] (FP8)
+  const unsigned* a_amax;   // amax bits of the activation operand (FP8)
+  unsigned* amax_out;       // amax bits of the produced intermediate (FP8 GEMM1)
+  int* status;
+  int num_sms;
+};
+cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s);
+
+// status word of the current device
+int* status_word();
+
+}  // namespace moe

@@ -1,0 +1,420 @@
+// Token-to-expert permutation, activation gather, split-K / FP8 activation
+// passes and the routing-weighted combine.
+//
+// "FusedMoE vs MegaMoE" (zwxr.cn), section 2.3: routing scatters the tokens
+// of a batch to experts and the results must be put back in token order;
+// section 3.1: the fused design sorts tokens by expert, builds an index of
+// which rows belong to which expert, computes, then reorders and sums the
+// results with the routing weights.
+#include "moe_device.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kAlignThreads = 1024;
+constexpr int kAlignWarps = kAlignThreads / 32;
+
+// Exclusive scan over blockDim.x (= 1024) values, one per thread; returns the
+// exclusive prefix of the caller and writes the block total to *total.
+__device__ int block_exclusive_scan(int v, int* scratch /* >= 33 ints */, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += n;
+  }
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = (lane < (int)(blockDim.x >> 5)) ? scratch[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, wi, off);
+      if (lane >= off) wi += n;
+    }
+    scratch[lane] = wi - w;  // exclusive prefix of each warp
+    if (lane == 31) scratch[32] = wi;
+  }
+  __syncthreads();
+  const int res = scratch[warp] + incl - v;
+  *total = scratch[32];
+  __syncthreads();
+  return res;
+}
+
+// One CTA of 1024 threads.  Warp w owns the contiguous chunk of flat pair
+// indices [w*L, (w+1)*L).  Pass 1 counts, per warp and expert, with warp
+// match (no atomics, so the counts do not depend on timing); the per-expert
+// prefix over warps then gives every warp its first slot, so pass 2 writes
+// each pair at a position that preserves ascending flat index inside an
+// expert (a stable counting sort).
+__global__ void __launch_bounds__(kAlignThreads, 1)
+    k_align(const int32_t* __restrict__ ids, int T, int k, int E, int B, int32_t* __restrict__ sorted,
+            int32_t* __restrict__ eids, int32_t* __restrict__ npp_out, int32_t* __restrict__ counts_out,
+            int32_t* __restrict__ meta, int* status) {
+  extern __shared__ int sm[];
+  int* wc = sm;                       // [kAlignWarps][E] per-warp counts, then per-warp bases
+  int* off = wc + kAlignWarps * E;    // [E+1] padded offsets
+  int* cnt = off + E + 1;             // [E]
+  int* scan_tmp = cnt + E;            // [33]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int n = T * k;
+  const int L = (n + kAlignWarps - 1) / kAlignWarps;
+  const int beg = min(n, warp * L), end = min(n, beg + L);
+
+  for (int i = threadIdx.x; i < kAlignWarps * E; i += blockDim.x) wc[i] = 0;
+  __syncthreads();
+
+  // pass 1: per-warp histogram
+  bool bad = false;
+  for (int base = beg; base < end; base += 32) {
+    const int f = base + lane;
+    int e = -1;
+    if (f < end) {
+      e = ids[f];
+      if (e < 0 || e >= E) { bad = true; e = -1; }
+    }
+    const unsigned grp = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && lane == __ffs(grp) - 1) wc[warp * E + e] += __popc(grp);
+    __syncwarp();
+  }
+  if (bad) report(status, MOE_ERR_DEVICE_INDEX);
+  __syncthreads();
+
+  // per-expert totals and per-warp bases (exclusive over warps)
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int w = 0; w < kAlignWarps; ++w) {
+      const int c = wc[w * E + e];
+      wc[w * E + e] = run;
+      run += c;
+    }
+    cnt[e] = run;
+  }
+  __syncthreads();
+
+  // padded offsets and active list (E <= 1024 = blockDim)
+  {
+    const int e = threadIdx.x;
+    const int c = (e < E) ? cnt[e] : 0;
+    const int padded = (c + B - 1) / B * B;
+    int total_pad = 0, total_act = 0;
+    const int o = block_exclusive_scan(padded, scan_tmp, &total_pad);
+    const int a = block_exclusive_scan(c > 0 ? 1 : 0, scan_tmp, &total_act);
+    if (e < E) {
+      off[e] = o;
+      if (meta) {
+        meta[meta_offsets(E) + e] = o;
+        meta[meta_counts(E) + e] = c;
+        if (c > 0) meta[meta_active(E) + a] = e;
+      }
+      if (counts_out) counts_out[e] = c;
+    }
+    if (e == 0) {
+      off[E] = total_pad;
+      *npp_out = total_pad;
+      if (meta) {
+        meta[META_NPP] = total_pad;
+        meta[META_NBLK] = total_pad / B;
+        meta[META_NACT] = total_act;
+        meta[meta_offsets(E) + E] = total_pad;
+      }
+    }
+  }
+  __syncthreads();
+
+  // pass 2: stable scatter
+  for (int base = beg; base < end; base += 32) {
+    const int f = base + lane;
+    int e = -1;
+    if (f < end) {
+      e = ids[f];
+      if (e < 0 || e >= E) e = -1;
+    }
+    const unsigned grp = __match_any_sync(0xffffffffu, e);
+    int slot = 0;
+    if (e >= 0) slot = off[e] + wc[warp * E + e] + __popc(grp & ((1u << lane) - 1u));
+    __syncwarp();
+    if (e >= 0) {
+      sorted[slot] = f;
+      if (lane == __ffs(grp) - 1) wc[warp * E + e] += __popc(grp);
+    }
+    __syncwarp();
+  }
+
+  // block -> expert map and sentinel padding
+  const int total = off[E];
+  const int nblk = total / B;
+  for (int b = threadIdx.x; b < nblk; b += blockDim.x) {
+    int lo = 0, hi = E - 1;  // last expert with off[e] <= b*B
+    const int pos = b * B;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (off[mid] <= pos) lo = mid; else hi = mid - 1;
+    }
+    // skip empty experts sharing the same offset: the owner has off[e] <= pos < off[e+1]
+    while (lo < E - 1 && off[lo + 1] <= pos) ++lo;
+    eids[b] = lo;
+    const int fill_from = max(pos, off[lo] + cnt[lo]);
+    for (int q = fill_from; q < pos + B; ++q) sorted[q] = n;
+  }
+}
+
+// amax over n bf16 values (bit pattern of a non-negative float, atomicMax on
+// the bits is order independent).
+__global__ void k_amax_bf16(const uint16_t* __restrict__ X, size_t n, unsigned* amax_bits) {
+  float m = 0.0f;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+    m = fmaxf(m, fabsf(bf16_bits_to_f32(X[i])));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if ((threadIdx.x & 31) == 0) atomicMax(amax_bits, __float_as_uint(m));
+}
+
+// Gather of token rows into expert order, 16-byte vectors; one CTA per row
+// (grid-stride).  Rows holding the sentinel are zero-filled.
+__global__ void k_gather_copy(const uint4* __restrict__ X, int vec_per_row, int k, int n_pairs,
+                              const int32_t* __restrict__ sorted, const int32_t* __restrict__ meta,
+                              uint4* __restrict__ Xs) {
+  const int npp = meta[META_NPP];
+  for (int r = blockIdx.x; r < npp; r += gridDim.x) {
+    const int f = sorted[r];
+    uint4* dst = Xs + (size_t)r * vec_per_row;
+    if (f < n_pairs) {
+      const uint4* src = X + (size_t)(f / k) * vec_per_row;
+      for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) dst[v] = src[v];
+    } else {
+      for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) dst[v] = make_uint4(0, 0, 0, 0);
+    }
+  }
+}
+
+// Gather + dynamic per-tensor e4m3 quantisation: code = e4m3(x / s), s = amax/448.
+__global__ void k_gather_quant(const uint4* __restrict__ X, int vec_per_row /* 8 bf16 each */, int k, int n_pairs,
+                               const int32_t* __restrict__ sorted, const int32_t* __restrict__ meta,
+                               const unsigned* __restrict__ amax_bits, uint2* __restrict__ Xq) {
+  const int npp = meta[META_NPP];
+  const float s = e4m3_scale_from_amax(__uint_as_float(*amax_bits));
+  for (int r = blockIdx.x; r < npp; r += gridDim.x) {
+    const int f = sorted[r];
+    uint2* dst = Xq + (size_t)r * vec_per_row;
+    if (f < n_pairs) {
+      const uint4* src = X + (size_t)(f / k) * vec_per_row;
+      for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) {
+        const uint4 x = src[v];
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+        uint32_t q[2] = {0, 0};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t bits = (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xffffu);
+          q[j >> 2] |= (uint32_t)f32_to_e4m3(bf16_bits_to_f32(bits) / s) << (8 * (j & 3));
+        }
+        dst[v] = make_uint2(q[0], q[1]);
+      }
+    } else {
+      for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) dst[v] = make_uint2(0, 0);
+    }
+  }
+}
+
+// Split-K reduction of GEMM1 partials (fixed split order), scale, SiLU(gate)*up.
+__global__ void k_reduce_act(const float* __restrict__ P, int splits, size_t split_stride, int I, int B,
+                             const int32_t* __restrict__ eids, const int32_t* __restrict__ meta,
+                             const float* __restrict__ w_scale, const unsigned* __restrict__ a_amax_bits,
+                             int out_mode, void* __restrict__ A_out, unsigned* __restrict__ amax_bits) {
+  const int npp = meta[META_NPP];
+  float m = 0.0f;
+  for (int r = blockIdx.x; r < npp; r += gridDim.x) {
+    float scale = 1.0f;
+    if (w_scale) scale = e4m3_scale_from_amax(__uint_as_float(*a_amax_bits)) * w_scale[eids[r / B]];
+    const float* row = P + (size_t)r * 2 * I;
+    for (int i = threadIdx.x; i < I; i += blockDim.x) {
+      float g = 0.0f, u = 0.0f;
+      for (int s = 0; s < splits; ++s) {
+        g += row[(size_t)s * split_stride + i];
+        u += row[(size_t)s * split_stride + I + i];
+      }
+      if (w_scale) { g *= scale; u *= scale; }
+      const float a = silu(g) * u;
+      if (out_mode == 0) {
+        reinterpret_cast<__nv_bfloat16*>(A_out)[(size_t)r * I + i] = __float2bfloat16_rn(a);
+      } else {
+        reinterpret_cast<float*>(A_out)[(size_t)r * I + i] = a;
+        m = fmaxf(m, fabsf(a));
+      }
+    }
+  }
+  if (out_mode == 1) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if ((threadIdx.x & 31) == 0) atomicMax(amax_bits, __float_as_uint(m));
+  }
+}
+
+// A_q = e4m3(A / s), s = amax/448, rows below num_post_pad.
+__global__ void k_quant_act(const float4* __restrict__ A, int vec_per_row, const int32_t* __restrict__ meta,
+                            const unsigned* __restrict__ amax_bits, uint32_t* __restrict__ Aq) {
+  const int npp = meta[META_NPP];
+  const float s = e4m3_scale_from_amax(__uint_as_float(*amax_bits));
+  const size_t total = (size_t)npp * vec_per_row;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const float4 v = A[i];
+    Aq[i] = (uint32_t)f32_to_e4m3(v.x / s) | ((uint32_t)f32_to_e4m3(v.y / s) << 8) |
+            ((uint32_t)f32_to_e4m3(v.z / s) << 16) | ((uint32_t)f32_to_e4m3(v.w / s) << 24);
+  }
+}
+
+// out[t][h] = sum_j w[t][j] * (sum_s Y[s][t*k+j][h]) in j order then s order,
+// fp32, one rounding at the end.  4 consecutive h per thread.
+template <bool Y_BF16, bool OUT_BF16>
+__global__ void k_combine(const void* __restrict__ Yv, int splits, size_t split_stride, const float* __restrict__ w,
+                          int T, int k, int H, void* __restrict__ out) {
+  const int hv = H / 4;
+  const size_t total = (size_t)T * hv;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i / hv), h = (int)(i % hv) * 4;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < k; ++j) {
+      const size_t f = (size_t)t * k + j;
+      float y[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int s = 0; s < splits; ++s) {
+        if constexpr (Y_BF16) {
+          const uint2 v = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(Yv) +
+                                                          (size_t)s * split_stride + f * H + h);
+          y[0] += bf16_bits_to_f32(v.x & 0xffffu);
+          y[1] += bf16_bits_to_f32(v.x >> 16);
+          y[2] += bf16_bits_to_f32(v.y & 0xffffu);
+          y[3] += bf16_bits_to_f32(v.y >> 16);
+        } else {
+          const float4 v = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(Yv) +
+                                                            (size_t)s * split_stride + f * H + h);
+          y[0] += v.x;
+          y[1] += v.y;
+          y[2] += v.z;
+          y[3] += v.w;
+        }
+      }
+      const float wj = w[f];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[q] = fmaf(wj, y[q], acc[q]);
+    }
+    if constexpr (OUT_BF16) {
+      uint2 o;
+      o.x = pack_bf16x2(acc[0], acc[1]);
+      o.y = pack_bf16x2(acc[2], acc[3]);
+      *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(out) + (size_t)t * H + h) = o;
+    } else {
+      *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + (size_t)t * H + h) =
+          make_float4(acc[0], acc[1], acc[2], acc[3]);
+    }
+  }
+}
+
+// Scalar fallback of the combine for H not divisible by 4 (fp32 path only).
+template <bool Y_BF16, bool OUT_BF16>
+__global__ void k_combine_scalar(const void* __restrict__ Yv, int splits, size_t split_stride,
+                                 const float* __restrict__ w, int T, int k, int H, void* __restrict__ out) {
+  const size_t total = (size_t)T * H;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i / H), h = (int)(i % H);
+    float acc = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const size_t f = (size_t)t * k + j;
+      float y = 0.f;
+      for (int s = 0; s < splits; ++s) {
+        if constexpr (Y_BF16)
+          y += bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(Yv)[(size_t)s * split_stride + f * H + h]);
+        else
+          y += reinterpret_cast<const float*>(Yv)[(size_t)s * split_stride + f * H + h];
+      }
+      acc = fmaf(w[f], y, acc);
+    }
+    if constexpr (OUT_BF16)
+      reinterpret_cast<__nv_bfloat16*>(out)[i] = __float2bfloat16_rn(acc);
+    else
+      reinterpret_cast<float*>(out)[i] = acc;
+  }
+}
+
+int grid_for(size_t work, int threads, int cap_blocks = 152 * 16) {
+  size_t b = (work + threads - 1) / threads;
+  if (b < 1) b = 1;
+  if (b > (size_t)cap_blocks) b = cap_blocks;
+  return (int)b;
+}
+
+}  // namespace
+
+cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int B, int32_t* sorted, int32_t* eids,
+                         int32_t* npp, int32_t* counts, int32_t* meta, int* status, cudaStream_t s) {
+  const size_t smem = (size_t)(kAlignWarps * E + 2 * E + 1 + 33) * sizeof(int);
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(k_align, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) configured[dev] = true;
+  }
+  k_align<<<1, kAlignThreads, smem, s>>>(ids, T, k, E, B, sorted, eids, npp, counts, meta, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_amax_bf16(const void* X, size_t n, unsigned* amax_bits, cudaStream_t s) {
+  k_amax_bf16<<<grid_for(n, 256), 256, 0, s>>>((const uint16_t*)X, n, amax_bits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const void* X, int T, int H, int k, int elem_bytes, int mode, const unsigned* amax_bits,
+                          const int32_t* sorted, const int32_t* meta, int cap, void* Xs, cudaStream_t s) {
+  const int grid = cap < 152 * 8 ? (cap > 0 ? cap : 1) : 152 * 8;
+  if (mode == 0) {
+    const int vpr = H * elem_bytes / 16;
+    k_gather_copy<<<grid, 128, 0, s>>>((const uint4*)X, vpr, k, T * k, sorted, meta, (uint4*)Xs);
+  } else {
+    const int vpr = H / 8;
+    k_gather_quant<<<grid, 128, 0, s>>>((const uint4*)X, vpr, k, T * k, sorted, meta, amax_bits, (uint2*)Xs);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_act(const float* P, int splits, size_t split_stride, int I, int B, const int32_t* eids,
+                              const int32_t* meta, int cap, const float* w_scale, const unsigned* a_amax_bits,
+                              int out_mode, void* A_out, unsigned* amax_bits, cudaStream_t s) {
+  const int grid = cap < 152 * 8 ? (cap > 0 ? cap : 1) : 152 * 8;
+  k_reduce_act<<<grid, 256, 0, s>>>(P, splits, split_stride, I, B, eids, meta, w_scale, a_amax_bits, out_mode, A_out,
+                                    amax_bits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_act(const float* A, int I, const int32_t* meta, int cap, const unsigned* amax_bits,
+                             uint8_t* Aq, cudaStream_t s) {
+  const int vpr = I / 4;
+  k_quant_act<<<grid_for((size_t)cap * vpr, 256), 256, 0, s>>>((const float4*)A, vpr, meta, amax_bits,
+                                                               (uint32_t*)Aq);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const void* Y, int y_bf16, int splits, size_t split_stride, const float* w, int T, int k,
+                           int H, void* out, int out_bf16, cudaStream_t s) {
+  if (H % 4 == 0) {
+    const int grid = grid_for((size_t)T * (H / 4), 256);
+    if (y_bf16 && out_bf16) k_combine<true, true><<<grid, 256, 0, s>>>(Y, splits, split_stride, w, T, k, H, out);
+    else if (y_bf16) k_combine<true, false><<<grid, 256, 0, s>>>(Y, splits, split_stride, w, T, k, H, out);
+    else if (out_bf16) k_combine<false, true><<<grid, 256, 0, s>>>(Y, splits, split_stride, w, T, k, H, out);
+    else k_combine<false, false><<<grid, 256, 0, s>>>(Y, splits, split_stride, w, T, k, H, out);
+  } else {
+    const int grid = grid_for((size_t)T * H, 256);
+    if (y_bf16 && out_bf16) k_combine_scalar<true, true><<<grid, 256, 0, s>>>(Y, splits, split_stride, w, T, k, H, out);
+    else if (y_bf16) k_combine_scalar<true, false><<<grid, 256, 0, s>>>(Y, splits, split_stride, w, T, k, H, out);
+    else if (out_bf16) k_combine_scalar<false, true><<<grid, 256, 0, s>>>(Y, splits, split_stride, w, T, k, H, out);
+    else k_combine_scalar<false, false><<<grid, 256, 0, s>>>(Y, splits, split_stride, w, T, k, H, out);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

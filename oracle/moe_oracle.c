@@ -85,27 +85,36 @@ double oracle_e4m3_to_f64(uint8_t c) {
   return sign ? -mag : mag;
 }
 
+/* Decoded value of every e4m3 code, filled from oracle_e4m3_to_f64 before any
+ * parallel region (a cache of the decoder above, for speed only). */
+static double e4m3_table[256];
+static int e4m3_table_ready = 0;
+static void e4m3_table_init(void) {
+  if (e4m3_table_ready) return;
+  for (int c = 0; c < 256; ++c) e4m3_table[c] = oracle_e4m3_to_f64((uint8_t)c);
+  e4m3_table_ready = 1;
+}
+
 /* float -> E4M3, round to nearest with ties to even, saturating to +-448.
- * Written as a search over the 127 non-negative finite codes, which are in
- * increasing order of value: find the two neighbours and pick the nearer,
- * the even code on a tie. */
+ * The 127 non-negative finite codes are in increasing order of value: find
+ * the largest code not above |f| (binary search over the decoded values),
+ * then pick the nearer of it and the next code, the even code on a tie. */
 uint8_t oracle_f32_to_e4m3_satfinite(float f) {
   if (isnan(f)) return 0x7f;
+  e4m3_table_init();
   uint8_t sign = signbit(f) ? 0x80 : 0x00;
   double a = fabs((double)f);
   if (a >= 448.0) return (uint8_t)(sign | 0x7e);
-  int lo = 0; /* largest code with value <= a */
-  for (int c = 0; c <= 0x7e; ++c) {
-    if (oracle_e4m3_to_f64((uint8_t)c) <= a) lo = c;
+  int lo = 0, hi = 0x7e; /* invariant: table[lo] <= a < table[hi] */
+  while (hi - lo > 1) {
+    int mid = (lo + hi) / 2;
+    if (e4m3_table[mid] <= a) lo = mid; else hi = mid;
   }
-  int hi = lo + 1;
-  double vlo = oracle_e4m3_to_f64((uint8_t)lo);
-  double vhi = oracle_e4m3_to_f64((uint8_t)hi);
+  double vlo = e4m3_table[lo], vhi = e4m3_table[hi];
   int pick;
   if (a - vlo < vhi - a) pick = lo;
   else if (a - vlo > vhi - a) pick = hi;
   else pick = (lo & 1) ? hi : lo;
-  if (a == vlo) pick = lo;
   return (uint8_t)(sign | pick);
 }
 
@@ -113,7 +122,7 @@ static double load_elem(const void* p, int dtype, size_t i) {
   switch (dtype) {
     case ORC_F32: return (double)((const float*)p)[i];
     case ORC_BF16: return oracle_bf16_to_f64(((const uint16_t*)p)[i]);
-    case ORC_E4M3: return oracle_e4m3_to_f64(((const uint8_t*)p)[i]);
+    case ORC_E4M3: return e4m3_table[((const uint8_t*)p)[i]];
   }
   return NAN;
 }
@@ -128,6 +137,7 @@ double oracle_silu(double z) { return z / (1.0 + exp(-z)); }
 /*  weight distribution over the experts.)                                   */
 /* ------------------------------------------------------------------------ */
 void oracle_router_logits(const void* X, const void* Wr, int dtype, int T, int H, int E, double* logits) {
+  e4m3_table_init();
 #pragma omp parallel for schedule(static)
   for (int t = 0; t < T; ++t) {
     for (int e = 0; e < E; ++e) {
@@ -238,6 +248,7 @@ int oracle_moe_forward(const void* X, const void* Wr, const void* W13, const voi
   if (fp8 && (!w13_scale || !w2_scale || act_dtype != ORC_BF16)) return -1;
   if (!tokens) n_tokens = T;
   if (T == 0) return 0;
+  e4m3_table_init();
 
   double* logits = (double*)malloc(sizeof(double) * (size_t)T * E);
   int32_t* ids = (int32_t*)malloc(sizeof(int32_t) * (size_t)T * k);
@@ -303,15 +314,15 @@ int oracle_moe_forward(const void* X, const void* Wr, const void* W13, const voi
 #pragma omp for schedule(dynamic, 1)
     for (int t = 0; t < T; ++t) {
       for (int h = 0; h < H; ++h)
-        xq[h] = oracle_e4m3_to_f64(oracle_e4m3_quant(load_f32(X, act_dtype, (size_t)t * H + h), s_a1));
+        xq[h] = e4m3_table[oracle_e4m3_quant(load_f32(X, act_dtype, (size_t)t * H + h), s_a1)];
       for (int j = 0; j < k; ++j) {
         const int e = ids[(size_t)t * k + j];
         const size_t w13_base = (size_t)e * 2 * I * H;
         for (int i = 0; i < I; ++i) {
           double g = 0.0, u = 0.0;
           for (int h = 0; h < H; ++h) {
-            g += oracle_e4m3_to_f64(((const uint8_t*)W13)[w13_base + (size_t)i * H + h]) * xq[h];
-            u += oracle_e4m3_to_f64(((const uint8_t*)W13)[w13_base + (size_t)(I + i) * H + h]) * xq[h];
+            g += e4m3_table[((const uint8_t*)W13)[w13_base + (size_t)i * H + h]] * xq[h];
+            u += e4m3_table[((const uint8_t*)W13)[w13_base + (size_t)(I + i) * H + h]] * xq[h];
           }
           g = g * (double)s_a1 * (double)w13_scale[e];
           u = u * (double)s_a1 * (double)w13_scale[e];
@@ -336,12 +347,12 @@ int oracle_moe_forward(const void* X, const void* Wr, const void* W13, const voi
       for (int j = 0; j < k; ++j) {
         const int e = ids[(size_t)t * k + j];
         for (int i = 0; i < I; ++i)
-          aq[i] = oracle_e4m3_to_f64(oracle_e4m3_quant((float)A[((size_t)t * k + j) * I + i], s_a2));
+          aq[i] = e4m3_table[oracle_e4m3_quant((float)A[((size_t)t * k + j) * I + i], s_a2)];
         const size_t w2_base = (size_t)e * H * I;
         const double wj = w[(size_t)t * k + j];
         for (int h = 0; h < H; ++h) {
           double y = 0.0;
-          for (int i = 0; i < I; ++i) y += oracle_e4m3_to_f64(((const uint8_t*)W2)[w2_base + (size_t)h * I + i]) * aq[i];
+          for (int i = 0; i < I; ++i) y += e4m3_table[((const uint8_t*)W2)[w2_base + (size_t)h * I + i]] * aq[i];
           y = y * (double)s_a2 * (double)w2_scale[e];
           o[h] += wj * y;
         }

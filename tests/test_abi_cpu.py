@@ -1,0 +1,104 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports every
+entry point include/moe_api.h declares, sizes its workspace, and rejects bad
+arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from mixture_experts_layer_scan_gb300 import _build
+
+    _build.build()
+    import mixture_experts_layer_scan_gb300 as m
+
+    return m
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "moe_api.h")).read()
+    return sorted(set(re.findall(r"MOE_API\s+[\w\s\*]*?\b(moe_\w+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(moe):
+    names = _declared()
+    assert len(names) >= 9
+    lib = ctypes.CDLL(moe.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(moe.EXPORTS) == names
+
+
+def test_exports_nothing_else(moe):
+    import subprocess
+
+    out = subprocess.run(["nm", "-D", "--defined-only", moe.LIB_PATH], capture_output=True, text=True).stdout
+    syms = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    assert syms == set(_declared())
+
+
+def test_strerror_and_version(moe):
+    assert moe.strerror(0) == "ok"
+    assert "workspace" in moe.strerror(moe.MOE_ERR_WORKSPACE)
+    assert moe.version() >= 100
+
+
+def test_workspace_size_rules(moe):
+    f32 = moe.moe_workspace_size(64, 256, 512, 8, 2, moe.MOE_F32, moe.MOE_F32)
+    assert f32 > 0 and f32 % 256 == 0
+    dec = moe.moe_workspace_size(64, 4096, 14336, 8, 2, moe.MOE_BF16, moe.MOE_BF16)
+    pre = moe.moe_workspace_size(8192, 4096, 2048, 64, 8, moe.MOE_BF16, moe.MOE_BF16)
+    fp8 = moe.moe_workspace_size(64, 4096, 8192, 64, 8, moe.MOE_BF16, moe.MOE_E4M3)
+    assert 0 < dec < pre and fp8 > 0
+    # the prefill workspace holds at least the sorted activations, the intermediate and Y
+    cap = 8192 * 8 + 64 * 127
+    assert pre >= cap * 4096 * 2 + cap * 2048 * 2 + 8192 * 8 * 4096 * 2
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_workspace_size(64, 4000, 14336, 8, 2, moe.MOE_BF16, moe.MOE_BF16)
+    assert e.value.code == moe.MOE_ERR_UNSUPPORTED
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_workspace_size(64, 4096, 1024, 8, 9, moe.MOE_BF16, moe.MOE_BF16)
+    assert e.value.code == moe.MOE_ERR_ARG
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_workspace_size(64, 4096, 1024, 8, 2, moe.MOE_F32, moe.MOE_BF16)
+    assert e.value.code == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_align_capacity(moe):
+    assert moe.moe_align_capacity(64, 8, 128, 16) == (512 + 128 * 15, (512 + 128 * 15) // 16)
+    assert moe.moe_align_capacity(1, 2, 8, 16) == (2 + 2 * 15, 32 // 16)
+    assert moe.moe_align_capacity(0, 2, 8, 16) == (0, 0)
+
+
+def test_forward_argument_errors_before_launch(moe):
+    lib = moe.lib()
+    v = ctypes.c_void_p
+    fake = v(0x1000)  # never dereferenced: every call below fails validation first
+    odd = v(0x1008)
+    ws = v(0x100000)
+    # T = 0 is a successful no-op
+    assert lib.moe_forward(None, None, None, None, 0, 256, 256, 8, 2, 1, 1, 1, None, None, None, None, 0, None,
+                           None) == 0
+    # null pointers
+    assert lib.moe_forward(None, fake, fake, fake, 4, 256, 256, 8, 2, 1, 1, 1, None, None, fake, ws, 1 << 30, None,
+                           None) == moe.MOE_ERR_ARG
+    # misaligned
+    assert lib.moe_forward(odd, fake, fake, fake, 4, 256, 256, 8, 2, 1, 1, 1, None, None, fake, ws, 1 << 30, None,
+                           None) == moe.MOE_ERR_ALIGNMENT
+    # workspace too small
+    assert lib.moe_forward(fake, fake, fake, fake, 4, 256, 256, 8, 2, 1, 1, 1, None, None, fake, ws, 1024, None,
+                           None) == moe.MOE_ERR_WORKSPACE
+    # FP8 without scales
+    assert lib.moe_forward(fake, fake, fake, fake, 4, 256, 256, 8, 2, 1, 1, 2, None, None, fake, ws, 1 << 30, None,
+                           None) == moe.MOE_ERR_ARG
+    # bad sizes
+    assert lib.moe_forward(fake, fake, fake, fake, 4, 256, 256, 2000, 2, 1, 1, 1, None, None, fake, ws, 1 << 30,
+                           None, None) == moe.MOE_ERR_ARG
+    assert lib.moe_route(fake, fake, 4, 256, 8, 0, 1, 1, fake, fake, fake, None) == moe.MOE_ERR_ARG
+    assert lib.moe_align(fake, 4, 2, 8, 0, fake, fake, fake, None, None) == moe.MOE_ERR_ARG
+    assert lib.moe_topk_from_logits(fake, 4, 8, 9, 1, fake, fake, None) == moe.MOE_ERR_ARG

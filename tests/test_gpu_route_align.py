@@ -1,0 +1,96 @@
+"""GPU parity of the router (steps 1-2) and the permutation (step 3) against the CPU oracle.
+
+Routing ids, the sorted pair list, the block-to-expert map, the padded length
+and the per-expert counts must match bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import make_tie_free
+from moe_synth import make_layer, spec
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import mixture_experts_layer_scan_gb300 as m
+
+    assert torch.cuda.is_available()
+    return m
+
+
+def _logits_with_ties(T, E, seed):
+    rng = np.random.default_rng(seed)
+    lg = rng.standard_normal((T, E)).astype(np.float32)
+    lg[::3, : max(1, E // 3)] = lg[::3, :1]  # exact ties: lower index must rank first
+    lg[1::5, -1] = lg[1::5, 0]
+    return lg
+
+
+@pytest.mark.parametrize("T,E,k,renorm", [(1, 8, 2, True), (37, 8, 2, True), (64, 128, 8, True), (300, 64, 8, False),
+                                          (5, 1024, 32, True), (16, 3, 3, False), (129, 33, 1, False)])
+def test_topk_from_logits_bit_exact(moe, T, E, k, renorm):
+    lg = _logits_with_ties(T, E, T * 7 + E)
+    w, ids = moe.moe_topk_from_logits(torch.from_numpy(lg).cuda(), k, renorm)
+    rid, rw = oracle.topk(lg.astype(np.float64), k, renorm)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=1e-5, atol=1e-7)
+
+
+@pytest.mark.parametrize("name,T", [("tiny_f32", 64), ("mixtral_decode", 64), ("fine_decode", 64),
+                                    ("fp8_decode", 64), ("prefill", 8192), ("prefill_hot", 8192)])
+def test_route_matches_oracle(moe, name, T):
+    sp = spec(name, T=T)
+    L = make_layer(sp, weights=False)
+    make_tie_free(L)
+    logits, w, ids = moe.moe_route(L["X"].cuda(), L["Wr"].cuda(), sp.k, sp.renorm)
+    ref_lg = oracle.router_logits(L["X"], L["Wr"])
+    rid, rw = oracle.topk(ref_lg, sp.k, sp.renorm)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    # fp32 summation of H products: |err| <= H * 2^-24 * sum_h |x_h w_h| (plus the product roundings)
+    bound = (sp.H + 2) * 2.0 ** -24 * (np.abs(L["X"].double().numpy()) @ np.abs(L["Wr"].double().numpy()).T)
+    assert np.all(np.abs(logits.cpu().numpy() - ref_lg) <= bound)
+    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=1e-4, atol=1e-6)
+
+
+def _random_ids(T, k, E, seed, skew=False):
+    rng = np.random.default_rng(seed)
+    if skew:
+        p = 1.0 / np.arange(1, E + 1) ** 1.1
+        p /= p.sum()
+        return np.stack([rng.choice(E, size=k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+    return np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+
+
+@pytest.mark.parametrize("T,k,E,B", [(1, 1, 1, 1), (1, 2, 8, 16), (37, 2, 8, 16), (64, 8, 128, 16), (100, 3, 5, 4),
+                                     (257, 8, 64, 128), (1000, 6, 1024, 16), (8192, 8, 64, 128), (333, 7, 9, 1024)])
+def test_align_bit_exact(moe, T, k, E, B):
+    ids = _random_ids(T, k, E, T + 31 * E, skew=(T % 2 == 0))
+    s, ex, npp, counts = moe.moe_align(torch.from_numpy(ids).cuda(), E, B)
+    torch.cuda.synchronize()
+    assert moe.moe_get_status() == 0
+    rs, rex, rnpp, rcounts = oracle.align(ids, E, B)
+    n = int(npp.item())
+    assert n == rnpp
+    assert np.array_equal(s.cpu().numpy()[:n], rs)
+    assert np.array_equal(ex.cpu().numpy()[: n // B], rex)
+    assert np.array_equal(counts.cpu().numpy(), rcounts)
+
+
+def test_align_is_deterministic_and_flags_bad_ids(moe):
+    ids = _random_ids(512, 8, 64, 5)
+    a = moe.moe_align(torch.from_numpy(ids).cuda(), 64, 16)
+    b = moe.moe_align(torch.from_numpy(ids).cuda(), 64, 16)
+    n = int(a[2].item())
+    assert torch.equal(a[0][:n], b[0][:n]) and torch.equal(a[1][: n // 16], b[1][: n // 16])
+    torch.cuda.synchronize()
+    assert moe.moe_get_status() == 0
+    bad = ids.copy()
+    bad[3, 1] = 64
+    bad[7, 0] = -2
+    moe.moe_align(torch.from_numpy(bad).cuda(), 64, 16)
+    assert moe.moe_get_status() == moe.MOE_ERR_DEVICE_INDEX
+    assert moe.moe_get_status() == 0  # cleared by the read
