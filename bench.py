@@ -1,0 +1,438 @@
+"""Benchmark of the fused MoE layer forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME] [--no-sweep]
+
+One step is one moe_forward call (router, permutation, gather, GEMM1 with the
+SiLU(gate)*up epilogue, GEMM2, combine) on one synthetic token batch with the
+weights resident in HBM.  The headline workload is the Mixtral-shaped decode
+layer (hidden 4096, 8 experts, FFN 14336, top-2) at M = 64 tokens; a sweep over
+the other decode batch sizes, the fine-grained and FP8 decode layers and the
+8192-token prefill layer follows in "sweep" (fewer steps each).
+
+Prints ONE JSON line (rank 0).  Under torchrun every rank runs its own replica
+on its own GPU (tokens are independent: weak scaling, no collective on the data
+path); the timed region is bracketed by a barrier and the max over ranks is used.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from moe_synth import make_layer, spec  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+METRIC = "MoE-layer tokens/s; decode weight-stream HBM GB/s, prefill TFLOP/s vs peak"
+
+WORKLOADS = {
+    "mixtral_decode_M64": ("mixtral_decode", 64), "mixtral_decode_M16": ("mixtral_decode", 16),
+    "mixtral_decode_M4": ("mixtral_decode", 4), "mixtral_decode_M1": ("mixtral_decode", 1),
+    "fine_decode_M64": ("fine_decode", 64), "fine_decode_M32": ("fine_decode", 32),
+    "fine_decode_M8": ("fine_decode", 8), "fine_decode_M1": ("fine_decode", 1),
+    "fp8_decode_M64": ("fp8_decode", 64), "fp8_decode_M16": ("fp8_decode", 16), "fp8_decode_M1": ("fp8_decode", 1),
+    "prefill_T8192": ("prefill", 8192), "prefill_hot_T8192": ("prefill_hot", 8192),
+}
+HEADLINE = "mixtral_decode_M64"
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------
+# algorithmic work of one layer call (from the realised routing)
+# ----------------------------------------------------------------------------
+def work(sp, n_active: int, act_split: bool):
+    wb = 1 if sp.w == "e4m3" else (4 if sp.w == "f32" else 2)
+    ab = 4 if sp.act == "f32" else 2
+    n = sp.T * sp.k
+    I, H = sp.I, sp.H
+    w13 = n_active * 2 * I * H * wb
+    w2 = n_active * H * I * wb
+    a_bytes = n * I * (1 if sp.w == "e4m3" else ab * (2 if act_split else 1))
+    g1_bytes = w13 + n * H * (1 if sp.w == "e4m3" else ab) + a_bytes
+    g2_bytes = w2 + a_bytes + n * H * 4
+    layer_bytes = w13 + w2 + sp.E * H * ab + 2 * sp.T * H * ab
+    flops1 = 2.0 * n * 2 * I * H
+    flops2 = 2.0 * n * H * I
+    return {"w13_bytes": w13, "w2_bytes": w2, "gemm1_bytes": g1_bytes, "gemm2_bytes": g2_bytes,
+            "layer_bytes": layer_bytes, "gemm1_flops": flops1, "gemm2_flops": flops2,
+            "layer_flops": flops1 + flops2 + 2.0 * sp.T * sp.E * H, "bytes_per_active_expert": 3 * I * H * wb}
+
+
+def _sha(path):
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def traffic_from_profiles(kernel: str, workload: str):
+    """dram bytes per launch from a committed ncu summary, if the kernel source has not changed since."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path))
+    e = d.get(f"{kernel}:{workload}")
+    if not e:
+        return None
+    src = os.path.join(ROOT, "mixture_experts_layer_scan_gb300", "csrc", "moe_gemm_tc.cu")
+    if e.get("source_sha") != _sha(src):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                s, m = float(f[1]), float(f[2])
+            except ValueError:
+                continue
+            sm.append(s)
+            mx = m
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        loaded = [s for s in sm if s > 0.5 * (mx or max(sm))] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# our implementation
+# ----------------------------------------------------------------------------
+def run_ours(args, rank, world, dev):
+    import mixture_experts_layer_scan_gb300 as moe
+
+    pk = peaks()
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)  # graph capture needs a non-default stream
+    torch.cuda.set_stream(stream)
+    flush_buf = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    names = [args.workload] + ([] if args.no_sweep else [w for w in WORKLOADS if w != args.workload])
+    results = {}
+    head = None
+    for wi, wname in enumerate(names):
+        base, T = WORKLOADS[wname]
+        sp = spec(base, T=T)
+        L = make_layer(sp, device=dev)
+        X, Wr, W13, W2 = L["X"], L["Wr"], L["W13"], L["W2"]
+        s13, s2 = L["w13_scale"], L["w2_scale"]
+        act = moe.MOE_F32 if sp.act == "f32" else moe.MOE_BF16
+        wdt = {"f32": moe.MOE_F32, "bf16": moe.MOE_BF16, "e4m3": moe.MOE_E4M3}[sp.w]
+        plan = moe.moe_plan_info(T, sp.H, sp.I, sp.E, sp.k, act, wdt)
+        ws = torch.empty(plan["workspace_bytes"], dtype=torch.uint8, device=dev)
+        out = torch.empty_like(X)
+        # realised routing (the library's own router on the same batch)
+        _, _, ids = moe.moe_route(X, Wr, sp.k, sp.renorm)
+        n_active = int(torch.unique(ids).numel())
+        wk = work(sp, n_active, bool(plan["act_split"]))
+        weights_active = wk["w13_bytes"] + wk["w2_bytes"]
+        flush = weights_active < 2 * L2_BYTES  # else the step's own inputs exceed L2
+
+        def step(options=None):
+            moe.moe_forward(X, Wr, W13, W2, sp.k, sp.renorm, s13, s2, out=out, workspace=ws, options=options,
+                            stream=stream)
+
+        is_head = wi == 0
+        K = args.steps if is_head else min(args.steps, args.sweep_steps)
+        W = max(3, args.warmup)
+        for _ in range(W):
+            step()
+        torch.cuda.synchronize()
+        assert moe.moe_get_status() == 0
+        # CUDA graph of one layer call (replayed: no host launch gaps between steps)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
+            step()
+        for _ in range(W):
+            graph.replay()
+        torch.cuda.synchronize()
+
+        def timed(fn, k, flush_between):
+            if not flush_between:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(k):
+                    fn()
+                e1.record(stream)
+                e1.synchronize()
+                return e0.elapsed_time(e1)
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(k)]
+            for a, b in evs:
+                flush_buf.zero_()
+                a.record(stream)
+                fn()
+                b.record(stream)
+            torch.cuda.synchronize()
+            return sum(a.elapsed_time(b) for a, b in evs)
+
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        sampler = ClockSampler(torch.cuda.current_device()) if is_head and rank == 0 else None
+        if sampler:
+            sampler.__enter__()
+        total_ms = timed(graph.replay, K, flush)
+        if sampler:
+            sampler.__exit__()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+            t = torch.tensor([total_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            total_ms = float(t.item())
+        ms = total_ms / K
+        eager_ms = timed(step, min(K, 200), flush) / min(K, 200)
+
+        # per-stage durations (CUDA events recorded by the library on this stream)
+        kk = min(K, 100)
+        stage_ev = []
+        for _ in range(kk):
+            b = {n: torch.cuda.Event(enable_timing=True) for n in moe.STAGES}
+            e = {n: torch.cuda.Event(enable_timing=True) for n in moe.STAGES}
+            stage_ev.append((b, e))
+        for b, e in stage_ev:
+            if flush:
+                flush_buf.zero_()
+            step({"stage_begin": b, "stage_end": e})
+        torch.cuda.synchronize()
+        stage_ms = {n: sum(b[n].elapsed_time(e[n]) for b, e in stage_ev) / kk for n in moe.STAGES}
+        assert moe.moe_get_status() == 0
+
+        tok_s = world * T / (ms / 1e3)
+        decode = sp.T <= 64
+        g1_ms, g2_ms = stage_ms["gemm1"], stage_ms["gemm2"]
+        r = {"tokens_per_s": tok_s, "ms_per_step": ms, "eager_ms_per_step": eager_ms, "active_experts": n_active,
+             "plan": plan, "stage_ms": stage_ms, "l2": "flushed between steps" if flush else "inputs larger than L2"}
+        if decode:
+            r["layer_hbm_gbs"] = wk["layer_bytes"] / (ms / 1e3) / 1e9
+            r["layer_hbm_frac"] = r["layer_hbm_gbs"] / pk["hbm_gbs"]
+            r["gemm1_hbm_gbs"] = wk["gemm1_bytes"] / (g1_ms / 1e3) / 1e9
+            r["gemm2_hbm_gbs"] = wk["gemm2_bytes"] / (g2_ms / 1e3) / 1e9
+            r["gemm1_frac"] = r["gemm1_hbm_gbs"] / pk["hbm_gbs"]
+            r["gemm2_frac"] = r["gemm2_hbm_gbs"] / pk["hbm_gbs"]
+        else:
+            peak_t = pk["bf16_tflops_sustained"] * (2 if sp.w == "e4m3" else 1)
+            r["layer_tflops"] = wk["layer_flops"] / (ms / 1e3) / 1e12
+            r["layer_tensor_frac"] = r["layer_tflops"] / peak_t
+            r["gemm1_tflops"] = wk["gemm1_flops"] / (g1_ms / 1e3) / 1e12
+            r["gemm2_tflops"] = wk["gemm2_flops"] / (g2_ms / 1e3) / 1e12
+            r["gemm1_frac"] = r["gemm1_tflops"] / peak_t
+            r["gemm2_frac"] = r["gemm2_tflops"] / peak_t
+        r["work"] = wk
+        results[wname] = r
+
+        if is_head:
+            head = dict(r)
+            head["spec"] = sp
+            head["clocks"] = sampler.summary() if sampler else None
+            head["K"], head["W"] = K, W
+            # end to end through the C ABI with host buffers: H2D of the batch, the
+            # layer call, D2H of the output, every step
+            Xh = X.cpu().pin_memory()
+            outh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+            Xd = torch.empty_like(X)
+
+            def e2e_step():
+                Xd.copy_(Xh, non_blocking=True)
+                moe.moe_forward(Xd, Wr, W13, W2, sp.k, sp.renorm, s13, s2, out=out, workspace=ws, stream=stream)
+                outh.copy_(out, non_blocking=True)
+
+            for _ in range(W):
+                e2e_step()
+            torch.cuda.synchronize()
+            ke = min(K, 500)
+            e2e_ms = timed(e2e_step, ke, False) / ke
+            head["e2e"] = {"value": world * T / (e2e_ms / 1e3), "unit": "tokens/s",
+                           "h2d_bytes_per_step": X.numel() * X.element_size(),
+                           "d2h_bytes_per_step": out.numel() * out.element_size()}
+            head["cpu_layer"] = (L, sp)
+        del L, X, Wr, W13, W2, ws, out, graph
+        torch.cuda.empty_cache()
+    return head, results, pk
+
+
+def cpu_baseline(L, sp, budget_s=20.0):
+    """The CPU oracle, as it stands, on a bounded token sample of the workload, on all host cores."""
+    import oracle
+
+    oracle.set_threads(len(os.sched_getaffinity(0)))
+    cores = oracle.get_threads()
+    cpu = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in L.items()}
+    n = min(sp.T, max(1, 2 * cores))
+    tokens = list(range(n))
+    t0 = time.perf_counter()
+    oracle.moe_forward(cpu["X"], cpu["Wr"], cpu["W13"], cpu["W2"], sp.k, sp.renorm, cpu["w13_scale"],
+                       cpu["w2_scale"], tokens=tokens)
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} of the {sp.T} tokens of the batch (full layer weights, routing of all {sp.T} tokens), "
+                      f"{dt:.1f} s on {cores} threads"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--sweep-steps", type=int, default=200)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    base, T = WORKLOADS[args.workload]
+    sp = spec(base, T=T)
+    config = {"workload": args.workload, "tokens": T, "hidden": sp.H, "experts": sp.E, "intermediate": sp.I,
+              "topk": sp.k, "renorm": sp.renorm, "weights": sp.w, "activations": sp.act}
+
+    if args.impl == "reference":
+        if world > 1 and rank != 0:
+            return
+        import oracle
+
+        oracle.build()
+        L = make_layer(sp, device="cuda" if torch.cuda.is_available() else "cpu")
+        oracle.set_threads(len(os.sched_getaffinity(0)))
+        cores = oracle.get_threads()
+        cpu = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in L.items()}
+        n = min(T, max(1, cores))
+        tokens = list(range(n))
+
+        def ref_step():
+            oracle.moe_forward(cpu["X"], cpu["Wr"], cpu["W13"], cpu["W2"], sp.k, sp.renorm, cpu["w13_scale"],
+                               cpu["w2_scale"], tokens=tokens)
+
+        steps, warm = min(args.steps, 5), min(max(args.warmup, 0), 1)
+        for _ in range(warm):
+            ref_step()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            ref_step()
+        dt = (time.perf_counter() - t0) / steps
+        v = n / dt
+        sample = f"{n} of the {T} tokens per step, {steps} timed steps (full weights), {cores} threads"
+        print(json.dumps({"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 1,
+                          "steps": steps, "warmup": warm, "ms_per_step": dt * 1e3, "higher_is_better": True,
+                          "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                          "config": config,
+                          "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                           "sample": sample},
+                          "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}))
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    head, results, pk = run_ours(args, rank, world, dev)
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    hsp = head["spec"]
+    decode = hsp.T <= 64
+    wk = head["work"]
+    if decode:
+        roof = {"kernel": "k_gemm_tc (GEMM1, w13 + SiLU(gate)*up)", "bound": "hbm",
+                "achieved": head["gemm1_hbm_gbs"], "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": head["gemm1_frac"], "peak_source": pk["source"] + " (hbm_gbs)",
+                "algorithmic_bytes_per_launch": wk["gemm1_bytes"],
+                "per_unit": f"{2 * hsp.I * hsp.H * 2} B of w13 per active expert x {head['active_experts']} active"}
+    else:
+        roof = {"kernel": "k_gemm_tc (GEMM1)", "bound": "tensor", "achieved": head["gemm1_tflops"],
+                "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s", "frac": head["gemm1_frac"],
+                "peak_source": pk["source"] + " (bf16_tflops_sustained)"}
+    roof["traffic"] = traffic_from_profiles("gemm1", args.workload)
+    line = {"metric": METRIC, "value": head["tokens_per_s"], "unit": "tokens/s", "n_gpus": world, "steps": head["K"],
+            "warmup": head["W"], "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if hsp.act == "bf16" and hsp.w == "bf16" else hsp.w,
+            "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights, random-init Mixtral-shaped experts)",
+            "config": dict(config, l2=head["l2"], launch="CUDA graph of one moe_forward call",
+                           eager_ms_per_step=head["eager_ms_per_step"], plan=head["plan"],
+                           active_experts=head["active_experts"]),
+            "roofline": roof,
+            "layer": {"hbm_gbs": head.get("layer_hbm_gbs"), "frac": head.get("layer_hbm_frac"),
+                      "algorithmic_bytes": wk["layer_bytes"]} if decode else
+                     {"tflops": head.get("layer_tflops"), "frac": head.get("layer_tensor_frac")},
+            "stage_ms": head["stage_ms"], "clocks": head["clocks"], "e2e": head["e2e"],
+            "gpu_launches": head["plan"]["kernel_launches"] * head["K"]}
+    if not args.no_cpu_baseline:
+        L, csp = head["cpu_layer"]
+        line["cpu_baseline"] = cpu_baseline(L, csp)
+    sweep = {}
+    for name, r in results.items():
+        if name == args.workload:
+            continue
+        keep = {k: v for k, v in r.items() if k not in ("work", "plan")}
+        keep["stage_ms"] = {k: round(v, 4) for k, v in r["stage_ms"].items()}
+        sweep[name] = keep
+    if sweep:
+        line["sweep"] = sweep
+    print(json.dumps(line, default=float))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -98,12 +98,25 @@ typedef struct {
                          nothing sets, with a ~1 ms bound; the call then reports
                          MOE_ERR_DEVICE_TIMEOUT through moe_get_status and writes
                          nothing else.  0 in normal use. */
-  int reserved;
+  int act_split;      /* bf16 path: 0 = automatic (hi/lo in SWAP_AB, single in TOKEN_MAJOR),
+                         1 = intermediate stored as one bf16, 2 = as bf16 hi + bf16 lo
+                         (a - bf16(a)), GEMM2 then runs both parts into one fp32 accumulator */
   /* Nullable CUDA events recorded on `stream` right before / after the
    * kernels of each stage (the caller creates and owns them). */
   moe_event_t stage_begin[MOE_NUM_STAGES];
   moe_event_t stage_end[MOE_NUM_STAGES];
 } moe_options;
+
+/* What moe_forward will run for a shape (filled by moe_plan_info). */
+typedef struct {
+  int orientation;      /* MOE_ORIENT_SWAP_AB or MOE_ORIENT_TOKEN_MAJOR (0 on the fp32 path) */
+  int block;            /* permutation block size B */
+  int splits_gemm1;     /* K splits of GEMM1 / GEMM2 */
+  int splits_gemm2;
+  int act_split;        /* 1 if the bf16 intermediate is stored as hi + lo */
+  int kernel_launches;  /* kernels one moe_forward call launches */
+  size_t workspace_bytes;
+} moe_plan;
 
 /* Human-readable text of a return code (static storage). */
 MOE_API const char* moe_strerror(int code);
@@ -112,6 +125,11 @@ MOE_API const char* moe_strerror(int code);
  * options (written to *bytes).  Depends only on its arguments. */
 MOE_API int moe_workspace_size(int T, int H, int I, int E, int topk, moe_dtype act_dtype, moe_dtype w_dtype,
                        const moe_options* opts, size_t* bytes);
+
+/* Describes the kernels and workspace moe_forward uses for these arguments
+ * (host only, no device work).  Same argument rules as moe_workspace_size. */
+MOE_API int moe_plan_info(int T, int H, int I, int E, int topk, moe_dtype act_dtype, moe_dtype w_dtype,
+                          const moe_options* opts, moe_plan* info);
 
 /* Capacities of the permutation outputs for (T, topk, E, block):
  *   sorted_cap = T*topk + min(E, T*topk)*(block-1)     (int32 entries)
@@ -173,8 +191,9 @@ MOE_API int moe_align(const int32_t* topk_ids, int T, int topk, int E, int block
  *                in the GEMM epilogues (page 1, section "Routage backend pour la
  *                quantisation des tenseurs FP8": scaling fused where the data is used)
  *   tensor-core paths need H % 128 == 0 and I % 128 == 0.
- * The intermediate SiLU(gate)*up is stored in bf16 (fp32 on the fp32 path, e4m3 on
- * the FP8 path); accumulation is fp32 throughout; out is rounded once. */
+ * The intermediate SiLU(gate)*up is stored in bf16 (as a bf16 hi + lo pair in SWAP_AB
+ * mode, see moe_options.act_split; fp32 on the fp32 path; e4m3 on the FP8 path);
+ * accumulation is fp32 throughout; out is rounded once. */
 MOE_API int moe_forward(const void* hidden, const void* router_w, const void* w13, const void* w2, int T, int H, int I, int E,
                 int topk, int renorm, moe_dtype act_dtype, moe_dtype w_dtype, const float* w13_scale,
                 const float* w2_scale, void* out, void* workspace, size_t workspace_bytes, const moe_options* opts,

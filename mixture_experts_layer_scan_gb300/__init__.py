@@ -25,8 +25,8 @@ STAGES = ("route", "align", "gather", "gemm1", "act", "gemm2", "combine")
 NUM_STAGES = len(STAGES)
 
 # every entry point include/moe_api.h declares
-EXPORTS = ("moe_strerror", "moe_workspace_size", "moe_align_capacity", "moe_route", "moe_topk_from_logits",
-           "moe_align", "moe_forward", "moe_get_status", "moe_version")
+EXPORTS = ("moe_strerror", "moe_workspace_size", "moe_plan_info", "moe_align_capacity", "moe_route",
+           "moe_topk_from_logits", "moe_align", "moe_forward", "moe_get_status", "moe_version")
 
 
 class MoeError(RuntimeError):
@@ -37,8 +37,14 @@ class MoeError(RuntimeError):
 
 class moe_options(ctypes.Structure):
     _fields_ = [("orientation", ctypes.c_int), ("split_k", ctypes.c_int), ("inject_timeout", ctypes.c_int),
-                ("reserved", ctypes.c_int), ("stage_begin", ctypes.c_void_p * NUM_STAGES),
+                ("act_split", ctypes.c_int), ("stage_begin", ctypes.c_void_p * NUM_STAGES),
                 ("stage_end", ctypes.c_void_p * NUM_STAGES)]
+
+
+class moe_plan(ctypes.Structure):
+    _fields_ = [("orientation", ctypes.c_int), ("block", ctypes.c_int), ("splits_gemm1", ctypes.c_int),
+                ("splits_gemm2", ctypes.c_int), ("act_split", ctypes.c_int), ("kernel_launches", ctypes.c_int),
+                ("workspace_bytes", ctypes.c_size_t)]
 
 
 def _load():
@@ -52,6 +58,8 @@ def _load():
     lib.moe_version.argtypes = []
     lib.moe_workspace_size.restype = i
     lib.moe_workspace_size.argtypes = [i, i, i, i, i, i, i, P, ctypes.POINTER(sz)]
+    lib.moe_plan_info.restype = i
+    lib.moe_plan_info.argtypes = [i, i, i, i, i, i, i, P, ctypes.POINTER(moe_plan)]
     lib.moe_align_capacity.restype = i
     lib.moe_align_capacity.argtypes = [i, i, i, i, ctypes.POINTER(sz), ctypes.POINTER(sz)]
     lib.moe_route.restype = i
@@ -115,6 +123,7 @@ def _opts(options) -> Optional[ctypes.POINTER(moe_options)]:
     o.orientation = int(options.get("orientation", 0))
     o.split_k = int(options.get("split_k", 0))
     o.inject_timeout = int(options.get("inject_timeout", 0))
+    o.act_split = int(options.get("act_split", 0))
     for name, ev in (options.get("stage_begin") or {}).items():
         o.stage_begin[STAGES.index(name)] = ctypes.c_void_p(ev.cuda_event)
     for name, ev in (options.get("stage_end") or {}).items():
@@ -127,6 +136,13 @@ def moe_workspace_size(T: int, H: int, I: int, E: int, topk: int, act_dtype: int
     _check(_lib.moe_workspace_size(T, H, I, E, topk, act_dtype, w_dtype, _opts(options), ctypes.byref(n)),
            "moe_workspace_size")
     return int(n.value)
+
+
+def moe_plan_info(T: int, H: int, I: int, E: int, topk: int, act_dtype: int, w_dtype: int, options=None) -> dict:
+    info = moe_plan()
+    _check(_lib.moe_plan_info(T, H, I, E, topk, act_dtype, w_dtype, _opts(options), ctypes.byref(info)),
+           "moe_plan_info")
+    return {name: getattr(info, name) for name, _ in moe_plan._fields_}
 
 
 def moe_align_capacity(T: int, topk: int, E: int, block: int):

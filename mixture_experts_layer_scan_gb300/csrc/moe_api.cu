@@ -55,6 +55,7 @@ struct Plan {
   int s1 = 1, kb1 = 1, s2 = 1, kb2 = 1;
   int wbox2 = 128;  // token-major GEMM2 weight rows per load (N = 2 * wbox2)
   bool y_bf16 = false;
+  bool act_split = false;  // bf16 intermediate stored as hi + lo parts (two MMAs in GEMM2)
   size_t o_logits = 0, o_tw = 0, o_tid = 0, o_meta = 0, o_sorted = 0, o_eids = 0, o_xs = 0, o_aint = 0, o_af32 = 0,
          o_p1 = 0, o_y = 0, o_misc = 0, total = 0;
   size_t p1_stride = 0, y_stride = 0;
@@ -98,6 +99,8 @@ static int make_plan(int T, int H, int I, int E, int topk, moe_dtype act, moe_dt
   }
   const int orient = opts ? opts->orientation : MOE_ORIENT_AUTO;
   if (orient < 0 || orient > 2) return MOE_ERR_ARG;
+  const int act_mode = opts ? opts->act_split : 0;
+  if (act_mode < 0 || act_mode > 2) return MOE_ERR_ARG;
   const long n = (long)T * topk;
   if (p.path != PATH_F32) {
     if (H % 128 || I % 128) return MOE_ERR_UNSUPPORTED;
@@ -125,8 +128,11 @@ static int make_plan(int T, int H, int I, int E, int topk, moe_dtype act, moe_dt
       p.kb1 = H * eb / 128;
       p.kb2 = I * eb / 128;
       p.wbox2 = (H % 256 == 0) ? 128 : 64;
-      p.y_bf16 = true;
+      p.y_bf16 = false;
     }
+    // hi/lo intermediate: by default where it is free (swap-AB decode streams
+    // weights from HBM; the second MMA only uses idle tensor-core time)
+    p.act_split = p.path == PATH_BF16 && (act_mode == 2 || (act_mode == 0 && p.swap));
   } else {
     p.B = 16;
     p.swap = false;
@@ -149,7 +155,7 @@ static int make_plan(int T, int H, int I, int E, int topk, moe_dtype act, moe_dt
   p.o_sorted = take((size_t)p.cap * 4);
   p.o_eids = take((size_t)std::max<long>(p.nblk_cap, 1) * 4);
   p.o_xs = take((size_t)p.cap * H * xb);
-  p.o_aint = take((size_t)p.cap * I * xb);
+  p.o_aint = take((size_t)p.cap * I * xb * (p.act_split ? 2 : 1));
   if (p.path == PATH_FP8) p.o_af32 = take((size_t)p.cap * I * 4);
   if (p.s1 > 1) {
     p.p1_stride = (size_t)p.cap * 2 * I;
@@ -200,6 +206,27 @@ int moe_workspace_size(int T, int H, int I, int E, int topk, moe_dtype act_dtype
   const int rc = make_plan(T, H, I, E, topk, act_dtype, w_dtype, opts, &p);
   if (rc) return rc;
   *bytes = p.total;
+  return MOE_OK;
+}
+
+int moe_plan_info(int T, int H, int I, int E, int topk, moe_dtype act_dtype, moe_dtype w_dtype,
+                  const moe_options* opts, moe_plan* info) {
+  if (!info) return MOE_ERR_ARG;
+  Plan p;
+  const int rc = make_plan(T, H, I, E, topk, act_dtype, w_dtype, opts, &p);
+  if (rc) return rc;
+  info->orientation = p.path == PATH_F32 ? 0 : (p.swap ? MOE_ORIENT_SWAP_AB : MOE_ORIENT_TOKEN_MAJOR);
+  info->block = p.B;
+  info->splits_gemm1 = p.s1;
+  info->splits_gemm2 = p.s2;
+  info->act_split = p.act_split ? 1 : 0;
+  // router logits, top-k, align, gather, GEMM1, GEMM2, combine (+ amax and
+  // intermediate quantisation on the FP8 path, + the split-K reduction)
+  int n = 7;
+  if (p.path == PATH_FP8) n += 2;
+  if (p.s1 > 1) n += 1;
+  info->kernel_launches = T > 0 ? n : 0;
+  info->workspace_bytes = p.total;
   return MOE_OK;
 }
 
@@ -367,6 +394,7 @@ int moe_forward(const void* hidden, const void* router_w, const void* w13, const
     g1.w_scale = w13_scale;
     g1.a_amax = amax;
     g1.amax_out = amax + 1;
+    void* aint_lo = pl.act_split ? (void*)((uint16_t*)aint + (size_t)cap * I) : nullptr;
     if (pl.s1 > 1) {
       g1.epi = TC_EPI_G1_PART;
       g1.out = p1;
@@ -374,6 +402,7 @@ int moe_forward(const void* hidden, const void* router_w, const void* w13, const
     } else {
       g1.epi = fp8 ? TC_EPI_G1_F32AMAX : TC_EPI_G1_BF16;
       g1.out = fp8 ? (void*)af32 : aint;
+      g1.out_lo = aint_lo;
     }
     if (o) record(o->stage_begin[MOE_STAGE_GEMM1], s);
     MOE_TRY(launch_gemm_tc(g1, s));
@@ -382,8 +411,9 @@ int moe_forward(const void* hidden, const void* router_w, const void* w13, const
     // split-K reduction / FP8 quantisation of the intermediate
     if (o) record(o->stage_begin[MOE_STAGE_ACT], s);
     if (pl.s1 > 1)
-      MOE_TRY(launch_reduce_act(p1, pl.s1, pl.p1_stride, I, pl.B, eids, meta, cap, fp8 ? w13_scale : nullptr, amax,
-                                fp8 ? 1 : 0, fp8 ? (void*)af32 : aint, amax + 1, s));
+      MOE_TRY(launch_reduce_act(p1, pl.s1, pl.p1_stride, I, pl.B, n, sorted, eids, meta, cap,
+                                fp8 ? w13_scale : nullptr, amax, fp8 ? 1 : 0, fp8 ? (void*)af32 : aint, aint_lo, amax + 1,
+                                s));
     if (fp8) MOE_TRY(launch_quant_act(af32, I, meta, cap, amax + 1, (uint8_t*)aint, s));
     if (o) record(o->stage_end[MOE_STAGE_ACT], s);
 
@@ -392,6 +422,7 @@ int moe_forward(const void* hidden, const void* router_w, const void* w13, const
     g2.K = I;
     g2.W = w2;
     g2.X = aint;
+    g2.x_lo_rows = pl.act_split ? cap : 0;
     g2.w_rows_per_expert = H;
     g2.wbox = pl.swap ? 64 : pl.wbox2;
     g2.w_pair_off = g2.wbox;
@@ -416,7 +447,6 @@ int moe_forward(const void* hidden, const void* router_w, const void* w13, const
                          s));
   if (o) record(o->stage_end[MOE_STAGE_COMBINE], s);
 #undef MOE_TRY
-  (void)n;
   return MOE_OK;
 }
 

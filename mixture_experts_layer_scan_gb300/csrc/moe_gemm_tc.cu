@@ -48,11 +48,13 @@ struct TcDev {
   int kb_total, kb_per_split, splits, n_tiles;
   int w_rows_per_expert, w_pair_off, w_tile_rows, wbox, xbox;
   int stages;
+  int x_lo_rows;    // >0: the activation operand also has a bf16 low part at row offset x_lo_rows
   uint32_t stage_bytes, w_bytes, xchg_off, bar_off;
   const int32_t* sorted;
   const int32_t* eids;
   const int32_t* meta;
   void* out;
+  void* out_lo;     // GEMM1: low bf16 part of the intermediate (nullable)
   size_t out_split_stride;
   const float* w_scale;
   const unsigned* a_amax;
@@ -174,6 +176,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tma_load_2d(sw, &tmW, kb * KBLK, d.wr0, fb);
           tma_load_2d(sw + p.wbox * 128, &tmW, kb * KBLK, d.wr0 + p.w_pair_off, fb);
           tma_load_2d(sw + p.w_bytes, &tmX, kb * KBLK, d.xrow, fb);
+          if (p.x_lo_rows) tma_load_2d(sw + p.w_bytes + p.xbox * 128, &tmX, kb * KBLK, d.xrow + p.x_lo_rows, fb);
           ++issued;
           if (++stage == p.stages) {
             stage = 0;
@@ -217,6 +220,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int kk = 0; kk < 4; ++kk)
             tc_mma<FP8>(dt, sdesc_k_sw128(a_base + kk * 32), sdesc_k_sw128(b_base + kk * 32), idesc,
                         (kb > d.kb0 || kk > 0) ? 1u : 0u);
+          if (p.x_lo_rows) {
+            // the low bf16 part of the activations into the same fp32 accumulator:
+            // W (x_hi + x_lo) carries ~16 significant bits of the intermediate
+            const uint32_t lo = sx + p.xbox * 128;
+            const uint32_t a_lo = SWAP ? sw : lo;
+            const uint32_t b_lo = SWAP ? lo : sw;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma<FP8>(dt, sdesc_k_sw128(a_lo + kk * 32), sdesc_k_sw128(b_lo + kk * 32), idesc, 1u);
+          }
           tc_commit(bar_empty + 8 * stage);
           any = true;
           if (++stage == p.stages) {
@@ -276,7 +289,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const float a = silu(v[j] * scale) * (xb[j] * scale);
                 const size_t o = (size_t)(d.xrow + c) * p.I + i;
                 if constexpr (EPI == TC_EPI_G1_BF16) {
-                  reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(a);
+                  const __nv_bfloat16 hi = __float2bfloat16_rn(a);
+                  reinterpret_cast<__nv_bfloat16*>(p.out)[o] = hi;
+                  if (p.out_lo)
+                    reinterpret_cast<__nv_bfloat16*>(p.out_lo)[o] = __float2bfloat16_rn(a - __bfloat162float(hi));
                 } else {
                   reinterpret_cast<float*>(p.out)[o] = a;
                   amax = fmaxf(amax, fabsf(a));
@@ -326,10 +342,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const size_t o = row * p.I + (size_t)d.n * p.wbox + c0;
           if constexpr (EPI == TC_EPI_G1_BF16) {
             uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + o);
-            dst[0] = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
-                                pack_bf16x2(a[6], a[7]));
-            dst[1] = make_uint4(pack_bf16x2(a[8], a[9]), pack_bf16x2(a[10], a[11]), pack_bf16x2(a[12], a[13]),
-                                pack_bf16x2(a[14], a[15]));
+            uint32_t hv[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) hv[j] = pack_bf16x2(a[2 * j], a[2 * j + 1]);
+            dst[0] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+            dst[1] = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+            if (p.out_lo) {
+              uint32_t lv[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                lv[j] = pack_bf16x2(a[2 * j] - bf16_bits_to_f32(hv[j] & 0xffffu),
+                                    a[2 * j + 1] - bf16_bits_to_f32(hv[j] >> 16));
+              uint4* dl = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out_lo) + o);
+              dl[0] = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+              dl[1] = make_uint4(lv[4], lv[5], lv[6], lv[7]);
+            }
           } else {
             float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + o);
 #pragma unroll
@@ -453,7 +480,8 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s) {
   CUtensorMap mw, mx;
   if (!make_map(&mw, a.W, eb, (uint64_t)a.K, (uint64_t)a.E * a.w_rows_per_expert, (uint32_t)a.wbox))
     return cudaErrorInvalidValue;
-  if (!make_map(&mx, a.X, eb, (uint64_t)a.K, (uint64_t)a.cap, (uint32_t)a.xbox)) return cudaErrorInvalidValue;
+  if (!make_map(&mx, a.X, eb, (uint64_t)a.K, (uint64_t)a.cap + (uint64_t)a.x_lo_rows, (uint32_t)a.xbox))
+    return cudaErrorInvalidValue;
 
   TcDev p = {};
   p.epi = a.epi;
@@ -475,6 +503,8 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s) {
   p.eids = a.eids;
   p.meta = a.meta;
   p.out = a.out;
+  p.out_lo = a.out_lo;
+  p.x_lo_rows = a.x_lo_rows;
   p.out_split_stride = a.out_split_stride;
   p.w_scale = a.w_scale;
   p.a_amax = a.a_amax;
@@ -483,7 +513,7 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s) {
 
   const bool xchg = a.swap && (a.epi == TC_EPI_G1_BF16 || a.epi == TC_EPI_G1_F32AMAX);
   p.w_bytes = (uint32_t)(2 * a.wbox * 128);
-  p.stage_bytes = p.w_bytes + (uint32_t)(a.xbox * 128);
+  p.stage_bytes = p.w_bytes + (uint32_t)(a.xbox * 128) * (a.x_lo_rows ? 2u : 1u);
   const uint32_t bar_bytes = 8 * (2 * kMaxStages + 5) + 16;
   const uint32_t budget = 227 * 1024 - 1024 - (xchg ? kXchgBytes : 0) - bar_bytes;
   int stages = (int)(budget / p.stage_bytes);
@@ -512,9 +542,9 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s) {
   MOE_TC_CASE(true, true, TC_EPI_G1_PART)
   MOE_TC_CASE(true, true, TC_EPI_G2_F32)
   MOE_TC_CASE(false, false, TC_EPI_G1_BF16)
-  MOE_TC_CASE(false, false, TC_EPI_G2_BF16)
+  MOE_TC_CASE(false, false, TC_EPI_G2_F32)
   MOE_TC_CASE(false, true, TC_EPI_G1_F32AMAX)
-  MOE_TC_CASE(false, true, TC_EPI_G2_BF16)
+  MOE_TC_CASE(false, true, TC_EPI_G2_F32)
 #undef MOE_TC_CASE
   return cudaErrorInvalidValue;
 }

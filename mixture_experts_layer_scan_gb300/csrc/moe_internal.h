@@ -39,9 +39,12 @@ cudaError_t launch_gather(const void* X, int T, int H, int k, int elem_bytes, in
                           const int32_t* sorted, const int32_t* meta, int cap, void* Xs, cudaStream_t s);
 // split-K reduction of the GEMM1 partials + scale + SiLU(gate)*up.
 //   out_mode 0: bf16 A_int   1: fp32 A (+ amax into amax_bits)
-cudaError_t launch_reduce_act(const float* P, int splits, size_t split_stride, int I, int B, const int32_t* eids,
-                              const int32_t* meta, int cap, const float* w_scale, const unsigned* a_amax_bits,
-                              int out_mode, void* A_out, unsigned* amax_bits, cudaStream_t s);
+// Padding rows (sentinel pairs) become zero and stay out of the amax.
+// out_mode 0 with A_lo != nullptr also writes the low bf16 part a - bf16(a).
+cudaError_t launch_reduce_act(const float* P, int splits, size_t split_stride, int I, int B, int n_pairs,
+                              const int32_t* sorted, const int32_t* eids, const int32_t* meta, int cap,
+                              const float* w_scale, const unsigned* a_amax_bits, int out_mode, void* A_out,
+                              void* A_lo, unsigned* amax_bits, cudaStream_t s);
 // A_q[r][i] = e4m3(A[r][i] / (amax/448)) for r < num_post_pad
 cudaError_t launch_quant_act(const float* A, int I, const int32_t* meta, int cap, const unsigned* amax_bits,
                              uint8_t* Aq, cudaStream_t s);
@@ -88,6 +91,8 @@ struct TcGemmArgs {
   const int32_t* eids;
   const int32_t* meta;
   void* out;
+  void* out_lo;             // GEMM1 bf16: low part of the intermediate, a - bf16(a) (nullable)
+  int x_lo_rows;            // GEMM2: >0 when X holds a low bf16 part at rows [x_lo_rows, x_lo_rows + cap)
   size_t out_split_stride;  // elements between split partial buffers
   const float* w_scale;     // [E] (FP8)
   const unsigned* a_amax;   // amax bits of the activation operand (FP8)

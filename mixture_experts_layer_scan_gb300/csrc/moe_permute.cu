@@ -223,12 +223,25 @@ __global__ void k_gather_quant(const uint4* __restrict__ X, int vec_per_row /* 8
 
 // Split-K reduction of GEMM1 partials (fixed split order), scale, SiLU(gate)*up.
 __global__ void k_reduce_act(const float* __restrict__ P, int splits, size_t split_stride, int I, int B,
+                             int n_pairs, const int32_t* __restrict__ sorted,
                              const int32_t* __restrict__ eids, const int32_t* __restrict__ meta,
                              const float* __restrict__ w_scale, const unsigned* __restrict__ a_amax_bits,
-                             int out_mode, void* __restrict__ A_out, unsigned* __restrict__ amax_bits) {
+                             int out_mode, void* __restrict__ A_out, void* __restrict__ A_lo,
+                             unsigned* __restrict__ amax_bits) {
   const int npp = meta[META_NPP];
   float m = 0.0f;
   for (int r = blockIdx.x; r < npp; r += gridDim.x) {
+    // padding rows were never written by GEMM1: emit zeros, keep them out of the amax
+    if (sorted[r] >= n_pairs) {
+      for (int i = threadIdx.x; i < I; i += blockDim.x) {
+        if (out_mode == 0) {
+          reinterpret_cast<__nv_bfloat16*>(A_out)[(size_t)r * I + i] = __float2bfloat16_rn(0.0f);
+          if (A_lo) reinterpret_cast<__nv_bfloat16*>(A_lo)[(size_t)r * I + i] = __float2bfloat16_rn(0.0f);
+        } else
+          reinterpret_cast<float*>(A_out)[(size_t)r * I + i] = 0.0f;
+      }
+      continue;
+    }
     float scale = 1.0f;
     if (w_scale) scale = e4m3_scale_from_amax(__uint_as_float(*a_amax_bits)) * w_scale[eids[r / B]];
     const float* row = P + (size_t)r * 2 * I;
@@ -241,7 +254,9 @@ __global__ void k_reduce_act(const float* __restrict__ P, int splits, size_t spl
       if (w_scale) { g *= scale; u *= scale; }
       const float a = silu(g) * u;
       if (out_mode == 0) {
-        reinterpret_cast<__nv_bfloat16*>(A_out)[(size_t)r * I + i] = __float2bfloat16_rn(a);
+        const __nv_bfloat16 hi = __float2bfloat16_rn(a);
+        reinterpret_cast<__nv_bfloat16*>(A_out)[(size_t)r * I + i] = hi;
+        if (A_lo) reinterpret_cast<__nv_bfloat16*>(A_lo)[(size_t)r * I + i] = __float2bfloat16_rn(a - __bfloat162float(hi));
       } else {
         reinterpret_cast<float*>(A_out)[(size_t)r * I + i] = a;
         m = fmaxf(m, fabsf(a));
@@ -382,12 +397,13 @@ cudaError_t launch_gather(const void* X, int T, int H, int k, int elem_bytes, in
   return cudaGetLastError();
 }
 
-cudaError_t launch_reduce_act(const float* P, int splits, size_t split_stride, int I, int B, const int32_t* eids,
-                              const int32_t* meta, int cap, const float* w_scale, const unsigned* a_amax_bits,
-                              int out_mode, void* A_out, unsigned* amax_bits, cudaStream_t s) {
+cudaError_t launch_reduce_act(const float* P, int splits, size_t split_stride, int I, int B, int n_pairs,
+                              const int32_t* sorted, const int32_t* eids, const int32_t* meta, int cap,
+                              const float* w_scale, const unsigned* a_amax_bits, int out_mode, void* A_out,
+                              void* A_lo, unsigned* amax_bits, cudaStream_t s) {
   const int grid = cap < 152 * 8 ? (cap > 0 ? cap : 1) : 152 * 8;
-  k_reduce_act<<<grid, 256, 0, s>>>(P, splits, split_stride, I, B, eids, meta, w_scale, a_amax_bits, out_mode, A_out,
-                                    amax_bits);
+  k_reduce_act<<<grid, 256, 0, s>>>(P, splits, split_stride, I, B, n_pairs, sorted, eids, meta, w_scale, a_amax_bits,
+                                    out_mode, A_out, A_lo, amax_bits);
   return cudaGetLastError();
 }
 

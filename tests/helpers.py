@@ -37,12 +37,14 @@ def make_tie_free(layer: dict, min_gap_rel: float = 1e-3, max_rounds: int = 30) 
     raise RuntimeError("could not make routing tie-free")
 
 
-def rel_err(got, ref) -> float:
-    """max |got - ref| / RMS(ref), the layer-output error measure."""
+def rel_err(got, ref, label: str = "") -> float:
+    """max |got - ref| / RMS(ref), the layer-output error measure (printed for the log)."""
     g = np.asarray(got, dtype=np.float64)
     r = np.asarray(ref, dtype=np.float64)
     rms = float(np.sqrt(np.mean(r * r)))
-    return float(np.max(np.abs(g - r))) / (rms if rms > 0 else 1.0)
+    err = float(np.max(np.abs(g - r))) / (rms if rms > 0 else 1.0)
+    print(f"[parity] {label} max|err|/rms = {err:.3e}")
+    return err
 
 
 TOL = {"f32": 1e-5, "bf16": 2e-2, "e4m3": 6e-2}

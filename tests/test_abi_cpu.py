@@ -12,9 +12,9 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def moe():
-    from mixture_experts_layer_scan_gb300 import _build
+    import __graft_entry__
 
-    _build.build()
+    __graft_entry__._builder().build()
     import mixture_experts_layer_scan_gb300 as m
 
     return m
@@ -27,7 +27,7 @@ def _declared():
 
 def test_every_declared_symbol_is_exported(moe):
     names = _declared()
-    assert len(names) >= 9
+    assert len(names) >= 10
     lib = ctypes.CDLL(moe.LIB_PATH)
     for n in names:
         assert hasattr(lib, n), n
@@ -67,6 +67,18 @@ def test_workspace_size_rules(moe):
     with pytest.raises(moe.MoeError) as e:
         moe.moe_workspace_size(64, 4096, 1024, 8, 2, moe.MOE_F32, moe.MOE_BF16)
     assert e.value.code == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_plan_info(moe):
+    d = moe.moe_plan_info(1, 2048, 768, 128, 8, moe.MOE_BF16, moe.MOE_BF16)
+    assert d["orientation"] == moe.ORIENT_SWAP_AB and d["block"] == 16 and d["act_split"] == 1
+    assert d["splits_gemm1"] > 1 and d["kernel_launches"] == 8
+    assert d["workspace_bytes"] == moe.moe_workspace_size(1, 2048, 768, 128, 8, moe.MOE_BF16, moe.MOE_BF16)
+    p = moe.moe_plan_info(8192, 4096, 2048, 64, 8, moe.MOE_BF16, moe.MOE_BF16)
+    assert p["orientation"] == moe.ORIENT_TOKEN_MAJOR and p["block"] == 128 and p["kernel_launches"] == 7
+    f = moe.moe_plan_info(64, 4096, 8192, 64, 8, moe.MOE_BF16, moe.MOE_E4M3)
+    assert f["act_split"] == 0 and f["kernel_launches"] >= 9
+    assert moe.moe_plan_info(64, 256, 512, 8, 2, moe.MOE_F32, moe.MOE_F32)["orientation"] == 0
 
 
 def test_align_capacity(moe):

@@ -77,6 +77,13 @@ def test_bf16_split_k(moe, splits):
     assert rel_err(out.float().cpu().numpy(), _ref(L)) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("orient,act_split", [(1, 1), (2, 2), (1, 2)])
+def test_bf16_intermediate_single_or_hi_lo(moe, orient, act_split):
+    L = _layer("mixtral_decode", T=40, H=384, I=256, E=8, k=2)
+    out = _run(moe, L, {"orientation": orient, "act_split": act_split})
+    assert rel_err(out.float().cpu().numpy(), _ref(L), f"orient={orient} act_split={act_split}") <= TOL["bf16"]
+
+
 def test_swap_ab_identity_both_orientations(moe):
     """C = A B computed as (B^T A^T)^T: the two operand placements agree with each other and the oracle."""
     L = _layer("mixtral_decode", T=48, H=256, I=256, E=8, k=2)
