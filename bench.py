@@ -245,6 +245,8 @@ def run_ours(args, rank, world, dev):
         for _ in range(kk):
             b = {n: torch.cuda.Event(enable_timing=True) for n in moe.STAGES}
             e = {n: torch.cuda.Event(enable_timing=True) for n in moe.STAGES}
+            for ev in list(b.values()) + list(e.values()):
+                ev.record(stream)  # torch creates the CUDA event on first record; the library re-records it
             stage_ev.append((b, e))
         for b, e in stage_ev:
             if flush:
