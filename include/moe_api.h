@@ -199,6 +199,33 @@ MOE_API int moe_forward(const void* hidden, const void* router_w, const void* w1
                 const float* w2_scale, void* out, void* workspace, size_t workspace_bytes, const moe_options* opts,
                 moe_stream_t stream);
 
+/* Allocation-free form of moe_forward (the pages have no counterpart; it is an
+ * interface convenience of this library).
+ *
+ * For callers that cannot allocate device memory when they run the layer --
+ * a plugin whose host engine owns and plans all device memory, a serving loop
+ * that may not take cudaMalloc's latency or implicit synchronisation, a C
+ * caller without a device allocator.  Same arguments and results as
+ * moe_forward, without the workspace: the workspace is a fixed array of
+ * MOE_NOALLOC_MAX_WORKSPACE bytes in this library's device memory, which every
+ * GPU that loads the library keeps until the process exits.
+ *  - Shapes whose moe_workspace_size() exceeds MOE_NOALLOC_MAX_WORKSPACE are
+ *    rejected with MOE_ERR_WORKSPACE before anything is enqueued (decode
+ *    batches of the usual sizes fit; prefill batches do not -- use moe_forward).
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) and caches it; make that first call before any
+ *    stream capture on that device.
+ *  - Every call on a device uses the same array and finds the previous call's
+ *    contents in it; the layer initialises what it reads, so nothing needs
+ *    clearing.  Calls whose GPU work overlaps (different streams, or several
+ *    host threads) race on the array: issue them on one stream.
+ *  - Allocates nothing, frees nothing, and calls no allocating library routine. */
+#define MOE_NOALLOC_MAX_WORKSPACE (32u << 20)
+MOE_API int moe_forward_noalloc(const void* hidden, const void* router_w, const void* w13, const void* w2, int T, int H,
+                                int I, int E, int topk, int renorm, moe_dtype act_dtype, moe_dtype w_dtype,
+                                const float* w13_scale, const float* w2_scale, void* out, const moe_options* opts,
+                                moe_stream_t stream);
+
 /* Synchronises `stream`, then reads and clears this device's status word.
  * Returns MOE_OK, MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_DEVICE_INDEX or MOE_ERR_CUDA. */
 MOE_API int moe_get_status(moe_stream_t stream);

@@ -26,7 +26,9 @@ NUM_STAGES = len(STAGES)
 
 # every entry point include/moe_api.h declares
 EXPORTS = ("moe_strerror", "moe_workspace_size", "moe_plan_info", "moe_align_capacity", "moe_route",
-           "moe_topk_from_logits", "moe_align", "moe_forward", "moe_get_status", "moe_version")
+           "moe_topk_from_logits", "moe_align", "moe_forward", "moe_forward_noalloc", "moe_get_status",
+           "moe_version")
+NOALLOC_MAX_WORKSPACE = 32 << 20
 
 
 class MoeError(RuntimeError):
@@ -70,6 +72,8 @@ def _load():
     lib.moe_align.argtypes = [P, i, i, i, i, P, P, P, P, P]
     lib.moe_forward.restype = i
     lib.moe_forward.argtypes = [P, P, P, P, i, i, i, i, i, i, i, i, P, P, P, P, sz, P, P]
+    lib.moe_forward_noalloc.restype = i
+    lib.moe_forward_noalloc.argtypes = [P, P, P, P, i, i, i, i, i, i, i, i, P, P, P, P, P]
     lib.moe_get_status.restype = i
     lib.moe_get_status.argtypes = [P]
     return lib
@@ -206,6 +210,25 @@ def moe_forward(hidden: torch.Tensor, router_w: torch.Tensor, w13: torch.Tensor,
     _check(_lib.moe_forward(_p(hidden), _p(router_w), _p(w13), _p(w2), T, H, I, E, topk, int(bool(renorm)), act, wdt,
                             _p(w13_scale), _p(w2_scale), _p(out), _p(workspace), workspace.numel(), opts,
                             _stream(stream)), "moe_forward")
+    return out
+
+
+def moe_forward_noalloc(hidden: torch.Tensor, router_w: torch.Tensor, w13: torch.Tensor, w2: torch.Tensor, topk: int,
+                        renorm: bool, w13_scale=None, w2_scale=None, out=None, options=None, stream=None):
+    """moe_forward without a workspace argument, for callers that cannot allocate device memory.
+
+    The library keeps the workspace in its own fixed device array (NOALLOC_MAX_WORKSPACE bytes per
+    device); larger shapes raise MoeError(MOE_ERR_WORKSPACE).  Pass `out` to allocate nothing here either.
+    """
+    T, H = hidden.shape
+    E, twoI, H2 = w13.shape
+    I = twoI // 2
+    if H2 != H or w2.shape != (E, H, I) or router_w.shape != (E, H):
+        raise ValueError("inconsistent shapes")
+    out = torch.empty_like(hidden) if out is None else out
+    _check(_lib.moe_forward_noalloc(_p(hidden), _p(router_w), _p(w13), _p(w2), T, H, I, E, topk, int(bool(renorm)),
+                                    _dt(hidden), _dt(w13), _p(w13_scale), _p(w2_scale), _p(out), _opts(options),
+                                    _stream(stream)), "moe_forward_noalloc")
     return out
 
 
