@@ -144,7 +144,9 @@ MOE_API int moe_align_capacity(int T, int topk, int E, int block, size_t* sorted
  *   descending order, equal values ranked by lower expert index (ranking is on
  *   the fp32 logit, which orders like p); topk_w[T][topk] (fp32) = p of those
  *   experts, divided by their sum when renorm != 0.
- * hidden and router_w have type act_dtype (MOE_F32 or MOE_BF16).
+ * hidden and router_w have type act_dtype (MOE_F32 or MOE_BF16); H must be a multiple
+ * of 8 (bf16) or 4 (fp32).  Long bf16 batches (T >= 256, E <= 256, H % 128 == 0) run the
+ * logits on the tensor cores, shorter ones on the CUDA cores; both accumulate in fp32.
  * Limits: 1 <= topk <= min(E, 32), E <= 1024. */
 MOE_API int moe_route(const void* hidden, const void* router_w, int T, int H, int E, int topk, int renorm,
               moe_dtype act_dtype, float* logits_out, float* topk_w, int32_t* topk_ids, moe_stream_t stream);

@@ -40,9 +40,11 @@ static int num_sms() {
   return sms[dev];
 }
 
-// Target CTA count used to choose K splits.  A fixed constant (twice the 152
-// SMs of a GB300) so that the workspace size depends only on the arguments.
-constexpr int kSplitTargetCtas = 2 * 152;
+// SM count used to plan K splits.  A fixed constant (the 152 SMs of a GB300)
+// so that the workspace size depends only on the arguments.
+constexpr int kPlanSms = 152;
+// Router logits go through the tensor-core GEMM from this many tokens on.
+constexpr int kRouterTcMinTokens = 256;
 
 enum Path { PATH_F32 = 0, PATH_BF16 = 1, PATH_FP8 = 2 };
 
@@ -63,16 +65,28 @@ struct Plan {
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// K splits of a swap-AB GEMM with base_tiles (expert x 128-row) tiles of
+// kb_total 128-byte K blocks.  The persistent kernel gives each CTA
+// ceil(tiles / SMs) tiles, so the step time follows
+//   ceil(base_tiles * s / SMs) * (ceil(kb_total / s) + 1)
+// (the +1 stands for the per-tile fill and epilogue); take the s in [1, 16]
+// with at least 2 K blocks per split that minimises it, fewest splits on ties.
 static int choose_splits(long base_tiles, int kb_total, int forced) {
-  int s;
-  if (forced > 0) {
-    s = forced;
-  } else {
-    s = (int)((kSplitTargetCtas + base_tiles - 1) / std::max<long>(base_tiles, 1));
-    s = std::min(s, std::max(1, kb_total / 4));
+  if (forced > 0) return std::max(1, std::min(forced, kb_total));
+  int best = 1;
+  long best_t = -1;
+  for (int s = 1; s <= 16 && s <= std::max(1, kb_total / 2); ++s) {
+    const int kbs = (kb_total + s - 1) / s;
+    const int se = (kb_total + kbs - 1) / kbs;
+    if (se != s) continue;
+    const long waves = (base_tiles * s + kPlanSms - 1) / kPlanSms;
+    const long t = waves * (kbs + 1);
+    if (best_t < 0 || t < best_t) {
+      best_t = t;
+      best = s;
+    }
   }
-  s = std::max(1, std::min(s, kb_total));
-  return s;
+  return best;
 }
 
 static int check_shape(int T, int H, int I, int E, int topk) {
@@ -158,7 +172,7 @@ static int make_plan(int T, int H, int I, int E, int topk, moe_dtype act, moe_dt
   p.o_aint = take((size_t)p.cap * I * xb * (p.act_split ? 2 : 1));
   if (p.path == PATH_FP8) p.o_af32 = take((size_t)p.cap * I * 4);
   if (p.s1 > 1) {
-    p.p1_stride = (size_t)p.cap * 2 * I;
+    p.p1_stride = (size_t)n * 2 * I;
     p.o_p1 = take(p.p1_stride * p.s1 * 4);
   }
   p.y_stride = (size_t)n * H;
@@ -175,6 +189,41 @@ static int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_C
 
 static void record(moe_event_t ev, cudaStream_t s) {
   if (ev) cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev), s);
+}
+
+// Router logits: the tensor-core GEMM for long bf16 batches (128 tokens per
+// tile, all experts in the N slot), the CUDA-core kernel otherwise.
+static cudaError_t launch_router(const void* X, const void* Wr, int T, int H, int E, moe_dtype act, float* logits,
+                                 int* status, cudaStream_t s) {
+  const int sms = num_sms();
+  if (act == MOE_BF16 && T >= kRouterTcMinTokens && E <= 256 && H % 128 == 0 && sms > 0) {
+    TcGemmArgs g = {};
+    g.swap = false;
+    g.fp8 = false;
+    g.epi = TC_EPI_LOGITS;
+    g.T = T;
+    g.k = 1;
+    g.E = 1;
+    g.H = H;
+    g.K = H;
+    g.W = Wr;
+    g.w_rows_per_expert = E;
+    g.wbox = ((E + 15) / 16 * 16) / 2;
+    g.w_pair_off = g.wbox;
+    g.w_tile_rows = 0;
+    g.xbox = 128;
+    g.n_tiles = 1;
+    g.splits = 1;
+    g.kb_per_split = H * 2 / 128;
+    g.cap = T;
+    g.X = X;
+    g.out = logits;
+    g.n_valid = E;
+    g.status = status;
+    g.num_sms = sms;
+    return launch_gemm_tc(g, s);
+  }
+  return launch_router_logits(X, Wr, T, H, E, act == MOE_BF16, logits, s);
 }
 
 }  // namespace moe
@@ -244,13 +293,16 @@ int moe_route(const void* hidden, const void* router_w, int T, int H, int E, int
               moe_dtype act_dtype, float* logits_out, float* topk_w, int32_t* topk_ids, moe_stream_t stream) {
   if (T < 0 || H < 1 || E < 1 || E > 1024 || topk < 1 || topk > E || topk > 32) return MOE_ERR_ARG;
   if (act_dtype != MOE_F32 && act_dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (H % (act_dtype == MOE_BF16 ? 8 : 4)) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
   if (!hidden || !router_w || !logits_out || !topk_w || !topk_ids) return MOE_ERR_ARG;
   if (misaligned(hidden) || misaligned(router_w) || misaligned(logits_out) || misaligned(topk_w) ||
       misaligned(topk_ids))
     return MOE_ERR_ALIGNMENT;
+  int* st = status_word();
+  if (!st) return MOE_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_router_logits(hidden, router_w, T, H, E, act_dtype == MOE_BF16, logits_out, s);
+  cudaError_t e = launch_router(hidden, router_w, T, H, E, act_dtype, logits_out, st, s);
   if (e == cudaSuccess) e = launch_topk(logits_out, T, E, topk, renorm != 0, topk_w, topk_ids, s);
   return cuda_rc(e);
 }
@@ -331,7 +383,7 @@ int moe_forward(const void* hidden, const void* router_w, const void* w13, const
 
   // 1-2. router
   if (o) record(o->stage_begin[MOE_STAGE_ROUTE], s);
-  MOE_TRY(launch_router_logits(hidden, router_w, T, H, E, act_dtype == MOE_BF16, logits, s));
+  MOE_TRY(launch_router(hidden, router_w, T, H, E, act_dtype, logits, st, s));
   MOE_TRY(launch_topk(logits, T, E, topk, renorm != 0, tw, tid, s));
   if (o) record(o->stage_end[MOE_STAGE_ROUTE], s);
 

@@ -12,6 +12,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "moe_api.h"
 
 namespace moe {
@@ -225,8 +227,40 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 }
 
 // Programmatic dependent launch: wait for the preceding kernel's results /
-// allow the next kernel to start its prologue.
+// allow the next kernel to start its prologue.  Every kernel of the layer is
+// launched with programmatic stream serialisation; each one lets its
+// dependents launch early and calls pdl_wait() before it reads anything the
+// previous kernel wrote (the wait returns once that kernel has completed and
+// its memory is visible), so only launch latency and prologues overlap.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_enter() {
+  pdl_launch_dependents();
+  pdl_wait();
+}
+
+// Host: launch a kernel with programmatic stream serialisation allowed.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// launch_pdl(...) inside a function returning cudaError_t: return the error if any.
+#define MOE_LAUNCH(...)                                  \
+  do {                                                   \
+    const cudaError_t moe_launch_err_ = launch_pdl(__VA_ARGS__); \
+    if (moe_launch_err_ != cudaSuccess) return moe_launch_err_;  \
+  } while (0)
 
 }  // namespace moe

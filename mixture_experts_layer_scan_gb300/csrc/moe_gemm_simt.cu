@@ -19,6 +19,7 @@ constexpr int kKc = 32;    // reduction chunk
 __global__ void __launch_bounds__(256) k_gemm1_simt(const float* __restrict__ Xs, const float* __restrict__ W13,
                                                     int H, int I, const int32_t* __restrict__ eids,
                                                     const int32_t* __restrict__ meta, float* __restrict__ A) {
+  pdl_enter();
   __shared__ float xs[kRows][kKc + 1];
   __shared__ float wg[kCols][kKc + 1];
   __shared__ float wu[kCols][kKc + 1];
@@ -63,6 +64,7 @@ __global__ void __launch_bounds__(256) k_gemm2_simt(const float* __restrict__ A,
                                                     int H, int I, int n_pairs, const int32_t* __restrict__ sorted,
                                                     const int32_t* __restrict__ eids,
                                                     const int32_t* __restrict__ meta, float* __restrict__ Y) {
+  pdl_enter();
   __shared__ float as[kRows][kKc + 1];
   __shared__ float ws[kCols][kKc + 1];
   const int b = blockIdx.x;
@@ -105,7 +107,7 @@ cudaError_t launch_gemm1_simt(const float* Xs, const float* W13, int H, int I, i
                               const int32_t* meta, int cap, float* A, cudaStream_t s) {
   if (B != kRows) return cudaErrorInvalidValue;
   dim3 grid(cap / kRows, (I + kCols - 1) / kCols);
-  k_gemm1_simt<<<grid, 256, 0, s>>>(Xs, W13, H, I, eids, meta, A);
+  MOE_LAUNCH(k_gemm1_simt, dim3(grid), dim3(256), 0, s, Xs, W13, H, I, eids, meta, A);
   return cudaGetLastError();
 }
 
@@ -114,7 +116,7 @@ cudaError_t launch_gemm2_simt(const float* A, const float* W2, int H, int I, int
                               cudaStream_t s) {
   if (B != kRows) return cudaErrorInvalidValue;
   dim3 grid(cap / kRows, (H + kCols - 1) / kCols);
-  k_gemm2_simt<<<grid, 256, 0, s>>>(A, W2, H, I, T * k, sorted, eids, meta, Y);
+  MOE_LAUNCH(k_gemm2_simt, dim3(grid), dim3(256), 0, s, A, W2, H, I, T * k, sorted, eids, meta, Y);
   return cudaGetLastError();
 }
 

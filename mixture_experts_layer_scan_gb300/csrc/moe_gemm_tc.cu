@@ -48,6 +48,7 @@ struct TcDev {
   int kb_total, kb_per_split, splits, n_tiles;
   int w_rows_per_expert, w_pair_off, w_tile_rows, wbox, xbox;
   int stages;
+  int n_valid;      // router: valid output columns
   int x_lo_rows;    // >0: the activation operand also has a bf16 low part at row offset x_lo_rows
   uint32_t stage_bytes, w_bytes, xchg_off, bar_off;
   const int32_t* sorted;
@@ -66,18 +67,32 @@ struct Tile {
   int e, xrow, ntok, npad, wr0, kb0, kb1, n, s;
 };
 
-template <bool SWAP>
+template <bool SWAP, int EPI>
 __device__ __forceinline__ int tile_count(const TcDev& p) {
-  if constexpr (SWAP)
+  if constexpr (EPI == TC_EPI_LOGITS)
+    return (p.T + 127) / 128;
+  else if constexpr (SWAP)
     return p.meta[META_NACT] * p.n_tiles * p.splits;
   else
     return (p.meta[META_NPP] / 128) * p.n_tiles;
 }
 
-template <bool SWAP>
+template <bool SWAP, int EPI>
 __device__ __forceinline__ Tile tile_at(const TcDev& p, int t) {
   Tile d;
-  if constexpr (SWAP) {
+  if constexpr (EPI == TC_EPI_LOGITS) {
+    // router: 128 consecutive (unsorted) tokens against all experts
+    d.n = 0;
+    d.s = 0;
+    d.e = 0;
+    d.xrow = t * 128;
+    d.ntok = 128;
+    d.npad = 128;
+    d.kb0 = 0;
+    d.kb1 = p.kb_total;
+    d.wr0 = 0;
+    return d;
+  } else if constexpr (SWAP) {
     const int per_e = p.n_tiles * p.splits;
     const int a = t / per_e;
     const int rem = t - a * per_e;
@@ -152,29 +167,48 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  // Everything below reads the routing results of the preceding kernels.
-  pdl_wait();
-  const int ntiles = tile_count<SWAP>(p);
+  // The tile list comes from the permutation metadata, which was complete
+  // before the preceding kernel started; only the activation tiles (and, in
+  // the epilogue, the FP8 scale) depend on the preceding kernel.
+  const int ntiles = tile_count<SWAP, EPI>(p);
   constexpr int KBLK = FP8 ? 128 : 64;  // elements per 128-byte K block
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer ----------------
+      // Expert weights do not depend on the preceding kernel: stream the first
+      // stages of weight tiles before waiting for it (programmatic dependent
+      // launch), so this kernel's HBM stream starts while the previous one drains.
+      int pre = 0;
+      if ((int)blockIdx.x < ntiles) {
+        const Tile d = tile_at<SWAP, EPI>(p, blockIdx.x);
+        pre = min(p.stages, d.kb1 - d.kb0);
+        for (int i = 0; i < pre; ++i) {
+          const uint32_t sw = sbase + i * p.stage_bytes;
+          const uint32_t fb = bar_full + 8 * i;
+          mbar_arrive_expect_tx(fb, p.stage_bytes);
+          tma_load_2d(sw, &tmW, (d.kb0 + i) * KBLK, d.wr0, fb);
+          tma_load_2d(sw + p.wbox * 128, &tmW, (d.kb0 + i) * KBLK, d.wr0 + p.w_pair_off, fb);
+        }
+      }
+      pdl_wait();
       int stage = 0;
       uint32_t phase = 0, issued = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-        const Tile d = tile_at<SWAP>(p, t);
+        const Tile d = tile_at<SWAP, EPI>(p, t);
         for (int kb = d.kb0; kb < d.kb1; ++kb) {
-          if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
           const uint32_t sw = sbase + stage * p.stage_bytes;
           const uint32_t fb = bar_full + 8 * stage;
-          mbar_arrive_expect_tx(fb, p.stage_bytes);
-          tma_load_2d(sw, &tmW, kb * KBLK, d.wr0, fb);
-          tma_load_2d(sw + p.wbox * 128, &tmW, kb * KBLK, d.wr0 + p.w_pair_off, fb);
+          if ((int)issued >= pre) {  // (the first `pre` stages already hold their weight tiles)
+            if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(fb, p.stage_bytes);
+            tma_load_2d(sw, &tmW, kb * KBLK, d.wr0, fb);
+            tma_load_2d(sw + p.wbox * 128, &tmW, kb * KBLK, d.wr0 + p.w_pair_off, fb);
+          }
           tma_load_2d(sw + p.w_bytes, &tmX, kb * KBLK, d.xrow, fb);
           if (p.x_lo_rows) tma_load_2d(sw + p.w_bytes + p.xbox * 128, &tmX, kb * KBLK, d.xrow + p.x_lo_rows, fb);
           ++issued;
@@ -184,6 +218,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
       }
+      // every load of this CTA is issued: the next kernel may start its prologue
+      pdl_launch_dependents();
       if (!ok) {  // let the copies already in flight land before the CTA exits
         const uint32_t first = issued > (uint32_t)p.stages ? issued - p.stages : 0u;
         for (uint32_t i = first; i < issued; ++i)
@@ -193,11 +229,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
+      pdl_wait();
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true, any = false;
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-        const Tile d = tile_at<SWAP>(p, t);
+        const Tile d = tile_at<SWAP, EPI>(p, t);
         const int N = SWAP ? d.npad : 2 * p.wbox;
         const uint32_t idesc = idesc_make(128, N, FP8);
         if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag, p.status)) {
@@ -251,6 +288,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
+    pdl_wait();
     const int q = warp & 3;        // tensor-memory lane quadrant this warp may read
     const int lrow = q * 32 + lane; // accumulator row of this thread
     float a_scale = 1.0f;
@@ -260,7 +298,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint32_t acc_phase = 0;
     const int n_pairs = p.T * p.k;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
-      const Tile d = tile_at<SWAP>(p, t);
+      const Tile d = tile_at<SWAP, EPI>(p, t);
       const bool ok = mbar_wait(bar_tfull + 8 * acc, acc_phase, abort_flag, p.status);
       if (epi_any(!ok)) break;
       tc_fence_after();
@@ -303,7 +341,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         named_bar_sync(1, 128);  // exchange buffers free for the next tile
       } else if constexpr (SWAP && EPI == TC_EPI_G1_PART) {
-        // raw fp32 split partial: P[s][row][col], col = i (gate) or I + i (up)
+        // raw fp32 split partial: P[s][pair][col], col = i (gate) or I + i (up)
         const int col = (lrow < 64) ? d.n * 64 + lrow : p.I + d.n * 64 + (lrow - 64);
         float* P = reinterpret_cast<float*>(p.out) + (size_t)d.s * p.out_split_stride;
         for (int c0 = 0; c0 < d.npad; c0 += 16) {
@@ -311,7 +349,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tmem_ld16(tb + (uint32_t)c0, v);
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            if (c0 + j < d.ntok) P[(size_t)(d.xrow + c0 + j) * (2 * p.I) + col] = v[j];
+            if (c0 + j < d.ntok) P[(size_t)p.sorted[d.xrow + c0 + j] * (2 * p.I) + col] = v[j];
         }
       } else if constexpr (SWAP && EPI == TC_EPI_G2_F32) {
         // Y[s][pair][h], h = n*128 + lrow, pair = sorted[xrow + c]
@@ -365,6 +403,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(a[j]));
           }
         }
+      } else if constexpr (EPI == TC_EPI_LOGITS) {
+        const int row = d.xrow + lrow;
+        const int ncols = 2 * p.wbox;
+        for (int c0 = 0; c0 < ncols; c0 += 16) {
+          float v[16];
+          tmem_ld16(tb + (uint32_t)c0, v);
+          if (row < p.T) {
+            float* dst = reinterpret_cast<float*>(p.out) + (size_t)row * p.n_valid;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (c0 + j < p.n_valid) dst[c0 + j] = v[j];
+          }
+        }
       } else if constexpr (!SWAP && (EPI == TC_EPI_G2_BF16 || EPI == TC_EPI_G2_F32)) {
         const int f = p.sorted[d.xrow + lrow];
         const int ncols = 2 * p.wbox;
@@ -404,7 +455,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   }
 
-  pdl_launch_dependents();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -503,6 +553,7 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s) {
   p.eids = a.eids;
   p.meta = a.meta;
   p.out = a.out;
+  p.n_valid = a.n_valid;
   p.out_lo = a.out_lo;
   p.x_lo_rows = a.x_lo_rows;
   p.out_split_stride = a.out_split_stride;
@@ -525,7 +576,9 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s) {
   const size_t smem = 1024 + (size_t)p.bar_off + bar_bytes;
 
   long upper;
-  if (a.swap)
+  if (a.epi == TC_EPI_LOGITS)
+    upper = (a.T + 127) / 128;
+  else if (a.swap)
     upper = (long)std::min(a.E, a.T * a.k) * a.n_tiles * a.splits;
   else
     upper = (long)(a.cap / 128) * a.n_tiles;
@@ -545,6 +598,7 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s) {
   MOE_TC_CASE(false, false, TC_EPI_G2_F32)
   MOE_TC_CASE(false, true, TC_EPI_G1_F32AMAX)
   MOE_TC_CASE(false, true, TC_EPI_G2_F32)
+  MOE_TC_CASE(false, false, TC_EPI_LOGITS)
 #undef MOE_TC_CASE
   return cudaErrorInvalidValue;
 }

@@ -37,7 +37,8 @@ cudaError_t launch_amax_bf16(const void* X, size_t n, unsigned* amax_bits, cudaS
 // mode 0: copy elements of elem_bytes; mode 1: bf16 -> e4m3 with scale amax/448
 cudaError_t launch_gather(const void* X, int T, int H, int k, int elem_bytes, int mode, const unsigned* amax_bits,
                           const int32_t* sorted, const int32_t* meta, int cap, void* Xs, cudaStream_t s);
-// split-K reduction of the GEMM1 partials + scale + SiLU(gate)*up.
+// split-K reduction of the GEMM1 partials P[split][pair][2I] + scale + SiLU(gate)*up
+// into sorted rows (row r holds pair sorted[r]).
 //   out_mode 0: bf16 A_int   1: fp32 A (+ amax into amax_bits)
 // Padding rows (sentinel pairs) become zero and stay out of the amax.
 // out_mode 0 with A_lo != nullptr also writes the low bf16 part a - bf16(a).
@@ -62,10 +63,11 @@ cudaError_t launch_gemm2_simt(const float* A, const float* W2, int H, int I, int
 // ---- tcgen05 grouped GEMM --------------------------------------------------------
 enum TcEpilogue {
   TC_EPI_G1_BF16 = 0,    // GEMM1: SiLU(gate)*up -> bf16 A_int
-  TC_EPI_G1_PART = 1,    // GEMM1: raw fp32 partials [split][row][2I] (gate cols [0,I), up [I,2I))
+  TC_EPI_G1_PART = 1,    // GEMM1: raw fp32 partials [split][pair][2I] (gate cols [0,I), up [I,2I))
   TC_EPI_G1_F32AMAX = 2, // GEMM1: scaled SiLU(gate)*up -> fp32 A + amax (FP8 path)
   TC_EPI_G2_F32 = 3,     // GEMM2: fp32 Y[split][pair][H]
-  TC_EPI_G2_BF16 = 4     // GEMM2: bf16 Y[pair][H]
+  TC_EPI_G2_BF16 = 4,    // GEMM2: bf16 Y[pair][H]
+  TC_EPI_LOGITS = 5      // router: fp32 logits[T][n_valid] of unsorted token rows (token-major only)
 };
 
 struct TcGemmArgs {
@@ -83,7 +85,8 @@ struct TcGemmArgs {
   int n_tiles;      // output tiles per expert (or per 128-row block)
   int splits;       // K splits (swap mode)
   int kb_per_split; // k-blocks (128 bytes of K) per split
-  int cap;          // rows of the sorted activation buffer
+  int cap;          // rows of the sorted activation buffer (T for the router)
+  int n_valid;      // router: number of output columns (experts) to store
   // tensors
   const void* W;    // weights viewed as [E * w_rows_per_expert][K]
   const void* X;    // sorted activations [cap][K]

@@ -6,8 +6,13 @@
 // section 3.1: the fused design sorts tokens by expert, builds an index of
 // which rows belong to which expert, computes, then reorders and sums the
 // results with the routing weights.
+#include <algorithm>
+#include <cooperative_groups.h>
+
 #include "moe_device.cuh"
 #include "moe_internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace moe {
 
@@ -46,25 +51,37 @@ __device__ int block_exclusive_scan(int v, int* scratch /* >= 33 ints */, int* t
   return res;
 }
 
-// One CTA of 1024 threads.  Warp w owns the contiguous chunk of flat pair
-// indices [w*L, (w+1)*L).  Pass 1 counts, per warp and expert, with warp
-// match (no atomics, so the counts do not depend on timing); the per-expert
-// prefix over warps then gives every warp its first slot, so pass 2 writes
-// each pair at a position that preserves ascending flat index inside an
-// expert (a stable counting sort).
+// Stable counting sort of the (token, slot) pairs by expert, run by one
+// thread-block cluster of `csize` CTAs x 1024 threads (csize = 1 for decode
+// batches).  CTA r owns the contiguous chunk r of the flat pair indices and
+// its warp w the contiguous sub-chunk w of that.  Pass 1 counts per warp and
+// expert with warp match (no atomics, so counts do not depend on timing).
+// Each CTA then reads the other CTAs' per-expert totals straight from their
+// shared memory (distributed shared memory of the cluster), which gives every
+// warp its first slot inside every expert; pass 2 writes each pair there, so
+// inside an expert the flat indices stay in ascending order.  No global
+// scratch is needed.
 __global__ void __launch_bounds__(kAlignThreads, 1)
     k_align(const int32_t* __restrict__ ids, int T, int k, int E, int B, int32_t* __restrict__ sorted,
             int32_t* __restrict__ eids, int32_t* __restrict__ npp_out, int32_t* __restrict__ counts_out,
             int32_t* __restrict__ meta, int* status) {
+  pdl_enter();
+  cg::cluster_group cluster = cg::this_cluster();
+  const int csize = (int)cluster.num_blocks();
+  const int crank = (int)cluster.block_rank();
   extern __shared__ int sm[];
   int* wc = sm;                       // [kAlignWarps][E] per-warp counts, then per-warp bases
-  int* off = wc + kAlignWarps * E;    // [E+1] padded offsets
-  int* cnt = off + E + 1;             // [E]
-  int* scan_tmp = cnt + E;            // [33]
+  int* ctot = wc + kAlignWarps * E;   // [E] this CTA's per-expert counts (read by the whole cluster)
+  int* off = ctot + E;                // [E+1] padded offsets
+  int* cnt = off + E + 1;             // [E] per-expert counts of the whole batch
+  int* cbase = cnt + E;               // [E] pairs of this expert in lower-ranked CTAs
+  int* scan_tmp = cbase + E;          // [33]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int n = T * k;
-  const int L = (n + kAlignWarps - 1) / kAlignWarps;
-  const int beg = min(n, warp * L), end = min(n, beg + L);
+  const int C = (n + csize - 1) / csize;
+  const int cbeg = min(n, crank * C), cend = min(n, cbeg + C);
+  const int L = (cend - cbeg + kAlignWarps - 1) / kAlignWarps;
+  const int beg = min(cend, cbeg + warp * L), end = min(cend, beg + L);
 
   for (int i = threadIdx.x; i < kAlignWarps * E; i += blockDim.x) wc[i] = 0;
   __syncthreads();
@@ -85,7 +102,7 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
   if (bad) report(status, MOE_ERR_DEVICE_INDEX);
   __syncthreads();
 
-  // per-expert totals and per-warp bases (exclusive over warps)
+  // this CTA's totals and per-warp bases (exclusive over warps)
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int run = 0;
     for (int w = 0; w < kAlignWarps; ++w) {
@@ -93,11 +110,22 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
       wc[w * E + e] = run;
       run += c;
     }
-    cnt[e] = run;
+    ctot[e] = run;
   }
-  __syncthreads();
+  cluster.sync();  // every CTA's ctot is complete
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int tot = 0, below = 0;
+    for (int r = 0; r < csize; ++r) {
+      const int v = *cluster.map_shared_rank(ctot + e, r);
+      if (r < crank) below += v;
+      tot += v;
+    }
+    cnt[e] = tot;
+    cbase[e] = below;
+  }
+  cluster.sync();  // remote reads done: no CTA touches another's shared memory after this
 
-  // padded offsets and active list (E <= 1024 = blockDim)
+  // padded offsets and active list (E <= 1024 = blockDim); identical in every CTA
   {
     const int e = threadIdx.x;
     const int c = (e < E) ? cnt[e] : 0;
@@ -107,21 +135,25 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
     const int a = block_exclusive_scan(c > 0 ? 1 : 0, scan_tmp, &total_act);
     if (e < E) {
       off[e] = o;
-      if (meta) {
-        meta[meta_offsets(E) + e] = o;
-        meta[meta_counts(E) + e] = c;
-        if (c > 0) meta[meta_active(E) + a] = e;
+      if (crank == 0) {
+        if (meta) {
+          meta[meta_offsets(E) + e] = o;
+          meta[meta_counts(E) + e] = c;
+          if (c > 0) meta[meta_active(E) + a] = e;
+        }
+        if (counts_out) counts_out[e] = c;
       }
-      if (counts_out) counts_out[e] = c;
     }
     if (e == 0) {
       off[E] = total_pad;
-      *npp_out = total_pad;
-      if (meta) {
-        meta[META_NPP] = total_pad;
-        meta[META_NBLK] = total_pad / B;
-        meta[META_NACT] = total_act;
-        meta[meta_offsets(E) + E] = total_pad;
+      if (crank == 0) {
+        *npp_out = total_pad;
+        if (meta) {
+          meta[META_NPP] = total_pad;
+          meta[META_NBLK] = total_pad / B;
+          meta[META_NACT] = total_act;
+          meta[meta_offsets(E) + E] = total_pad;
+        }
       }
     }
   }
@@ -137,7 +169,7 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
     }
     const unsigned grp = __match_any_sync(0xffffffffu, e);
     int slot = 0;
-    if (e >= 0) slot = off[e] + wc[warp * E + e] + __popc(grp & ((1u << lane) - 1u));
+    if (e >= 0) slot = off[e] + cbase[e] + wc[warp * E + e] + __popc(grp & ((1u << lane) - 1u));
     __syncwarp();
     if (e >= 0) {
       sorted[slot] = f;
@@ -146,18 +178,16 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
     __syncwarp();
   }
 
-  // block -> expert map and sentinel padding
+  // block -> expert map and sentinel padding, blocks spread over the cluster
   const int total = off[E];
   const int nblk = total / B;
-  for (int b = threadIdx.x; b < nblk; b += blockDim.x) {
-    int lo = 0, hi = E - 1;  // last expert with off[e] <= b*B
+  for (int b = crank * blockDim.x + threadIdx.x; b < nblk; b += csize * blockDim.x) {
+    int lo = 0, hi = E - 1;  // last expert with off[e] <= b*B: the owner of block b
     const int pos = b * B;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (off[mid] <= pos) lo = mid; else hi = mid - 1;
     }
-    // skip empty experts sharing the same offset: the owner has off[e] <= pos < off[e+1]
-    while (lo < E - 1 && off[lo + 1] <= pos) ++lo;
     eids[b] = lo;
     const int fill_from = max(pos, off[lo] + cnt[lo]);
     for (int q = fill_from; q < pos + B; ++q) sorted[q] = n;
@@ -167,6 +197,7 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
 // amax over n bf16 values (bit pattern of a non-negative float, atomicMax on
 // the bits is order independent).
 __global__ void k_amax_bf16(const uint16_t* __restrict__ X, size_t n, unsigned* amax_bits) {
+  pdl_enter();
   float m = 0.0f;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
     m = fmaxf(m, fabsf(bf16_bits_to_f32(X[i])));
@@ -180,6 +211,7 @@ __global__ void k_amax_bf16(const uint16_t* __restrict__ X, size_t n, unsigned* 
 __global__ void k_gather_copy(const uint4* __restrict__ X, int vec_per_row, int k, int n_pairs,
                               const int32_t* __restrict__ sorted, const int32_t* __restrict__ meta,
                               uint4* __restrict__ Xs) {
+  pdl_enter();
   const int npp = meta[META_NPP];
   for (int r = blockIdx.x; r < npp; r += gridDim.x) {
     const int f = sorted[r];
@@ -197,6 +229,7 @@ __global__ void k_gather_copy(const uint4* __restrict__ X, int vec_per_row, int 
 __global__ void k_gather_quant(const uint4* __restrict__ X, int vec_per_row /* 8 bf16 each */, int k, int n_pairs,
                                const int32_t* __restrict__ sorted, const int32_t* __restrict__ meta,
                                const unsigned* __restrict__ amax_bits, uint2* __restrict__ Xq) {
+  pdl_enter();
   const int npp = meta[META_NPP];
   const float s = e4m3_scale_from_amax(__uint_as_float(*amax_bits));
   for (int r = blockIdx.x; r < npp; r += gridDim.x) {
@@ -228,11 +261,13 @@ __global__ void k_reduce_act(const float* __restrict__ P, int splits, size_t spl
                              const float* __restrict__ w_scale, const unsigned* __restrict__ a_amax_bits,
                              int out_mode, void* __restrict__ A_out, void* __restrict__ A_lo,
                              unsigned* __restrict__ amax_bits) {
+  pdl_enter();
   const int npp = meta[META_NPP];
   float m = 0.0f;
   for (int r = blockIdx.x; r < npp; r += gridDim.x) {
-    // padding rows were never written by GEMM1: emit zeros, keep them out of the amax
-    if (sorted[r] >= n_pairs) {
+    // padding rows have no partials: emit zeros, keep them out of the amax
+    const int f = sorted[r];
+    if (f >= n_pairs) {
       for (int i = threadIdx.x; i < I; i += blockDim.x) {
         if (out_mode == 0) {
           reinterpret_cast<__nv_bfloat16*>(A_out)[(size_t)r * I + i] = __float2bfloat16_rn(0.0f);
@@ -244,7 +279,7 @@ __global__ void k_reduce_act(const float* __restrict__ P, int splits, size_t spl
     }
     float scale = 1.0f;
     if (w_scale) scale = e4m3_scale_from_amax(__uint_as_float(*a_amax_bits)) * w_scale[eids[r / B]];
-    const float* row = P + (size_t)r * 2 * I;
+    const float* row = P + (size_t)f * 2 * I;  // partials are indexed by pair
     for (int i = threadIdx.x; i < I; i += blockDim.x) {
       float g = 0.0f, u = 0.0f;
       for (int s = 0; s < splits; ++s) {
@@ -273,6 +308,7 @@ __global__ void k_reduce_act(const float* __restrict__ P, int splits, size_t spl
 // A_q = e4m3(A / s), s = amax/448, rows below num_post_pad.
 __global__ void k_quant_act(const float4* __restrict__ A, int vec_per_row, const int32_t* __restrict__ meta,
                             const unsigned* __restrict__ amax_bits, uint32_t* __restrict__ Aq) {
+  pdl_enter();
   const int npp = meta[META_NPP];
   const float s = e4m3_scale_from_amax(__uint_as_float(*amax_bits));
   const size_t total = (size_t)npp * vec_per_row;
@@ -283,48 +319,79 @@ __global__ void k_quant_act(const float4* __restrict__ A, int vec_per_row, const
   }
 }
 
-// out[t][h] = sum_j w[t][j] * (sum_s Y[s][t*k+j][h]) in j order then s order,
-// fp32, one rounding at the end.  4 consecutive h per thread.
+// out[t][h] = sum_j w[t][j] * (sum_s Y[s][t*k+j][h]): splits summed in s order,
+// then the k routed outputs accumulated in j order, fp32, one rounding at the
+// end.  8 consecutive h per thread; the loads of four (j, s) rows are issued
+// before their use so each thread keeps 8 x 16 bytes in flight.
+template <bool Y_BF16>
+__device__ __forceinline__ void load8(const void* Yv, size_t idx, float (&y)[8]) {
+  if constexpr (Y_BF16) {
+    const uint4 v = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(Yv) + idx);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      y[2 * i] = bf16_bits_to_f32(w[i] & 0xffffu);
+      y[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+    }
+  } else {
+    const float4 a = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(Yv) + idx);
+    const float4 b = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(Yv) + idx + 4);
+    y[0] = a.x; y[1] = a.y; y[2] = a.z; y[3] = a.w;
+    y[4] = b.x; y[5] = b.y; y[6] = b.z; y[7] = b.w;
+  }
+}
+
 template <bool Y_BF16, bool OUT_BF16>
-__global__ void k_combine(const void* __restrict__ Yv, int splits, size_t split_stride, const float* __restrict__ w,
-                          int T, int k, int H, void* __restrict__ out) {
-  const int hv = H / 4;
+__global__ void __launch_bounds__(256) k_combine(const void* __restrict__ Yv, int splits, size_t split_stride,
+                                                 const float* __restrict__ w, int T, int k, int H,
+                                                 void* __restrict__ out) {
+  pdl_enter();
+  const int hv = H / 8;
   const size_t total = (size_t)T * hv;
+  const int rows = k * splits;  // (j, s) rows, j-major
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
-    const int t = (int)(i / hv), h = (int)(i % hv) * 4;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < k; ++j) {
-      const size_t f = (size_t)t * k + j;
-      float y[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int s = 0; s < splits; ++s) {
-        if constexpr (Y_BF16) {
-          const uint2 v = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(Yv) +
-                                                          (size_t)s * split_stride + f * H + h);
-          y[0] += bf16_bits_to_f32(v.x & 0xffffu);
-          y[1] += bf16_bits_to_f32(v.x >> 16);
-          y[2] += bf16_bits_to_f32(v.y & 0xffffu);
-          y[3] += bf16_bits_to_f32(v.y >> 16);
-        } else {
-          const float4 v = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(Yv) +
-                                                            (size_t)s * split_stride + f * H + h);
-          y[0] += v.x;
-          y[1] += v.y;
-          y[2] += v.z;
-          y[3] += v.w;
+    const int t = (int)(i / hv), h = (int)(i % hv) * 8;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float yj[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int r0 = 0; r0 < rows; r0 += 4) {
+      float y[4][8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int r = r0 + q;
+        if (r < rows) {
+          const int j = r / splits, sp = r - j * splits;
+          load8<Y_BF16>(Yv, (size_t)sp * split_stride + ((size_t)t * k + j) * H + h, y[q]);
         }
       }
-      const float wj = w[f];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) acc[q] = fmaf(wj, y[q], acc[q]);
+      for (int q = 0; q < 4; ++q) {
+        const int r = r0 + q;
+        if (r < rows) {
+          const int j = r / splits, sp = r - j * splits;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) yj[c] += y[q][c];
+          if (sp == splits - 1) {
+            const float wj = w[(size_t)t * k + j];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              acc[c] = fmaf(wj, yj[c], acc[c]);
+              yj[c] = 0.f;
+            }
+          }
+        }
+      }
     }
     if constexpr (OUT_BF16) {
-      uint2 o;
+      uint4 o;
       o.x = pack_bf16x2(acc[0], acc[1]);
       o.y = pack_bf16x2(acc[2], acc[3]);
-      *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(out) + (size_t)t * H + h) = o;
+      o.z = pack_bf16x2(acc[4], acc[5]);
+      o.w = pack_bf16x2(acc[6], acc[7]);
+      *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(out) + (size_t)t * H + h) = o;
     } else {
-      *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + (size_t)t * H + h) =
-          make_float4(acc[0], acc[1], acc[2], acc[3]);
+      float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + (size_t)t * H + h);
+      dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
     }
   }
 }
@@ -333,6 +400,7 @@ __global__ void k_combine(const void* __restrict__ Yv, int splits, size_t split_
 template <bool Y_BF16, bool OUT_BF16>
 __global__ void k_combine_scalar(const void* __restrict__ Yv, int splits, size_t split_stride,
                                  const float* __restrict__ w, int T, int k, int H, void* __restrict__ out) {
+  pdl_enter();
   const size_t total = (size_t)T * H;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
     const int t = (int)(i / H), h = (int)(i % H);
@@ -366,7 +434,7 @@ int grid_for(size_t work, int threads, int cap_blocks = 152 * 16) {
 
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int B, int32_t* sorted, int32_t* eids,
                          int32_t* npp, int32_t* counts, int32_t* meta, int* status, cudaStream_t s) {
-  const size_t smem = (size_t)(kAlignWarps * E + 2 * E + 1 + 33) * sizeof(int);
+  const size_t smem = (size_t)(kAlignWarps * E + 4 * E + 1 + 33) * sizeof(int);
   static bool configured[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -375,12 +443,26 @@ cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int B, int32_t
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  k_align<<<1, kAlignThreads, smem, s>>>(ids, T, k, E, B, sorted, eids, npp, counts, meta, status);
-  return cudaGetLastError();
+  // one CTA up to 4096 pairs, then a cluster of up to 8 CTAs (about 4096 pairs each)
+  const long n = (long)T * k;
+  const int csize = (int)std::min<long>(8, std::max<long>(1, (n + 4095) / 4096));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(csize);
+  cfg.blockDim = dim3(kAlignThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = csize;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_align, ids, T, k, E, B, sorted, eids, npp, counts, meta, status);
 }
 
 cudaError_t launch_amax_bf16(const void* X, size_t n, unsigned* amax_bits, cudaStream_t s) {
-  k_amax_bf16<<<grid_for(n, 256), 256, 0, s>>>((const uint16_t*)X, n, amax_bits);
+  MOE_LAUNCH(k_amax_bf16, dim3(grid_for(n, 256)), dim3(256), 0, s, (const uint16_t*)X, n, amax_bits);
   return cudaGetLastError();
 }
 
@@ -389,10 +471,10 @@ cudaError_t launch_gather(const void* X, int T, int H, int k, int elem_bytes, in
   const int grid = cap < 152 * 8 ? (cap > 0 ? cap : 1) : 152 * 8;
   if (mode == 0) {
     const int vpr = H * elem_bytes / 16;
-    k_gather_copy<<<grid, 128, 0, s>>>((const uint4*)X, vpr, k, T * k, sorted, meta, (uint4*)Xs);
+    MOE_LAUNCH(k_gather_copy, dim3(grid), dim3(128), 0, s, (const uint4*)X, vpr, k, T * k, sorted, meta, (uint4*)Xs);
   } else {
     const int vpr = H / 8;
-    k_gather_quant<<<grid, 128, 0, s>>>((const uint4*)X, vpr, k, T * k, sorted, meta, amax_bits, (uint2*)Xs);
+    MOE_LAUNCH(k_gather_quant, dim3(grid), dim3(128), 0, s, (const uint4*)X, vpr, k, T * k, sorted, meta, amax_bits, (uint2*)Xs);
   }
   return cudaGetLastError();
 }
@@ -402,7 +484,7 @@ cudaError_t launch_reduce_act(const float* P, int splits, size_t split_stride, i
                               const float* w_scale, const unsigned* a_amax_bits, int out_mode, void* A_out,
                               void* A_lo, unsigned* amax_bits, cudaStream_t s) {
   const int grid = cap < 152 * 8 ? (cap > 0 ? cap : 1) : 152 * 8;
-  k_reduce_act<<<grid, 256, 0, s>>>(P, splits, split_stride, I, B, n_pairs, sorted, eids, meta, w_scale, a_amax_bits,
+  MOE_LAUNCH(k_reduce_act, dim3(grid), dim3(256), 0, s, P, splits, split_stride, I, B, n_pairs, sorted, eids, meta, w_scale, a_amax_bits,
                                     out_mode, A_out, A_lo, amax_bits);
   return cudaGetLastError();
 }
@@ -410,25 +492,25 @@ cudaError_t launch_reduce_act(const float* P, int splits, size_t split_stride, i
 cudaError_t launch_quant_act(const float* A, int I, const int32_t* meta, int cap, const unsigned* amax_bits,
                              uint8_t* Aq, cudaStream_t s) {
   const int vpr = I / 4;
-  k_quant_act<<<grid_for((size_t)cap * vpr, 256), 256, 0, s>>>((const float4*)A, vpr, meta, amax_bits,
+  MOE_LAUNCH(k_quant_act, dim3(grid_for((size_t)cap * vpr, 256)), dim3(256), 0, s, (const float4*)A, vpr, meta, amax_bits,
                                                                (uint32_t*)Aq);
   return cudaGetLastError();
 }
 
 cudaError_t launch_combine(const void* Y, int y_bf16, int splits, size_t split_stride, const float* w, int T, int k,
                            int H, void* out, int out_bf16, cudaStream_t s) {
-  if (H % 4 == 0) {
-    const int grid = grid_for((size_t)T * (H / 4), 256);
-    if (y_bf16 && out_bf16) k_combine<true, true><<<grid, 256, 0, s>>>(Y, splits, split_stride, w, T, k, H, out);
-    else if (y_bf16) k_combine<true, false><<<grid, 256, 0, s>>>(Y, splits, split_stride, w, T, k, H, out);
-    else if (out_bf16) k_combine<false, true><<<grid, 256, 0, s>>>(Y, splits, split_stride, w, T, k, H, out);
-    else k_combine<false, false><<<grid, 256, 0, s>>>(Y, splits, split_stride, w, T, k, H, out);
+  if (H % 8 == 0) {
+    const int grid = grid_for((size_t)T * (H / 8), 256);
+    if (y_bf16 && out_bf16) MOE_LAUNCH(k_combine<true, true>, dim3(grid), dim3(256), 0, s, Y, splits, split_stride, w, T, k, H, out);
+    else if (y_bf16) MOE_LAUNCH(k_combine<true, false>, dim3(grid), dim3(256), 0, s, Y, splits, split_stride, w, T, k, H, out);
+    else if (out_bf16) MOE_LAUNCH(k_combine<false, true>, dim3(grid), dim3(256), 0, s, Y, splits, split_stride, w, T, k, H, out);
+    else MOE_LAUNCH(k_combine<false, false>, dim3(grid), dim3(256), 0, s, Y, splits, split_stride, w, T, k, H, out);
   } else {
     const int grid = grid_for((size_t)T * H, 256);
-    if (y_bf16 && out_bf16) k_combine_scalar<true, true><<<grid, 256, 0, s>>>(Y, splits, split_stride, w, T, k, H, out);
-    else if (y_bf16) k_combine_scalar<true, false><<<grid, 256, 0, s>>>(Y, splits, split_stride, w, T, k, H, out);
-    else if (out_bf16) k_combine_scalar<false, true><<<grid, 256, 0, s>>>(Y, splits, split_stride, w, T, k, H, out);
-    else k_combine_scalar<false, false><<<grid, 256, 0, s>>>(Y, splits, split_stride, w, T, k, H, out);
+    if (y_bf16 && out_bf16) MOE_LAUNCH(k_combine_scalar<true, true>, dim3(grid), dim3(256), 0, s, Y, splits, split_stride, w, T, k, H, out);
+    else if (y_bf16) MOE_LAUNCH(k_combine_scalar<true, false>, dim3(grid), dim3(256), 0, s, Y, splits, split_stride, w, T, k, H, out);
+    else if (out_bf16) MOE_LAUNCH(k_combine_scalar<false, true>, dim3(grid), dim3(256), 0, s, Y, splits, split_stride, w, T, k, H, out);
+    else MOE_LAUNCH(k_combine_scalar<false, false>, dim3(grid), dim3(256), 0, s, Y, splits, split_stride, w, T, k, H, out);
   }
   return cudaGetLastError();
 }

@@ -14,63 +14,70 @@ namespace moe {
 namespace {
 
 constexpr int kRouterWarps = 8;
-constexpr int kRouterTT = 4;    // tokens per CTA
-constexpr int kRouterEPW = 2;   // experts per warp
-constexpr int kRouterHC = 1024; // hidden columns staged per pass
+constexpr int kRouterTT = 4;  // tokens per CTA
 
-// logits[t][e] = sum_h X[t][h] * Wr[e][h]; a CTA covers kRouterTT tokens and
-// kRouterWarps*kRouterEPW experts, staging the token rows in shared memory.
-// Each lane accumulates a strided slice of h; the warp then reduces with a
-// fixed butterfly, so the result does not depend on scheduling.
+// 16-byte vector of router inputs, widened to fp32.
+__device__ __forceinline__ void load16(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = bf16_bits_to_f32(w[i] & 0xffffu);
+    v[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+  }
+}
+__device__ __forceinline__ void load16(const float* p, float (&v)[4]) {
+  const float4 u = *reinterpret_cast<const float4*>(p);
+  v[0] = u.x;
+  v[1] = u.y;
+  v[2] = u.z;
+  v[3] = u.w;
+}
+
+// logits[t][e] = sum_h X[t][h] * Wr[e][h] on the CUDA cores (decode batches and
+// the fp32 layer).  A CTA owns one expert and kRouterTT tokens; its 8 warps
+// split H into interleaved 16-byte vectors (one pass over Wr[e] per CTA),
+// each warp reduces with a fixed butterfly and the 8 warp sums are added in
+// warp order, so the result does not depend on scheduling.
 template <typename TIn>
 __global__ void __launch_bounds__(kRouterWarps * 32) k_router_logits(const TIn* __restrict__ X,
                                                                       const TIn* __restrict__ Wr, int T, int H, int E,
                                                                       float* __restrict__ logits) {
-  __shared__ float xs[kRouterTT][kRouterHC];
+  pdl_enter();
+  constexpr int V = 16 / sizeof(TIn);
+  __shared__ float red[kRouterWarps][kRouterTT];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t0 = blockIdx.x * kRouterTT;
-  const int e0 = (blockIdx.y * kRouterWarps + warp) * kRouterEPW;
-  float acc[kRouterEPW][kRouterTT];
+  const int t0 = blockIdx.x * kRouterTT, e = blockIdx.y;
+  const int nt = min(kRouterTT, T - t0);
+  float acc[kRouterTT];
 #pragma unroll
-  for (int a = 0; a < kRouterEPW; ++a)
+  for (int b = 0; b < kRouterTT; ++b) acc[b] = 0.0f;
+  const TIn* w = Wr + (size_t)e * H;
+  for (int h = (warp * 32 + lane) * V; h < H; h += kRouterWarps * 32 * V) {
+    float wv[V];
+    load16(w + h, wv);
 #pragma unroll
-    for (int b = 0; b < kRouterTT; ++b) acc[a][b] = 0.0f;
-
-  for (int hc = 0; hc < H; hc += kRouterHC) {
-    const int hn = min(kRouterHC, H - hc);
-    __syncthreads();
-    for (int i = threadIdx.x; i < kRouterTT * kRouterHC; i += blockDim.x) {
-      const int tt = i / kRouterHC, h = i % kRouterHC;
-      xs[tt][h] = (t0 + tt < T && h < hn) ? to_f32(X[(size_t)(t0 + tt) * H + hc + h]) : 0.0f;
-    }
-    __syncthreads();
+    for (int b = 0; b < kRouterTT; ++b) {
+      if (b < nt) {
+        float xv[V];
+        load16(X + (size_t)(t0 + b) * H + h, xv);
 #pragma unroll
-    for (int a = 0; a < kRouterEPW; ++a) {
-      const int e = e0 + a;
-      if (e >= E) break;
-      const TIn* w = Wr + (size_t)e * H + hc;
-      for (int h = lane; h < hn; h += 32) {
-        const float wv = to_f32(w[h]);
-#pragma unroll
-        for (int b = 0; b < kRouterTT; ++b) acc[a][b] = fmaf(wv, xs[b][h], acc[a][b]);
+        for (int q = 0; q < V; ++q) acc[b] = fmaf(wv[q], xv[q], acc[b]);
       }
     }
   }
 #pragma unroll
-  for (int a = 0; a < kRouterEPW; ++a)
+  for (int b = 0; b < kRouterTT; ++b) {
 #pragma unroll
-    for (int b = 0; b < kRouterTT; ++b)
+    for (int off = 16; off > 0; off >>= 1) acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], off);
+    if (lane == 0) red[warp][b] = acc[b];
+  }
+  __syncthreads();
+  if (threadIdx.x < nt) {
+    float sum = 0.0f;
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) acc[a][b] += __shfl_xor_sync(0xffffffffu, acc[a][b], off);
-  if (lane == 0) {
-#pragma unroll
-    for (int a = 0; a < kRouterEPW; ++a) {
-      const int e = e0 + a;
-      if (e >= E) break;
-#pragma unroll
-      for (int b = 0; b < kRouterTT; ++b)
-        if (t0 + b < T) logits[(size_t)(t0 + b) * E + e] = acc[a][b];
-    }
+    for (int w8 = 0; w8 < kRouterWarps; ++w8) sum += red[w8][threadIdx.x];
+    logits[(size_t)(t0 + threadIdx.x) * E + e] = sum;
   }
 }
 
@@ -84,6 +91,7 @@ __device__ __forceinline__ bool ranks_before(float v, int i, float bv, int bi) {
 // already taken.  Lane j keeps the j-th pick.
 __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, int T, int E, int k, int renorm,
                                               float* __restrict__ topk_w, int32_t* __restrict__ topk_ids) {
+  pdl_enter();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + warp;
   if (t >= T) return;
@@ -142,19 +150,19 @@ __global__ void k_inject_timeout(const int* flag, int* status) {
 
 cudaError_t launch_router_logits(const void* X, const void* Wr, int T, int H, int E, bool bf16, float* logits,
                                  cudaStream_t s) {
-  dim3 grid((T + kRouterTT - 1) / kRouterTT, (E + kRouterWarps * kRouterEPW - 1) / (kRouterWarps * kRouterEPW));
+  dim3 grid((T + kRouterTT - 1) / kRouterTT, E);
   if (bf16)
-    k_router_logits<__nv_bfloat16><<<grid, kRouterWarps * 32, 0, s>>>(
+    MOE_LAUNCH(k_router_logits<__nv_bfloat16>, dim3(grid), dim3(kRouterWarps * 32), 0, s, 
         (const __nv_bfloat16*)X, (const __nv_bfloat16*)Wr, T, H, E, logits);
   else
-    k_router_logits<float><<<grid, kRouterWarps * 32, 0, s>>>((const float*)X, (const float*)Wr, T, H, E, logits);
+    MOE_LAUNCH(k_router_logits<float>, dim3(grid), dim3(kRouterWarps * 32), 0, s, (const float*)X, (const float*)Wr, T, H, E, logits);
   return cudaGetLastError();
 }
 
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int renorm, float* w, int32_t* ids,
                         cudaStream_t s) {
   const int warps = 8;
-  k_topk<<<(T + warps - 1) / warps, warps * 32, 0, s>>>(logits, T, E, k, renorm, w, ids);
+  MOE_LAUNCH(k_topk, dim3((T + warps - 1) / warps), dim3(warps * 32), 0, s, logits, T, E, k, renorm, w, ids);
   return cudaGetLastError();
 }
 

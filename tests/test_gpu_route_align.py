@@ -56,6 +56,21 @@ def test_route_matches_oracle(moe, name, T):
     np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=1e-4, atol=1e-6)
 
 
+@pytest.mark.parametrize("T,H,E,k", [(256, 256, 40, 6), (300, 384, 256, 8), (1000, 128, 8, 2), (255, 256, 64, 8),
+                                     (257, 512, 16, 4)])
+def test_route_tensor_core_and_cuda_core_paths(moe, T, H, E, k):
+    """T >= 256 bf16 batches take the tcgen05 logits GEMM (E in the N slot, masked to E); shorter ones the CUDA cores."""
+    sp = spec("prefill", T=T, H=H, E=E, k=k)
+    L = make_layer(sp, weights=False)
+    make_tie_free(L)
+    logits, w, ids = moe.moe_route(L["X"].cuda(), L["Wr"].cuda(), k, True)
+    ref_lg = oracle.router_logits(L["X"], L["Wr"])
+    rid, rw = oracle.topk(ref_lg, k, True)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    bound = (H + 2) * 2.0 ** -24 * (np.abs(L["X"].double().numpy()) @ np.abs(L["Wr"].double().numpy()).T)
+    assert np.all(np.abs(logits.cpu().numpy() - ref_lg) <= bound)
+
+
 def _random_ids(T, k, E, seed, skew=False):
     rng = np.random.default_rng(seed)
     if skew:
