@@ -71,7 +71,9 @@ static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 //   ceil(base_tiles * s / SMs) * (ceil(kb_total / s) + 1)
 // (the +1 stands for the per-tile fill and epilogue); take the s in [1, 16]
 // with at least 2 K blocks per split that minimises it, fewest splits on ties.
-static int choose_splits(long base_tiles, int kb_total, int forced) {
+// split_penalty (in K blocks) charges an extra reduction kernel, if splitting
+// needs one.
+static int choose_splits(long base_tiles, int kb_total, int forced, int split_penalty) {
   if (forced > 0) return std::max(1, std::min(forced, kb_total));
   int best = 1;
   long best_t = -1;
@@ -80,7 +82,7 @@ static int choose_splits(long base_tiles, int kb_total, int forced) {
     const int se = (kb_total + kbs - 1) / kbs;
     if (se != s) continue;
     const long waves = (base_tiles * s + kPlanSms - 1) / kPlanSms;
-    const long t = waves * (kbs + 1);
+    const long t = waves * (kbs + 1) + (s > 1 ? split_penalty : 0);
     if (best_t < 0 || t < best_t) {
       best_t = t;
       best = s;
@@ -128,10 +130,11 @@ static int make_plan(int T, int H, int I, int E, int topk, moe_dtype act, moe_dt
       const int forced = opts ? opts->split_k : 0;
       if (forced < 0) return MOE_ERR_ARG;
       const int kbt1 = H * eb / 128, kbt2 = I * eb / 128;
-      p.s1 = choose_splits(act_upper * (I / 64), kbt1, forced);
+      // swap-AB tiles: 128 gate + 128 up rows (GEMM1), 256 rows of w2 (GEMM2)
+      p.s1 = choose_splits(act_upper * (I / 128), kbt1, forced, 8);
       p.kb1 = (kbt1 + p.s1 - 1) / p.s1;
       p.s1 = (kbt1 + p.kb1 - 1) / p.kb1;
-      p.s2 = choose_splits(act_upper * (H / 128), kbt2, forced);
+      p.s2 = choose_splits(act_upper * ((H + 255) / 256), kbt2, forced, 0);
       p.kb2 = (kbt2 + p.s2 - 1) / p.s2;
       p.s2 = (kbt2 + p.kb2 - 1) / p.kb2;
       p.y_bf16 = false;
@@ -437,10 +440,10 @@ int moe_forward(const void* hidden, const void* router_w, const void* w13, const
     g1.X = xs;
     g1.w_rows_per_expert = 2 * I;
     g1.w_pair_off = I;
-    g1.wbox = pl.swap ? 64 : 128;
-    g1.w_tile_rows = g1.wbox;
+    g1.wbox = 128;
+    g1.w_tile_rows = 128;
     g1.xbox = pl.xbox;
-    g1.n_tiles = I / g1.wbox;
+    g1.n_tiles = I / 128;
     g1.splits = pl.s1;
     g1.kb_per_split = pl.kb1;
     g1.w_scale = w13_scale;
@@ -476,11 +479,11 @@ int moe_forward(const void* hidden, const void* router_w, const void* w13, const
     g2.X = aint;
     g2.x_lo_rows = pl.act_split ? cap : 0;
     g2.w_rows_per_expert = H;
-    g2.wbox = pl.swap ? 64 : pl.wbox2;
+    g2.wbox = pl.swap ? 128 : pl.wbox2;
     g2.w_pair_off = g2.wbox;
     g2.w_tile_rows = 2 * g2.wbox;
     g2.xbox = pl.xbox;
-    g2.n_tiles = H / g2.w_tile_rows;
+    g2.n_tiles = (H + g2.w_tile_rows - 1) / g2.w_tile_rows;
     g2.splits = pl.s2;
     g2.kb_per_split = pl.kb2;
     g2.w_scale = w2_scale;

@@ -16,17 +16,20 @@
 //               global stores
 //
 // Orientation.  In swap-AB mode (thin decode batches) the MMA computes
-// C^T[N,M] = B^T[N,K] A^T[K,M]: 128 expert weight rows occupy the M slot and
-// the expert's few tokens (padded to 16) the N slot, so no tensor-core row is
+// C^T[N,M] = B^T[N,K] A^T[K,M]: expert weight rows occupy the M slot and the
+// expert's few tokens (padded to 16) the N slot, so no tensor-core row is
 // spent on empty token rows (page 1, section "Swap-AB pour l'utilisation de
 // WGMMA", Figure 1: the large expert N dimension moved into the fixed-size
-// operand slot; Hopper's slot is 64 rows, tcgen05's is 128).  In token-major
-// mode (prefill) 128 sorted token rows fill M and 256 weight rows N.
+// operand slot; Hopper's slot is 64 rows, tcgen05's is 128).  A swap-AB tile
+// is 256 weight rows, issued as two M = 128 MMAs (accumulators D0 and D1)
+// against one shared activation tile, so each stage's activation bytes serve
+// twice the weight bytes.  In token-major mode (prefill) 128 sorted token rows
+// fill M and 256 weight rows N.
 //
 // The weight tile is two TMA loads of `wbox` rows.  For GEMM1 they are the
-// gate rows and the matching up rows, so SiLU(gate)*up pairs values of one
-// tile: in token-major mode inside one thread (columns c and wbox+c), in
-// swap-AB mode across TMEM lanes i and 64+i through shared memory.
+// gate rows and the matching up rows, so SiLU(gate)*up pairs values held by
+// one thread: TMEM lane i of D0 and D1 in swap-AB mode, columns c and wbox+c
+// in token-major mode.
 #include <mutex>
 
 #include "moe_device.cuh"
@@ -38,9 +41,7 @@ namespace {
 
 constexpr int kTcThreads = 192;
 constexpr int kMaxStages = 8;
-constexpr int kXchgStride = 17;                           // floats per exchange row (16 + 1 pad)
-constexpr uint32_t kXchgBytes = 2 * 64 * kXchgStride * 4; // double-buffered 64 x 16 fp32
-constexpr uint32_t kTmemCols = 512;                       // two 256-column accumulators
+constexpr uint32_t kTmemCols = 512;  // all of tensor memory: accumulator buffers
 
 struct TcDev {
   int epi;
@@ -48,9 +49,12 @@ struct TcDev {
   int kb_total, kb_per_split, splits, n_tiles;
   int w_rows_per_expert, w_pair_off, w_tile_rows, wbox, xbox;
   int stages;
+  int nbuf;         // accumulator buffers (2: epilogue of one tile overlaps the next; 1 for wide swap tiles)
+  int buf_cols;     // tensor-memory columns per buffer
+  int d1_col;       // swap-AB: column of accumulator D1 (weight rows 128..255) inside a buffer
   int n_valid;      // router: valid output columns
   int x_lo_rows;    // >0: the activation operand also has a bf16 low part at row offset x_lo_rows
-  uint32_t stage_bytes, w_bytes, xchg_off, bar_off;
+  uint32_t stage_bytes, w_bytes, bar_off;
   const int32_t* sorted;
   const int32_t* eids;
   const int32_t* meta;
@@ -143,7 +147,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t bar_drain = bar_tempty + 16;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + p.bar_off + 8 * (2 * kMaxStages + 5));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* xchg = reinterpret_cast<float*>(smem + p.xchg_off);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -154,7 +157,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_tfull + 8 * b, 1);
       mbar_init(bar_tempty + 8 * b, 128);
-    }
+    }  // (buffer 1 unused when nbuf == 1)
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -242,7 +245,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t dt = tmem_base + (uint32_t)acc * 256u;
+        const uint32_t dt = tmem_base + (uint32_t)(acc * p.buf_cols);
         for (int kb = d.kb0; kb < d.kb1; ++kb) {
           if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.status)) {
             ok = false;
@@ -251,21 +254,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc_fence_after();
           const uint32_t sw = sbase + stage * p.stage_bytes;
           const uint32_t sx = sw + p.w_bytes;
-          const uint32_t a_base = SWAP ? sw : sx;
-          const uint32_t b_base = SWAP ? sx : sw;
+          // the optional low bf16 part of the activations goes into the same fp32
+          // accumulator: W (x_hi + x_lo) carries ~16 significant bits of the intermediate
+          const int parts = p.x_lo_rows ? 2 : 1;
+          for (int part = 0; part < parts; ++part) {
+            const uint32_t sxp = sx + (uint32_t)(part * p.xbox * 128);
+            if constexpr (SWAP) {
+              // D0 += W[rows 0..127] X^T, D1 += W[rows 128..255] X^T
+              const uint32_t w1 = sw + (uint32_t)(p.wbox * 128);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc_mma<FP8>(dt, sdesc_k_sw128(a_base + kk * 32), sdesc_k_sw128(b_base + kk * 32), idesc,
-                        (kb > d.kb0 || kk > 0) ? 1u : 0u);
-          if (p.x_lo_rows) {
-            // the low bf16 part of the activations into the same fp32 accumulator:
-            // W (x_hi + x_lo) carries ~16 significant bits of the intermediate
-            const uint32_t lo = sx + p.xbox * 128;
-            const uint32_t a_lo = SWAP ? sw : lo;
-            const uint32_t b_lo = SWAP ? lo : sw;
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t acc_in = (part > 0 || kb > d.kb0 || kk > 0) ? 1u : 0u;
+                const uint64_t bdesc = sdesc_k_sw128(sxp + kk * 32);
+                tc_mma<FP8>(dt, sdesc_k_sw128(sw + kk * 32), bdesc, idesc, acc_in);
+                tc_mma<FP8>(dt + (uint32_t)p.d1_col, sdesc_k_sw128(w1 + kk * 32), bdesc, idesc, acc_in);
+              }
+            } else {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              tc_mma<FP8>(dt, sdesc_k_sw128(a_lo + kk * 32), sdesc_k_sw128(b_lo + kk * 32), idesc, 1u);
+              for (int kk = 0; kk < 4; ++kk)
+                tc_mma<FP8>(dt, sdesc_k_sw128(sxp + kk * 32), sdesc_k_sw128(sw + kk * 32), idesc,
+                            (part > 0 || kb > d.kb0 || kk > 0) ? 1u : 0u);
+            }
           }
           tc_commit(bar_empty + 8 * stage);
           any = true;
@@ -276,7 +285,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         if (!ok) break;
         tc_commit(bar_tfull + 8 * acc);
-        if (++acc == 2) {
+        if (++acc == p.nbuf) {
           acc = 0;
           acc_phase ^= 1u;
         }
@@ -302,68 +311,67 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const bool ok = mbar_wait(bar_tfull + 8 * acc, acc_phase, abort_flag, p.status);
       if (epi_any(!ok)) break;
       tc_fence_after();
-      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * 256u;
+      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.buf_cols);
       const float scale = FP8 ? a_scale * p.w_scale[d.e] : 1.0f;
 
       if constexpr (SWAP && (EPI == TC_EPI_G1_BF16 || EPI == TC_EPI_G1_F32AMAX)) {
-        // lanes 0..63: gate of column i = n*64 + lrow; lanes 64..127: up of i = n*64 + lrow - 64
-        const bool is_up = lrow >= 64;
-        const int il = is_up ? lrow - 64 : lrow;
-        const int i = d.n * 64 + il;
-        for (int c0 = 0, buf = 0; c0 < d.npad; c0 += 16, buf ^= 1) {
-          float v[16];
-          tmem_ld16(tb + (uint32_t)c0, v);
-          float* xb = xchg + (buf * 64 + il) * kXchgStride;
-          if (is_up) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) xb[j] = v[j];
-          }
-          named_bar_sync(1, 128);
-          if (!is_up) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int c = c0 + j;
-              if (c < d.ntok) {
-                const float a = silu(v[j] * scale) * (xb[j] * scale);
-                const size_t o = (size_t)(d.xrow + c) * p.I + i;
-                if constexpr (EPI == TC_EPI_G1_BF16) {
-                  const __nv_bfloat16 hi = __float2bfloat16_rn(a);
-                  reinterpret_cast<__nv_bfloat16*>(p.out)[o] = hi;
-                  if (p.out_lo)
-                    reinterpret_cast<__nv_bfloat16*>(p.out_lo)[o] = __float2bfloat16_rn(a - __bfloat162float(hi));
-                } else {
-                  reinterpret_cast<float*>(p.out)[o] = a;
-                  amax = fmaxf(amax, fabsf(a));
-                }
-              }
-            }
-          }
-        }
-        named_bar_sync(1, 128);  // exchange buffers free for the next tile
-      } else if constexpr (SWAP && EPI == TC_EPI_G1_PART) {
-        // raw fp32 split partial: P[s][pair][col], col = i (gate) or I + i (up)
-        const int col = (lrow < 64) ? d.n * 64 + lrow : p.I + d.n * 64 + (lrow - 64);
-        float* P = reinterpret_cast<float*>(p.out) + (size_t)d.s * p.out_split_stride;
+        // lane r of D0 / D1: gate / up of intermediate column i = n*128 + r, one column per token
+        const int i = d.n * 128 + lrow;
         for (int c0 = 0; c0 < d.npad; c0 += 16) {
-          float v[16];
-          tmem_ld16(tb + (uint32_t)c0, v);
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (c0 + j < d.ntok) P[(size_t)p.sorted[d.xrow + c0 + j] * (2 * p.I) + col] = v[j];
-        }
-      } else if constexpr (SWAP && EPI == TC_EPI_G2_F32) {
-        // Y[s][pair][h], h = n*128 + lrow, pair = sorted[xrow + c]
-        const int h = d.n * 128 + lrow;
-        float* Y = reinterpret_cast<float*>(p.out) + (size_t)d.s * p.out_split_stride;
-        for (int c0 = 0; c0 < d.npad; c0 += 16) {
-          float v[16];
-          tmem_ld16(tb + (uint32_t)c0, v);
+          float g[16], u[16];
+          tmem_ld16(tb + (uint32_t)c0, g);
+          tmem_ld16(tb + (uint32_t)(p.d1_col + c0), u);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int c = c0 + j;
             if (c < d.ntok) {
-              const int f = p.sorted[d.xrow + c];
-              if (f < n_pairs) Y[(size_t)f * p.H + h] = v[j] * scale;
+              const float a = silu(g[j] * scale) * (u[j] * scale);
+              const size_t o = (size_t)(d.xrow + c) * p.I + i;
+              if constexpr (EPI == TC_EPI_G1_BF16) {
+                const __nv_bfloat16 hi = __float2bfloat16_rn(a);
+                reinterpret_cast<__nv_bfloat16*>(p.out)[o] = hi;
+                if (p.out_lo)
+                  reinterpret_cast<__nv_bfloat16*>(p.out_lo)[o] = __float2bfloat16_rn(a - __bfloat162float(hi));
+              } else {
+                reinterpret_cast<float*>(p.out)[o] = a;
+                amax = fmaxf(amax, fabsf(a));
+              }
+            }
+          }
+        }
+      } else if constexpr (SWAP && EPI == TC_EPI_G1_PART) {
+        // raw fp32 split partials P[s][pair][col]: gate at col i, up at col I + i
+        const int i = d.n * 128 + lrow;
+        float* P = reinterpret_cast<float*>(p.out) + (size_t)d.s * p.out_split_stride;
+        for (int c0 = 0; c0 < d.npad; c0 += 16) {
+          float g[16], u[16];
+          tmem_ld16(tb + (uint32_t)c0, g);
+          tmem_ld16(tb + (uint32_t)(p.d1_col + c0), u);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (c0 + j < d.ntok) {
+              float* row = P + (size_t)p.sorted[d.xrow + c0 + j] * (2 * p.I);
+              row[i] = g[j];
+              row[p.I + i] = u[j];
+            }
+          }
+        }
+      } else if constexpr (SWAP && EPI == TC_EPI_G2_F32) {
+        // Y[s][pair][h]: h = n*256 + r (D0) and n*256 + 128 + r (D1), pair = sorted[xrow + c]
+        const int h0 = d.n * 256 + lrow;
+        const bool h1_ok = h0 + 128 < p.H;
+        float* Y = reinterpret_cast<float*>(p.out) + (size_t)d.s * p.out_split_stride;
+        for (int c0 = 0; c0 < d.npad; c0 += 16) {
+          float v0[16], v1[16];
+          tmem_ld16(tb + (uint32_t)c0, v0);
+          tmem_ld16(tb + (uint32_t)(p.d1_col + c0), v1);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int c = c0 + j;
+            if (c < d.ntok) {
+              float* row = Y + (size_t)p.sorted[d.xrow + c] * p.H;
+              row[h0] = v0[j] * scale;
+              if (h1_ok) row[h0 + 128] = v1[j] * scale;
             }
           }
         }
@@ -562,17 +570,26 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s) {
   p.amax_out = a.amax_out;
   p.status = a.status;
 
-  const bool xchg = a.swap && (a.epi == TC_EPI_G1_BF16 || a.epi == TC_EPI_G1_F32AMAX);
   p.w_bytes = (uint32_t)(2 * a.wbox * 128);
   p.stage_bytes = p.w_bytes + (uint32_t)(a.xbox * 128) * (a.x_lo_rows ? 2u : 1u);
   const uint32_t bar_bytes = 8 * (2 * kMaxStages + 5) + 16;
-  const uint32_t budget = 227 * 1024 - 1024 - (xchg ? kXchgBytes : 0) - bar_bytes;
+  const uint32_t budget = 227 * 1024 - 1024 - bar_bytes;
   int stages = (int)(budget / p.stage_bytes);
   if (stages > kMaxStages) stages = kMaxStages;
   if (stages < 2) return cudaErrorInvalidValue;
   p.stages = stages;
-  p.xchg_off = (uint32_t)stages * p.stage_bytes;
-  p.bar_off = p.xchg_off + (xchg ? kXchgBytes : 0);
+  p.bar_off = (uint32_t)stages * p.stage_bytes;
+  if (a.swap) {
+    // D0 and D1 of xbox columns each; two buffers while they fit in 512 columns
+    if (a.xbox > 256) return cudaErrorInvalidValue;
+    p.d1_col = a.xbox <= 128 ? 128 : 256;
+    p.buf_cols = 2 * p.d1_col;
+    p.nbuf = (2 * p.buf_cols <= (int)kTmemCols) ? 2 : 1;
+  } else {
+    p.d1_col = 0;
+    p.buf_cols = 256;
+    p.nbuf = 2;
+  }
   const size_t smem = 1024 + (size_t)p.bar_off + bar_bytes;
 
   long upper;

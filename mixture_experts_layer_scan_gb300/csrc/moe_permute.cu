@@ -255,53 +255,61 @@ __global__ void k_gather_quant(const uint4* __restrict__ X, int vec_per_row /* 8
 }
 
 // Split-K reduction of GEMM1 partials (fixed split order), scale, SiLU(gate)*up.
-__global__ void k_reduce_act(const float* __restrict__ P, int splits, size_t split_stride, int I, int B,
-                             int n_pairs, const int32_t* __restrict__ sorted,
-                             const int32_t* __restrict__ eids, const int32_t* __restrict__ meta,
-                             const float* __restrict__ w_scale, const unsigned* __restrict__ a_amax_bits,
-                             int out_mode, void* __restrict__ A_out, void* __restrict__ A_lo,
-                             unsigned* __restrict__ amax_bits) {
+// blockIdx.x walks the sorted rows, blockIdx.y a 1024-column chunk of I; each
+// thread owns 4 consecutive columns (16-byte partial loads).
+__global__ void __launch_bounds__(256)
+    k_reduce_act(const float* __restrict__ P, int splits, size_t split_stride, int I, int B, int n_pairs,
+                 const int32_t* __restrict__ sorted, const int32_t* __restrict__ eids,
+                 const int32_t* __restrict__ meta, const float* __restrict__ w_scale,
+                 const unsigned* __restrict__ a_amax_bits, int out_mode, void* __restrict__ A_out,
+                 void* __restrict__ A_lo, unsigned* __restrict__ amax_bits) {
   pdl_enter();
   const int npp = meta[META_NPP];
+  const int i = blockIdx.y * 1024 + threadIdx.x * 4;
   float m = 0.0f;
-  for (int r = blockIdx.x; r < npp; r += gridDim.x) {
-    // padding rows have no partials: emit zeros, keep them out of the amax
-    const int f = sorted[r];
-    if (f >= n_pairs) {
-      for (int i = threadIdx.x; i < I; i += blockDim.x) {
-        if (out_mode == 0) {
-          reinterpret_cast<__nv_bfloat16*>(A_out)[(size_t)r * I + i] = __float2bfloat16_rn(0.0f);
-          if (A_lo) reinterpret_cast<__nv_bfloat16*>(A_lo)[(size_t)r * I + i] = __float2bfloat16_rn(0.0f);
-        } else
-          reinterpret_cast<float*>(A_out)[(size_t)r * I + i] = 0.0f;
+  if (i < I) {
+    for (int r = blockIdx.x; r < npp; r += gridDim.x) {
+      const int f = sorted[r];
+      float a[4] = {0.f, 0.f, 0.f, 0.f};
+      if (f < n_pairs) {  // padding rows have no partials: zeros, outside the amax
+        float scale = 1.0f;
+        if (w_scale) scale = e4m3_scale_from_amax(__uint_as_float(*a_amax_bits)) * w_scale[eids[r / B]];
+        const float* row = P + (size_t)f * 2 * I;  // partials are indexed by pair
+        float g[4] = {0.f, 0.f, 0.f, 0.f}, u[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int sp = 0; sp < splits; ++sp) {
+          const float4 gv = *reinterpret_cast<const float4*>(row + (size_t)sp * split_stride + i);
+          const float4 uv = *reinterpret_cast<const float4*>(row + (size_t)sp * split_stride + I + i);
+          g[0] += gv.x; g[1] += gv.y; g[2] += gv.z; g[3] += gv.w;
+          u[0] += uv.x; u[1] += uv.y; u[2] += uv.z; u[3] += uv.w;
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (w_scale) {
+            g[c] *= scale;
+            u[c] *= scale;
+          }
+          a[c] = silu(g[c]) * u[c];
+          m = fmaxf(m, fabsf(a[c]));
+        }
       }
-      continue;
-    }
-    float scale = 1.0f;
-    if (w_scale) scale = e4m3_scale_from_amax(__uint_as_float(*a_amax_bits)) * w_scale[eids[r / B]];
-    const float* row = P + (size_t)f * 2 * I;  // partials are indexed by pair
-    for (int i = threadIdx.x; i < I; i += blockDim.x) {
-      float g = 0.0f, u = 0.0f;
-      for (int s = 0; s < splits; ++s) {
-        g += row[(size_t)s * split_stride + i];
-        u += row[(size_t)s * split_stride + I + i];
-      }
-      if (w_scale) { g *= scale; u *= scale; }
-      const float a = silu(g) * u;
+      const size_t o = (size_t)r * I + i;
       if (out_mode == 0) {
-        const __nv_bfloat16 hi = __float2bfloat16_rn(a);
-        reinterpret_cast<__nv_bfloat16*>(A_out)[(size_t)r * I + i] = hi;
-        if (A_lo) reinterpret_cast<__nv_bfloat16*>(A_lo)[(size_t)r * I + i] = __float2bfloat16_rn(a - __bfloat162float(hi));
+        const uint32_t h01 = pack_bf16x2(a[0], a[1]), h23 = pack_bf16x2(a[2], a[3]);
+        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(A_out) + o) = make_uint2(h01, h23);
+        if (A_lo) {
+          const uint32_t l01 = pack_bf16x2(a[0] - bf16_bits_to_f32(h01 & 0xffffu), a[1] - bf16_bits_to_f32(h01 >> 16));
+          const uint32_t l23 = pack_bf16x2(a[2] - bf16_bits_to_f32(h23 & 0xffffu), a[3] - bf16_bits_to_f32(h23 >> 16));
+          *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(A_lo) + o) = make_uint2(l01, l23);
+        }
       } else {
-        reinterpret_cast<float*>(A_out)[(size_t)r * I + i] = a;
-        m = fmaxf(m, fabsf(a));
+        *reinterpret_cast<float4*>(reinterpret_cast<float*>(A_out) + o) = make_float4(a[0], a[1], a[2], a[3]);
       }
     }
   }
   if (out_mode == 1) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    if ((threadIdx.x & 31) == 0) atomicMax(amax_bits, __float_as_uint(m));
+    if ((threadIdx.x & 31) == 0 && m > 0.0f) atomicMax(amax_bits, __float_as_uint(m));
   }
 }
 
@@ -341,25 +349,32 @@ __device__ __forceinline__ void load8(const void* Yv, size_t idx, float (&y)[8])
   }
 }
 
-template <bool Y_BF16, bool OUT_BF16>
+// G consecutive lanes share one output vector: lane g accumulates the routed
+// slots j = g, g+G, ... (each one the sum of its K-split partials, in split
+// order), then the G partial sums are added in a fixed butterfly.  The order of
+// every addition is fixed, so the result is the same on every run.
+template <bool Y_BF16, bool OUT_BF16, int G>
 __global__ void __launch_bounds__(256) k_combine(const void* __restrict__ Yv, int splits, size_t split_stride,
                                                  const float* __restrict__ w, int T, int k, int H,
                                                  void* __restrict__ out) {
   pdl_enter();
   const int hv = H / 8;
-  const size_t total = (size_t)T * hv;
-  const int rows = k * splits;  // (j, s) rows, j-major
+  const size_t total = (size_t)T * hv * G;  // a multiple of G: groups never straddle the tail
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
-    const int t = (int)(i / hv), h = (int)(i % hv) * 8;
+    const int g = (int)(i % G);
+    const size_t o = i / G;
+    const int t = (int)(o / hv), h = (int)(o % hv) * 8;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     float yj[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    // this lane's (j, split) rows, j-major: j = g, g+G, ...; four loads in flight
+    const int rows = ((k - g + G - 1) / G) * splits;
     for (int r0 = 0; r0 < rows; r0 += 4) {
       float y[4][8];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int r = r0 + q;
         if (r < rows) {
-          const int j = r / splits, sp = r - j * splits;
+          const int j = g + (r / splits) * G, sp = r % splits;
           load8<Y_BF16>(Yv, (size_t)sp * split_stride + ((size_t)t * k + j) * H + h, y[q]);
         }
       }
@@ -367,11 +382,10 @@ __global__ void __launch_bounds__(256) k_combine(const void* __restrict__ Yv, in
       for (int q = 0; q < 4; ++q) {
         const int r = r0 + q;
         if (r < rows) {
-          const int j = r / splits, sp = r - j * splits;
 #pragma unroll
           for (int c = 0; c < 8; ++c) yj[c] += y[q][c];
-          if (sp == splits - 1) {
-            const float wj = w[(size_t)t * k + j];
+          if (r % splits == splits - 1) {
+            const float wj = w[(size_t)t * k + g + (r / splits) * G];
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
               acc[c] = fmaf(wj, yj[c], acc[c]);
@@ -381,13 +395,21 @@ __global__ void __launch_bounds__(256) k_combine(const void* __restrict__ Yv, in
         }
       }
     }
+    if constexpr (G > 1) {
+      const unsigned mask = __activemask();
+#pragma unroll
+      for (int off = 1; off < G; off <<= 1)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc[c] += __shfl_xor_sync(mask, acc[c], off);
+    }
+    if (g != 0) continue;
     if constexpr (OUT_BF16) {
-      uint4 o;
-      o.x = pack_bf16x2(acc[0], acc[1]);
-      o.y = pack_bf16x2(acc[2], acc[3]);
-      o.z = pack_bf16x2(acc[4], acc[5]);
-      o.w = pack_bf16x2(acc[6], acc[7]);
-      *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(out) + (size_t)t * H + h) = o;
+      uint4 v;
+      v.x = pack_bf16x2(acc[0], acc[1]);
+      v.y = pack_bf16x2(acc[2], acc[3]);
+      v.z = pack_bf16x2(acc[4], acc[5]);
+      v.w = pack_bf16x2(acc[6], acc[7]);
+      *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(out) + (size_t)t * H + h) = v;
     } else {
       float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + (size_t)t * H + h);
       dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
@@ -483,9 +505,10 @@ cudaError_t launch_reduce_act(const float* P, int splits, size_t split_stride, i
                               const int32_t* sorted, const int32_t* eids, const int32_t* meta, int cap,
                               const float* w_scale, const unsigned* a_amax_bits, int out_mode, void* A_out,
                               void* A_lo, unsigned* amax_bits, cudaStream_t s) {
-  const int grid = cap < 152 * 8 ? (cap > 0 ? cap : 1) : 152 * 8;
-  MOE_LAUNCH(k_reduce_act, dim3(grid), dim3(256), 0, s, P, splits, split_stride, I, B, n_pairs, sorted, eids, meta, w_scale, a_amax_bits,
-                                    out_mode, A_out, A_lo, amax_bits);
+  const int chunks = (I + 1023) / 1024;
+  const int rows = std::max(1, std::min(cap, std::max(1, 152 * 8 / chunks)));
+  MOE_LAUNCH(k_reduce_act, dim3(rows, chunks), dim3(256), 0, s, P, splits, split_stride, I, B, n_pairs, sorted, eids,
+             meta, w_scale, a_amax_bits, out_mode, A_out, A_lo, amax_bits);
   return cudaGetLastError();
 }
 
@@ -497,21 +520,32 @@ cudaError_t launch_quant_act(const float* A, int I, const int32_t* meta, int cap
   return cudaGetLastError();
 }
 
+template <bool YB, bool OB>
+static cudaError_t combine_vec(const void* Y, int splits, size_t split_stride, const float* w, int T, int k, int H,
+                               void* out, cudaStream_t s) {
+  // small batches: split each output's routed slots over G lanes for more parallelism
+  const size_t vecs = (size_t)T * (H / 8);
+  const int G = vecs >= (size_t)152 * 2048 ? 1 : (k >= 4 ? 4 : (k >= 2 ? 2 : 1));
+  const int grid = grid_for(vecs * G, 256);
+  if (G == 4) MOE_LAUNCH(k_combine<YB, OB, 4>, dim3(grid), dim3(256), 0, s, Y, splits, split_stride, w, T, k, H, out);
+  else if (G == 2) MOE_LAUNCH(k_combine<YB, OB, 2>, dim3(grid), dim3(256), 0, s, Y, splits, split_stride, w, T, k, H, out);
+  else MOE_LAUNCH(k_combine<YB, OB, 1>, dim3(grid), dim3(256), 0, s, Y, splits, split_stride, w, T, k, H, out);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_combine(const void* Y, int y_bf16, int splits, size_t split_stride, const float* w, int T, int k,
                            int H, void* out, int out_bf16, cudaStream_t s) {
   if (H % 8 == 0) {
-    const int grid = grid_for((size_t)T * (H / 8), 256);
-    if (y_bf16 && out_bf16) MOE_LAUNCH(k_combine<true, true>, dim3(grid), dim3(256), 0, s, Y, splits, split_stride, w, T, k, H, out);
-    else if (y_bf16) MOE_LAUNCH(k_combine<true, false>, dim3(grid), dim3(256), 0, s, Y, splits, split_stride, w, T, k, H, out);
-    else if (out_bf16) MOE_LAUNCH(k_combine<false, true>, dim3(grid), dim3(256), 0, s, Y, splits, split_stride, w, T, k, H, out);
-    else MOE_LAUNCH(k_combine<false, false>, dim3(grid), dim3(256), 0, s, Y, splits, split_stride, w, T, k, H, out);
-  } else {
-    const int grid = grid_for((size_t)T * H, 256);
-    if (y_bf16 && out_bf16) MOE_LAUNCH(k_combine_scalar<true, true>, dim3(grid), dim3(256), 0, s, Y, splits, split_stride, w, T, k, H, out);
-    else if (y_bf16) MOE_LAUNCH(k_combine_scalar<true, false>, dim3(grid), dim3(256), 0, s, Y, splits, split_stride, w, T, k, H, out);
-    else if (out_bf16) MOE_LAUNCH(k_combine_scalar<false, true>, dim3(grid), dim3(256), 0, s, Y, splits, split_stride, w, T, k, H, out);
-    else MOE_LAUNCH(k_combine_scalar<false, false>, dim3(grid), dim3(256), 0, s, Y, splits, split_stride, w, T, k, H, out);
+    if (y_bf16 && out_bf16) return combine_vec<true, true>(Y, splits, split_stride, w, T, k, H, out, s);
+    if (y_bf16) return combine_vec<true, false>(Y, splits, split_stride, w, T, k, H, out, s);
+    if (out_bf16) return combine_vec<false, true>(Y, splits, split_stride, w, T, k, H, out, s);
+    return combine_vec<false, false>(Y, splits, split_stride, w, T, k, H, out, s);
   }
+  const int grid = grid_for((size_t)T * H, 256);
+  if (y_bf16 && out_bf16) MOE_LAUNCH(k_combine_scalar<true, true>, dim3(grid), dim3(256), 0, s, Y, splits, split_stride, w, T, k, H, out);
+  else if (y_bf16) MOE_LAUNCH(k_combine_scalar<true, false>, dim3(grid), dim3(256), 0, s, Y, splits, split_stride, w, T, k, H, out);
+  else if (out_bf16) MOE_LAUNCH(k_combine_scalar<false, true>, dim3(grid), dim3(256), 0, s, Y, splits, split_stride, w, T, k, H, out);
+  else MOE_LAUNCH(k_combine_scalar<false, false>, dim3(grid), dim3(256), 0, s, Y, splits, split_stride, w, T, k, H, out);
   return cudaGetLastError();
 }
 
