@@ -353,12 +353,16 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--sweep-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override the workload's token count (smaller cases for profiling)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
 
+    if args.tokens:
+        WORKLOADS[args.workload] = (WORKLOADS[args.workload][0], args.tokens)
     base, T = WORKLOADS[args.workload]
     sp = spec(base, T=T)
     config = {"workload": args.workload, "tokens": T, "hidden": sp.H, "experts": sp.E, "intermediate": sp.I,

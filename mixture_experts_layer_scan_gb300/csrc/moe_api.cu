@@ -45,6 +45,8 @@ static int num_sms() {
 constexpr int kPlanSms = 152;
 // Router logits go through the tensor-core GEMM from this many tokens on.
 constexpr int kRouterTcMinTokens = 256;
+// Largest swap-AB activation tile whose rows GEMM1 gathers itself.
+constexpr int kGatherInGemmMaxRows = 32;
 
 enum Path { PATH_F32 = 0, PATH_BF16 = 1, PATH_FP8 = 2 };
 
@@ -58,6 +60,7 @@ struct Plan {
   int wbox2 = 128;  // token-major GEMM2 weight rows per load (N = 2 * wbox2)
   bool y_bf16 = false;
   bool act_split = false;  // bf16 intermediate stored as hi + lo parts (two MMAs in GEMM2)
+  bool gather_in_gemm = false;  // GEMM1 gathers its activation rows itself (TMA tile::gather4)
   size_t o_logits = 0, o_tw = 0, o_tid = 0, o_meta = 0, o_sorted = 0, o_eids = 0, o_xs = 0, o_aint = 0, o_af32 = 0,
          o_p1 = 0, o_y = 0, o_misc = 0, total = 0;
   size_t p1_stride = 0, y_stride = 0;
@@ -150,6 +153,10 @@ static int make_plan(int T, int H, int I, int E, int topk, moe_dtype act, moe_dt
     // hi/lo intermediate: by default where it is free (swap-AB decode streams
     // weights from HBM; the second MMA only uses idle tensor-core time)
     p.act_split = p.path == PATH_BF16 && (act_mode == 2 || (act_mode == 0 && p.swap));
+    // GEMM1 gathers token rows itself (one tile::gather4 per 4 rows) when the
+    // activation tile is short; for wider tiles the per-stage TMA instruction
+    // count outweighs the saved kernel, so rows are gathered beforehand.
+    p.gather_in_gemm = p.swap && p.xbox <= kGatherInGemmMaxRows;
   } else {
     p.B = 16;
     p.swap = false;
@@ -171,7 +178,11 @@ static int make_plan(int T, int H, int I, int E, int topk, moe_dtype act, moe_dt
   p.o_meta = take((size_t)meta_words(E) * 4);
   p.o_sorted = take((size_t)p.cap * 4);
   p.o_eids = take((size_t)std::max<long>(p.nblk_cap, 1) * 4);
-  p.o_xs = take((size_t)p.cap * H * xb);
+  // gathered activation rows: the fp32 path gathers into sorted order; the
+  // tensor-core paths gather inside GEMM1 (FP8 keeps a token-order e4m3 copy)
+  size_t xs_bytes = (size_t)p.cap * H * xb;                      // rows gathered into expert order
+  if (p.gather_in_gemm) xs_bytes = p.path == PATH_FP8 ? (size_t)T * H : 0;  // token order (FP8: e4m3 copy)
+  p.o_xs = take(xs_bytes);
   p.o_aint = take((size_t)p.cap * I * xb * (p.act_split ? 2 : 1));
   if (p.path == PATH_FP8) p.o_af32 = take((size_t)p.cap * I * 4);
   if (p.s1 > 1) {
@@ -222,6 +233,7 @@ static cudaError_t launch_router(const void* X, const void* Wr, int T, int H, in
     g.X = X;
     g.out = logits;
     g.n_valid = E;
+    g.early = true;  // the router reads no earlier kernel's output before its dependency wait except weights
     g.status = status;
     g.num_sms = sms;
     return launch_gemm_tc(g, s);
@@ -272,10 +284,12 @@ int moe_plan_info(int T, int H, int I, int E, int topk, moe_dtype act_dtype, moe
   info->splits_gemm1 = p.s1;
   info->splits_gemm2 = p.s2;
   info->act_split = p.act_split ? 1 : 0;
-  // router logits, top-k, align, gather, GEMM1, GEMM2, combine (+ amax and
-  // intermediate quantisation on the FP8 path, + the split-K reduction)
-  int n = 7;
-  if (p.path == PATH_FP8) n += 2;
+  // router logits, top-k, align, GEMM1, GEMM2, combine (+ the row gather unless
+  // GEMM1 gathers; + amax and quantisation kernels on the FP8 path; + the
+  // split-K reduction)
+  int n = 6;
+  if (!p.gather_in_gemm) n += 1;            // row gather (FP8: with input quantisation)
+  if (p.path == PATH_FP8) n += p.gather_in_gemm ? 3 : 2;  // input amax (+ input quantisation), intermediate quantisation
   if (p.s1 > 1) n += 1;
   info->kernel_launches = T > 0 ? n : 0;
   info->workspace_bytes = p.total;
@@ -395,13 +409,17 @@ int moe_forward(const void* hidden, const void* router_w, const void* w13, const
   MOE_TRY(launch_align(tid, T, topk, E, pl.B, sorted, eids, meta + META_NPP, nullptr, meta, st, s));
   if (o) record(o->stage_end[MOE_STAGE_ALIGN], s);
 
-  // 4. gather (+ FP8 input quantisation)
+  // 4. activations: the fp32 path gathers rows into expert order here; the
+  // tensor-core paths gather inside GEMM1 (FP8: quantise the input to e4m3 first)
   if (o) record(o->stage_begin[MOE_STAGE_GATHER], s);
   if (pl.path == PATH_FP8) {
     MOE_TRY(cudaMemsetAsync(amax, 0, 2 * sizeof(unsigned), s));
     MOE_TRY(launch_amax_bf16(hidden, (size_t)T * H, amax, s));
-    MOE_TRY(launch_gather(hidden, T, H, topk, 2, 1, amax, sorted, meta, cap, xs, s));
-  } else {
+    if (pl.gather_in_gemm)
+      MOE_TRY(launch_quant_x(hidden, (size_t)T * H, amax, (uint8_t*)xs, s));
+    else
+      MOE_TRY(launch_gather(hidden, T, H, topk, 2, 1, amax, sorted, meta, cap, xs, s));
+  } else if (!pl.gather_in_gemm) {
     MOE_TRY(launch_gather(hidden, T, H, topk, pl.path == PATH_F32 ? 4 : 2, 0, nullptr, sorted, meta, cap, xs, s));
   }
   if (o) record(o->stage_end[MOE_STAGE_GATHER], s);
@@ -437,7 +455,8 @@ int moe_forward(const void* hidden, const void* router_w, const void* w13, const
     TcGemmArgs g1 = g;
     g1.K = H;
     g1.W = w13;
-    g1.X = xs;
+    g1.X = (fp8 || !pl.gather_in_gemm) ? (const void*)xs : hidden;
+    g1.gather = pl.gather_in_gemm;
     g1.w_rows_per_expert = 2 * I;
     g1.w_pair_off = I;
     g1.wbox = 128;
@@ -491,6 +510,10 @@ int moe_forward(const void* hidden, const void* router_w, const void* w13, const
     g2.out = y;
     g2.out_split_stride = pl.y_stride;
     g2.epi = pl.y_bf16 ? TC_EPI_G2_BF16 : TC_EPI_G2_F32;
+    // GEMM2's predecessor is GEMM1 or a kernel GEMM1 let launch, and GEMM1 lets
+    // its dependents launch only after its own dependency wait: the permutation
+    // metadata is complete by then, so GEMM2 may stream weights early.
+    g2.early = true;
     if (o) record(o->stage_begin[MOE_STAGE_GEMM2], s);
     MOE_TRY(launch_gemm_tc(g2, s));
     if (o) record(o->stage_end[MOE_STAGE_GEMM2], s);

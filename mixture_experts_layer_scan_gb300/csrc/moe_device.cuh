@@ -134,6 +134,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t smem_dst, const void* tmap,
       : "memory");
 }
 
+// Four rows (row0..row3) of a 2-D tensor whose map has a one-row box, each
+// box-width wide from column c_inner, into consecutive rows at smem_dst.
+__device__ __forceinline__ void tma_gather4(uint32_t smem_dst, const void* tmap, int c_inner, int row0, int row1,
+                                            int row2, int row3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3, %4, %5, %6}], [%7];" ::"r"(smem_dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c_inner), "r"(row0), "r"(row1), "r"(row2), "r"(row3), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }

@@ -49,6 +49,8 @@ struct TcDev {
   int kb_total, kb_per_split, splits, n_tiles;
   int w_rows_per_expert, w_pair_off, w_tile_rows, wbox, xbox;
   int stages;
+  int gather;       // 1: activation rows gathered by token from an unsorted [T][K] tensor
+  int early;        // 1: the tile list may be read and weights streamed before the dependency wait
   int nbuf;         // accumulator buffers (2: epilogue of one tile overlaps the next; 1 for wide swap tiles)
   int buf_cols;     // tensor-memory columns per buffer
   int d1_col;       // swap-AB: column of accumulator D1 (weight rows 128..255) inside a buffer
@@ -170,57 +172,98 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  // The tile list comes from the permutation metadata, which was complete
-  // before the preceding kernel started; only the activation tiles (and, in
-  // the epilogue, the FP8 scale) depend on the preceding kernel.
+  // Programmatic dependent launch: kernels of this library let their
+  // dependents launch early, so nothing written by an earlier kernel may be
+  // read before pdl_wait() -- except when the host sets `early`: for GEMM2
+  // (launched only after GEMM1 has itself passed its wait, so the permutation
+  // metadata is complete) and for the router GEMM (which reads none).
+  if (!p.early) pdl_wait();
   const int ntiles = tile_count<SWAP, EPI>(p);
   constexpr int KBLK = FP8 ? 128 : 64;  // elements per 128-byte K block
 
   if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- TMA producer ----------------
-      // Expert weights do not depend on the preceding kernel: stream the first
-      // stages of weight tiles before waiting for it (programmatic dependent
-      // launch), so this kernel's HBM stream starts while the previous one drains.
-      int pre = 0;
-      if ((int)blockIdx.x < ntiles) {
-        const Tile d = tile_at<SWAP, EPI>(p, blockIdx.x);
-        pre = min(p.stages, d.kb1 - d.kb0);
-        for (int i = 0; i < pre; ++i) {
-          const uint32_t sw = sbase + i * p.stage_bytes;
-          const uint32_t fb = bar_full + 8 * i;
-          mbar_arrive_expect_tx(fb, p.stage_bytes);
-          tma_load_2d(sw, &tmW, (d.kb0 + i) * KBLK, d.wr0, fb);
-          tma_load_2d(sw + p.wbox * 128, &tmW, (d.kb0 + i) * KBLK, d.wr0 + p.w_pair_off, fb);
-        }
+    // ---------------- TMA producer (warp 0) ----------------
+    // Lane 0 waits for free stages, arms their barriers and loads the weight
+    // tiles.  The activation tile is either one tiled load of consecutive
+    // sorted rows (lane 0), or -- when the activations are gathered -- one
+    // tile::gather4 load per group of 4 rows, issued by the 32 lanes in
+    // parallel with the token row of each sorted (token, slot) pair.
+    //
+    // Expert weights do not depend on the preceding kernel: lane 0 streams the
+    // first stages of weight tiles before waiting for it (programmatic
+    // dependent launch), so this kernel's HBM stream starts while the previous
+    // one drains.
+    int pre = 0;
+    if (p.early && lane == 0 && (int)blockIdx.x < ntiles) {
+      const Tile d = tile_at<SWAP, EPI>(p, blockIdx.x);
+      pre = min(p.stages, d.kb1 - d.kb0);
+      for (int i = 0; i < pre; ++i) {
+        const uint32_t sw = sbase + i * p.stage_bytes;
+        const uint32_t fb = bar_full + 8 * i;
+        mbar_arrive_expect_tx(fb, p.stage_bytes);
+        tma_load_2d(sw, &tmW, (d.kb0 + i) * KBLK, d.wr0, fb);
+        tma_load_2d(sw + p.wbox * 128, &tmW, (d.kb0 + i) * KBLK, d.wr0 + p.w_pair_off, fb);
       }
-      pdl_wait();
-      int stage = 0;
-      uint32_t phase = 0, issued = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-        const Tile d = tile_at<SWAP, EPI>(p, t);
-        for (int kb = d.kb0; kb < d.kb1; ++kb) {
-          const uint32_t sw = sbase + stage * p.stage_bytes;
-          const uint32_t fb = bar_full + 8 * stage;
-          if ((int)issued >= pre) {  // (the first `pre` stages already hold their weight tiles)
-            if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p.status)) {
-              ok = false;
-              break;
-            }
+    }
+    pdl_wait();
+    const int n_pairs = p.T * p.k;
+    const int npp = (EPI == TC_EPI_LOGITS) ? 0 : p.meta[META_NPP];
+    const int groups = p.xbox / 4;  // gather4 groups per activation tile (<= 64)
+    int stage = 0;
+    uint32_t phase = 0, issued = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      const Tile d = tile_at<SWAP, EPI>(p, t);
+      int rows[2][4];  // token rows of this lane's gather groups g = lane and lane + 32
+      if (p.gather) {
+#pragma unroll
+        for (int gi = 0; gi < 2; ++gi)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = d.xrow + 4 * (lane + 32 * gi) + i;
+            const int f = (r < npp) ? p.sorted[r] : n_pairs;
+            rows[gi][i] = (f < n_pairs) ? f / p.k : 0;  // padding rows read token 0; never stored
+          }
+      }
+      for (int kb = d.kb0; kb < d.kb1; ++kb) {
+        const uint32_t sw = sbase + stage * p.stage_bytes;
+        const uint32_t fb = bar_full + 8 * stage;
+        uint32_t good = 1;
+        if (lane == 0 && (int)issued >= pre) {  // (the first `pre` stages already hold their weight tiles)
+          if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p.status)) {
+            good = 0;
+          } else {
             mbar_arrive_expect_tx(fb, p.stage_bytes);
             tma_load_2d(sw, &tmW, kb * KBLK, d.wr0, fb);
             tma_load_2d(sw + p.wbox * 128, &tmW, kb * KBLK, d.wr0 + p.w_pair_off, fb);
           }
+        }
+        good = __shfl_sync(0xffffffffu, good, 0);
+        if (!good) {
+          ok = false;
+          break;
+        }
+        if (p.gather) {
+#pragma unroll
+          for (int gi = 0; gi < 2; ++gi) {
+            const int g = lane + 32 * gi;
+            if (g < groups)
+              tma_gather4(sw + p.w_bytes + (uint32_t)g * 512u, &tmX, kb * KBLK, rows[gi][0], rows[gi][1],
+                          rows[gi][2], rows[gi][3], fb);
+          }
+        } else if (lane == 0) {
           tma_load_2d(sw + p.w_bytes, &tmX, kb * KBLK, d.xrow, fb);
           if (p.x_lo_rows) tma_load_2d(sw + p.w_bytes + p.xbox * 128, &tmX, kb * KBLK, d.xrow + p.x_lo_rows, fb);
-          ++issued;
-          if (++stage == p.stages) {
-            stage = 0;
-            phase ^= 1u;
-          }
+        }
+        __syncwarp();
+        ++issued;
+        if (++stage == p.stages) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
+    }
+    if (lane == 0) {
       // every load of this CTA is issued: the next kernel may start its prologue
       pdl_launch_dependents();
       if (!ok) {  // let the copies already in flight land before the CTA exits
@@ -378,6 +421,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       } else if constexpr (!SWAP && (EPI == TC_EPI_G1_BF16 || EPI == TC_EPI_G1_F32AMAX)) {
         // row = xrow + lrow; columns [0, wbox) gate, [wbox, 2 wbox) up of i = n*wbox + c
         const size_t row = (size_t)(d.xrow + lrow);
+        const bool row_valid = p.sorted[row] < n_pairs;
         for (int c0 = 0; c0 < p.wbox; c0 += 16) {
           float g[16], u[16];
           tmem_ld16(tb + (uint32_t)c0, g);
@@ -407,8 +451,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + o);
 #pragma unroll
             for (int j = 0; j < 4; ++j) dst[j] = make_float4(a[4 * j], a[4 * j + 1], a[4 * j + 2], a[4 * j + 3]);
+            if (row_valid) {  // padding rows hold token 0's values: keep them out of the amax
 #pragma unroll
-            for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(a[j]));
+              for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(a[j]));
+            }
           }
         }
       } else if constexpr (EPI == TC_EPI_LOGITS) {
@@ -538,8 +584,13 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s) {
   CUtensorMap mw, mx;
   if (!make_map(&mw, a.W, eb, (uint64_t)a.K, (uint64_t)a.E * a.w_rows_per_expert, (uint32_t)a.wbox))
     return cudaErrorInvalidValue;
-  if (!make_map(&mx, a.X, eb, (uint64_t)a.K, (uint64_t)a.cap + (uint64_t)a.x_lo_rows, (uint32_t)a.xbox))
+  if (a.gather) {
+    // tile::gather4 needs a one-row box: 4 such rows per instruction
+    if (a.xbox % 4 || a.xbox > 256 || a.x_lo_rows) return cudaErrorInvalidValue;
+    if (!make_map(&mx, a.X, eb, (uint64_t)a.K, (uint64_t)a.T, 1u)) return cudaErrorInvalidValue;
+  } else if (!make_map(&mx, a.X, eb, (uint64_t)a.K, (uint64_t)a.cap + (uint64_t)a.x_lo_rows, (uint32_t)a.xbox)) {
     return cudaErrorInvalidValue;
+  }
 
   TcDev p = {};
   p.epi = a.epi;
@@ -561,6 +612,8 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s) {
   p.eids = a.eids;
   p.meta = a.meta;
   p.out = a.out;
+  p.gather = a.gather ? 1 : 0;
+  p.early = a.early ? 1 : 0;
   p.n_valid = a.n_valid;
   p.out_lo = a.out_lo;
   p.x_lo_rows = a.x_lo_rows;

@@ -46,6 +46,8 @@ cudaError_t launch_reduce_act(const float* P, int splits, size_t split_stride, i
                               const int32_t* sorted, const int32_t* eids, const int32_t* meta, int cap,
                               const float* w_scale, const unsigned* a_amax_bits, int out_mode, void* A_out,
                               void* A_lo, unsigned* amax_bits, cudaStream_t s);
+// Xq[i] = e4m3(X[i] / (amax/448)) for the n bf16 values of X (n % 8 == 0)
+cudaError_t launch_quant_x(const void* X, size_t n, const unsigned* amax_bits, uint8_t* Xq, cudaStream_t s);
 // A_q[r][i] = e4m3(A[r][i] / (amax/448)) for r < num_post_pad
 cudaError_t launch_quant_act(const float* A, int I, const int32_t* meta, int cap, const unsigned* amax_bits,
                              uint8_t* Aq, cudaStream_t s);
@@ -86,6 +88,9 @@ struct TcGemmArgs {
   int splits;       // K splits (swap mode)
   int kb_per_split; // k-blocks (128 bytes of K) per split
   int cap;          // rows of the sorted activation buffer (T for the router)
+  bool gather;      // X is the unsorted [T][K] tensor; rows are gathered by token (tile::gather4)
+  bool early;       // tile list and weights may be read before the dependency wait: only when every
+                    // kernel that wrote the metadata finished before the preceding kernel could launch
   int n_valid;      // router: number of output columns (experts) to store
   // tensors
   const void* W;    // weights viewed as [E * w_rows_per_expert][K]

@@ -254,6 +254,25 @@ __global__ void k_gather_quant(const uint4* __restrict__ X, int vec_per_row /* 8
   }
 }
 
+// Dynamic per-tensor e4m3 quantisation of the layer input (token order; the
+// GEMM gathers the rows it needs): code = e4m3(x / s), s = amax/448.
+__global__ void k_quant_x(const uint4* __restrict__ X, size_t nvec, const unsigned* __restrict__ amax_bits,
+                          uint2* __restrict__ Xq) {
+  pdl_enter();
+  const float s = e4m3_scale_from_amax(__uint_as_float(*amax_bits));
+  for (size_t v = (size_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec; v += (size_t)gridDim.x * blockDim.x) {
+    const uint4 x = X[v];
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t q[2] = {0, 0};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t bits = (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xffffu);
+      q[j >> 2] |= (uint32_t)f32_to_e4m3(bf16_bits_to_f32(bits) / s) << (8 * (j & 3));
+    }
+    Xq[v] = make_uint2(q[0], q[1]);
+  }
+}
+
 // Split-K reduction of GEMM1 partials (fixed split order), scale, SiLU(gate)*up.
 // blockIdx.x walks the sorted rows, blockIdx.y a 1024-column chunk of I; each
 // thread owns 4 consecutive columns (16-byte partial loads).
@@ -498,6 +517,11 @@ cudaError_t launch_gather(const void* X, int T, int H, int k, int elem_bytes, in
     const int vpr = H / 8;
     MOE_LAUNCH(k_gather_quant, dim3(grid), dim3(128), 0, s, (const uint4*)X, vpr, k, T * k, sorted, meta, amax_bits, (uint2*)Xs);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_x(const void* X, size_t n, const unsigned* amax_bits, uint8_t* Xq, cudaStream_t s) {
+  MOE_LAUNCH(k_quant_x, dim3(grid_for(n / 8, 256)), dim3(256), 0, s, (const uint4*)X, n / 8, amax_bits, (uint2*)Xq);
   return cudaGetLastError();
 }
 
