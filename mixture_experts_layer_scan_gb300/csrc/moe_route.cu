@@ -81,6 +81,8 @@ __global__ void __launch_bounds__(kRouterWarps * 32) k_router_logits(const TIn* 
   }
 }
 
+constexpr int kTopkCache = 8;  // logits per lane kept in registers by the top-k kernel
+
 // (value, index) order of the ranking: larger value first, lower index on ties.
 __device__ __forceinline__ bool ranks_before(float v, int i, float bv, int bi) {
   return v > bv || (v == bv && i < bi);
@@ -96,13 +98,23 @@ __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, 
   const int t = blockIdx.x * (blockDim.x >> 5) + warp;
   if (t >= T) return;
   const float* l = logits + (size_t)t * E;
+  // the first kTopkCache logits of this lane stay in registers (all of them for E <= 256);
+  // the scan order and arithmetic are those of a plain loop over e = lane, lane+32, ...
+  float cache[kTopkCache];
+#pragma unroll
+  for (int q = 0; q < kTopkCache; ++q) cache[q] = (lane + 32 * q < E) ? l[lane + 32 * q] : -INFINITY;
   uint32_t taken = 0;  // bit q: expert lane + 32*q taken
   float my_v = 0.0f;
   int my_i = 0;
   for (int j = 0; j < k; ++j) {
     float bv = -INFINITY;
     int bi = 0x7fffffff;
-    for (int q = 0, e = lane; e < E; ++q, e += 32) {
+#pragma unroll
+    for (int q = 0; q < kTopkCache; ++q) {
+      const int e = lane + 32 * q;
+      if (e < E && !(taken & (1u << q)) && ranks_before(cache[q], e, bv, bi)) { bv = cache[q]; bi = e; }
+    }
+    for (int q = kTopkCache, e = lane + 32 * kTopkCache; e < E; ++q, e += 32) {
       if (taken & (1u << q)) continue;
       const float v = l[e];
       if (ranks_before(v, e, bv, bi)) { bv = v; bi = e; }
@@ -117,7 +129,7 @@ __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, 
     if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
     if (lane == j) { my_v = bv; my_i = bi; }
   }
-  // softmax: m is the largest logit (the first pick)
+  // softmax: m is the largest logit (the first pick); each lane sums its experts in ascending order
   const float m = __shfl_sync(0xffffffffu, my_v, 0);
   const float ex = (lane < k) ? expf(my_v - m) : 0.0f;
   float denom;
@@ -125,7 +137,10 @@ __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, 
     denom = ex;
   } else {
     denom = 0.0f;
-    for (int e = lane; e < E; e += 32) denom += expf(l[e] - m);
+#pragma unroll
+    for (int q = 0; q < kTopkCache; ++q)
+      if (lane + 32 * q < E) denom += expf(cache[q] - m);
+    for (int e = lane + 32 * kTopkCache; e < E; e += 32) denom += expf(l[e] - m);
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) denom += __shfl_xor_sync(0xffffffffu, denom, off);
