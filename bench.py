@@ -46,6 +46,7 @@ WORKLOADS = {
 }
 SWEEP_SKIP = {"tiny_f32_T64"}  # correctness-size fp32 layer: not a throughput workload
 HEADLINE = "mixtral_decode_M64"
+SINGLE_LAUNCH = {"auto": 0, "on": 1, "off": 2}  # moe_options.single_launch
 
 
 def max_over_ranks(x: float, world: int, device) -> float:
@@ -191,8 +192,17 @@ def run_ours(args, rank, world, dev):
         s13, s2 = L["w13_scale"], L["w2_scale"]
         act = moe.MOE_F32 if sp.act == "f32" else moe.MOE_BF16
         wdt = {"f32": moe.MOE_F32, "bf16": moe.MOE_BF16, "e4m3": moe.MOE_E4M3}[sp.w]
-        plan = moe.moe_plan_info(T, sp.H, sp.I, sp.E, sp.k, act, wdt)
-        ws = torch.empty(plan["workspace_bytes"], dtype=torch.uint8, device=dev)
+        base_opts = {"single_launch": SINGLE_LAUNCH[args.single_launch]}
+        plan = moe.moe_plan_info(T, sp.H, sp.I, sp.E, sp.k, act, wdt, base_opts)
+        # the two decode paths (one cooperative kernel / the multi-kernel sequence) where both apply
+        paths = {}
+        for pname, code in (("single_launch", 1), ("multi_kernel", 2)):
+            try:
+                paths[pname] = moe.moe_plan_info(T, sp.H, sp.I, sp.E, sp.k, act, wdt, {"single_launch": code})
+            except moe.MoeError:
+                pass
+        ws_bytes = max([plan["workspace_bytes"]] + [q["workspace_bytes"] for q in paths.values()])
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         out = torch.empty_like(X)
         # realised routing (the library's own router on the same batch)
         _, _, ids = moe.moe_route(X, Wr, sp.k, sp.renorm)
@@ -202,7 +212,9 @@ def run_ours(args, rank, world, dev):
         flush = weights_active < 2 * L2_BYTES  # else the step's own inputs exceed L2
 
         def step(options=None):
-            moe.moe_forward(X, Wr, W13, W2, sp.k, sp.renorm, s13, s2, out=out, workspace=ws, options=options,
+            o = dict(base_opts)
+            o.update(options or {})
+            moe.moe_forward(X, Wr, W13, W2, sp.k, sp.renorm, s13, s2, out=out, workspace=ws, options=o,
                             stream=stream)
 
         is_head = wi == 0
@@ -253,6 +265,18 @@ def run_ours(args, rank, world, dev):
         total_ms = max_over_ranks(total_ms, world, dev)
         ms = total_ms / K
         eager_ms = timed(step, min(K, 200), flush) / min(K, 200)
+        paths_ms = {}
+        if len(paths) == 2:
+            for pname, code in (("single_launch", 1), ("multi_kernel", 2)):
+                g_alt = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g_alt, stream=stream, capture_error_mode="thread_local"):
+                    step({"single_launch": code})
+                for _ in range(W):
+                    g_alt.replay()
+                ka = min(K, 500)
+                paths_ms[pname] = timed(g_alt.replay, ka, flush) / ka
+                del g_alt
+            assert moe.moe_get_status() == 0
 
         # per-stage durations (CUDA events recorded by the library on this stream)
         kk = min(K, 100)
@@ -276,6 +300,8 @@ def run_ours(args, rank, world, dev):
         g1_ms, g2_ms = stage_ms["gemm1"], stage_ms["gemm2"]
         r = {"tokens_per_s": tok_s, "ms_per_step": ms, "eager_ms_per_step": eager_ms, "active_experts": n_active,
              "plan": plan, "stage_ms": stage_ms, "l2": "flushed between steps" if flush else "inputs larger than L2"}
+        if paths_ms:
+            r["paths_ms_per_step"] = paths_ms
         if decode:
             r["layer_hbm_gbs"] = wk["layer_bytes"] / (ms / 1e3) / 1e9
             r["layer_hbm_frac"] = r["layer_hbm_gbs"] / pk["hbm_gbs"]
@@ -307,7 +333,8 @@ def run_ours(args, rank, world, dev):
 
             def e2e_step():
                 Xd.copy_(Xh, non_blocking=True)
-                moe.moe_forward(Xd, Wr, W13, W2, sp.k, sp.renorm, s13, s2, out=out, workspace=ws, stream=stream)
+                moe.moe_forward(Xd, Wr, W13, W2, sp.k, sp.renorm, s13, s2, out=out, workspace=ws, options=base_opts,
+                                stream=stream)
                 outh.copy_(out, non_blocking=True)
 
             for _ in range(W):
@@ -353,6 +380,9 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--sweep-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--single-launch", default="auto", choices=sorted(SINGLE_LAUNCH),
+                    help="decode batches: the whole layer as one cooperative kernel (on), the multi-kernel "
+                         "sequence (off), or the library's choice (auto)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the workload's token count (smaller cases for profiling)")
     args = ap.parse_args()

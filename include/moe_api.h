@@ -88,6 +88,27 @@ typedef enum {
   MOE_NUM_STAGES = 7
 } moe_stage;
 
+/* Phase stamps of the single-launch kernel (moe_options.trace), per CTA. */
+typedef enum {
+  MOE_TRACE_START = 0,      /* kernel entry, after the prologue */
+  MOE_TRACE_ROUTER = 1,     /* router logits of this CTA written */
+  MOE_TRACE_BARRIER0 = 2,   /* all logits visible */
+  MOE_TRACE_TOPK = 3,       /* top-k of this CTA's tokens written */
+  MOE_TRACE_BARRIER1 = 4,   /* all routing visible */
+  MOE_TRACE_TABLES = 5,     /* expert tables built in shared memory */
+  MOE_TRACE_GATHERED = 6,   /* token rows in expert order (after the third barrier; = TABLES without it) */
+  MOE_TRACE_G1_ISSUED = 7,  /* producer: loads of every GEMM1 tile of this CTA issued */
+  MOE_TRACE_G2_READY = 8,   /* producer: first GEMM2 tile found its intermediate complete */
+  MOE_TRACE_ISSUED = 9,     /* producer: every load issued */
+  MOE_TRACE_MMA_DONE = 10,  /* MMA issuer: last tile committed */
+  MOE_TRACE_G1_DONE = 11,   /* epilogue: last GEMM1 tile of this CTA signalled */
+  MOE_TRACE_EPI_DONE = 12,  /* epilogue: last tile stored */
+  MOE_TRACE_COMB_FIRST = 13,/* combine: first unit's outputs all arrived */
+  MOE_TRACE_COMB_DONE = 14, /* combine: last unit written */
+  MOE_TRACE_END = 15,       /* CTA done */
+  MOE_TRACE_WORDS = 16
+} moe_trace_event;
+
 /* Optional knobs of moe_forward / moe_workspace_size.  Pass NULL for defaults
  * (all-zero struct == defaults).  The same options must be given to
  * moe_workspace_size and to the moe_forward calls that use that workspace. */
@@ -101,6 +122,15 @@ typedef struct {
   int act_split;      /* bf16 path: 0 = automatic (hi/lo in SWAP_AB, single in TOKEN_MAJOR),
                          1 = intermediate stored as one bf16, 2 = as bf16 hi + bf16 lo
                          (a - bf16(a)), GEMM2 then runs both parts into one fp32 accumulator */
+  void* trace;        /* nullable device buffer of MOE_TRACE_WORDS uint64 per SM: when the call
+                         runs as a single launch, CTA c writes %globaltimer stamps (ns) of its
+                         phases to trace[c * MOE_TRACE_WORDS + moe_trace_event]; events a CTA
+                         does not reach are left as they were (zero the buffer first) */
+  int single_launch;  /* bf16 SWAP_AB batches: 0 = automatic, 1 = run the whole layer as one
+                         cooperative kernel (MOE_ERR_UNSUPPORTED where it does not apply:
+                         it needs the bf16 path in SWAP_AB mode, T <= 64, T*topk <= 512,
+                         E <= 256), 2 = always the multi-kernel sequence.  Both give
+                         bit-identical outputs. */
   /* Nullable CUDA events recorded on `stream` right before / after the
    * kernels of each stage (the caller creates and owns them). */
   moe_event_t stage_begin[MOE_NUM_STAGES];
@@ -115,6 +145,7 @@ typedef struct {
   int splits_gemm2;
   int act_split;        /* 1 if the bf16 intermediate is stored as hi + lo */
   int kernel_launches;  /* kernels one moe_forward call launches */
+  int single_launch;    /* 1 if the whole layer runs as one cooperative kernel */
   size_t workspace_bytes;
 } moe_plan;
 
@@ -195,7 +226,14 @@ MOE_API int moe_align(const int32_t* topk_ids, int T, int topk, int E, int block
  *   tensor-core paths need H % 128 == 0 and I % 128 == 0.
  * The intermediate SiLU(gate)*up is stored in bf16 (as a bf16 hi + lo pair in SWAP_AB
  * mode, see moe_options.act_split; fp32 on the fp32 path; e4m3 on the FP8 path);
- * accumulation is fp32 throughout; out is rounded once. */
+ * accumulation is fp32 throughout; out is rounded once.
+ * Single launch (moe_options.single_launch): thin bf16 decode batches may run all
+ * seven steps in one cooperative kernel ("Mixture-of-Experts kernel engineering on
+ * Amazon SageMaker AI", intro: routing, shuffle and expert networks as one batched
+ * operation); its stage events then bracket that one kernel (recorded as GEMM1, the
+ * other stages empty).  All its CTAs must be resident at once: the call fails with
+ * MOE_ERR_CUDA if the device cannot hold them (e.g. while another kernel occupies SMs
+ * under MPS limits). */
 MOE_API int moe_forward(const void* hidden, const void* router_w, const void* w13, const void* w2, int T, int H, int I, int E,
                 int topk, int renorm, moe_dtype act_dtype, moe_dtype w_dtype, const float* w13_scale,
                 const float* w2_scale, void* out, void* workspace, size_t workspace_bytes, const moe_options* opts,

@@ -23,6 +23,10 @@ MOE_ERR_CUDA, MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_DEVICE_INDEX, MOE_ERR_ALIGNMENT = 
 ORIENT_AUTO, ORIENT_SWAP_AB, ORIENT_TOKEN_MAJOR = 0, 1, 2
 STAGES = ("route", "align", "gather", "gemm1", "act", "gemm2", "combine")
 NUM_STAGES = len(STAGES)
+# phase stamps of the single-launch kernel (moe_options.trace), in the order of moe_trace_event
+TRACE_EVENTS = ("start", "router", "barrier0", "topk", "barrier1", "tables", "gathered", "g1_issued", "g2_ready",
+                "issued", "mma_done", "g1_done", "epi_done", "comb_first", "comb_done", "end")
+TRACE_WORDS = len(TRACE_EVENTS)
 
 # every entry point include/moe_api.h declares
 EXPORTS = ("moe_strerror", "moe_workspace_size", "moe_plan_info", "moe_align_capacity", "moe_route",
@@ -39,14 +43,15 @@ class MoeError(RuntimeError):
 
 class moe_options(ctypes.Structure):
     _fields_ = [("orientation", ctypes.c_int), ("split_k", ctypes.c_int), ("inject_timeout", ctypes.c_int),
-                ("act_split", ctypes.c_int), ("stage_begin", ctypes.c_void_p * NUM_STAGES),
+                ("act_split", ctypes.c_int), ("trace", ctypes.c_void_p), ("single_launch", ctypes.c_int),
+                ("stage_begin", ctypes.c_void_p * NUM_STAGES),
                 ("stage_end", ctypes.c_void_p * NUM_STAGES)]
 
 
 class moe_plan(ctypes.Structure):
     _fields_ = [("orientation", ctypes.c_int), ("block", ctypes.c_int), ("splits_gemm1", ctypes.c_int),
                 ("splits_gemm2", ctypes.c_int), ("act_split", ctypes.c_int), ("kernel_launches", ctypes.c_int),
-                ("workspace_bytes", ctypes.c_size_t)]
+                ("single_launch", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t)]
 
 
 def _load():
@@ -128,6 +133,9 @@ def _opts(options) -> Optional[ctypes.POINTER(moe_options)]:
     o.split_k = int(options.get("split_k", 0))
     o.inject_timeout = int(options.get("inject_timeout", 0))
     o.act_split = int(options.get("act_split", 0))
+    o.single_launch = int(options.get("single_launch", 0))
+    if options.get("trace") is not None:
+        o.trace = ctypes.c_void_p(options["trace"].data_ptr())
     for name, ev in (options.get("stage_begin") or {}).items():
         o.stage_begin[STAGES.index(name)] = ctypes.c_void_p(ev.cuda_event)
     for name, ev in (options.get("stage_end") or {}).items():

@@ -47,6 +47,12 @@ constexpr int kPlanSms = 152;
 constexpr int kRouterTcMinTokens = 256;
 // Largest swap-AB activation tile whose rows GEMM1 gathers itself.
 constexpr int kGatherInGemmMaxRows = 32;
+// Single-launch decode kernel limits (shared-memory tables, one token column per epilogue thread).
+constexpr int kFusedMaxTokens = 64;
+constexpr int kFusedMaxPairs = 512;
+constexpr int kFusedMaxExperts = 256;
+// moe_options.single_launch == 0 picks the single-launch kernel for eligible shapes.
+constexpr bool kFusedAuto = false;
 
 enum Path { PATH_F32 = 0, PATH_BF16 = 1, PATH_FP8 = 2 };
 
@@ -61,6 +67,8 @@ struct Plan {
   bool y_bf16 = false;
   bool act_split = false;  // bf16 intermediate stored as hi + lo parts (two MMAs in GEMM2)
   bool gather_in_gemm = false;  // GEMM1 gathers its activation rows itself (TMA tile::gather4)
+  bool fused = false;           // the whole layer as one cooperative kernel
+  size_t o_sync = 0;
   size_t o_logits = 0, o_tw = 0, o_tid = 0, o_meta = 0, o_sorted = 0, o_eids = 0, o_xs = 0, o_aint = 0, o_af32 = 0,
          o_p1 = 0, o_y = 0, o_misc = 0, total = 0;
   size_t p1_stride = 0, y_stride = 0;
@@ -163,6 +171,12 @@ static int make_plan(int T, int H, int I, int E, int topk, moe_dtype act, moe_dt
   }
   p.cap = n + std::min<long>(E, n) * (p.B - 1);
   p.nblk_cap = p.cap / p.B;
+  const int single = opts ? opts->single_launch : 0;
+  if (single < 0 || single > 2) return MOE_ERR_ARG;
+  const bool fused_ok = p.path == PATH_BF16 && p.swap && T <= kFusedMaxTokens && n <= kFusedMaxPairs &&
+                        E <= kFusedMaxExperts;
+  if (single == 1 && !fused_ok) return MOE_ERR_UNSUPPORTED;
+  p.fused = fused_ok && (single == 1 || (single == 0 && kFusedAuto));
 
   const size_t A = 256;
   size_t o = 0;
@@ -192,6 +206,7 @@ static int make_plan(int T, int H, int I, int E, int topk, moe_dtype act, moe_dt
   p.y_stride = (size_t)n * H;
   p.o_y = take(p.y_stride * p.s2 * (p.y_bf16 ? 2 : 4));
   p.o_misc = take(256);
+  if (p.fused) p.o_sync = take(fused_sync_bytes(T, H, I, E));
   p.total = o;
   *pl = p;
   return MOE_OK;
@@ -291,7 +306,9 @@ int moe_plan_info(int T, int H, int I, int E, int topk, moe_dtype act_dtype, moe
   if (!p.gather_in_gemm) n += 1;            // row gather (FP8: with input quantisation)
   if (p.path == PATH_FP8) n += p.gather_in_gemm ? 3 : 2;  // input amax (+ input quantisation), intermediate quantisation
   if (p.s1 > 1) n += 1;
+  if (p.fused) n = 1;
   info->kernel_launches = T > 0 ? n : 0;
+  info->single_launch = p.fused ? 1 : 0;
   info->workspace_bytes = p.total;
   return MOE_OK;
 }
@@ -391,6 +408,60 @@ int moe_forward(const void* hidden, const void* router_w, const void* w13, const
     e = (x);                       \
     if (e != cudaSuccess) return MOE_ERR_CUDA; \
   } while (0)
+
+  if (pl.fused && !(o && o->inject_timeout)) {
+    // steps 1-7 in one cooperative kernel; its events bracket the kernel as GEMM1
+    if (o) {
+      for (int st = MOE_STAGE_ROUTE; st < MOE_STAGE_GEMM1; ++st) {
+        record(o->stage_begin[st], s);
+        record(o->stage_end[st], s);
+      }
+      record(o->stage_begin[MOE_STAGE_GEMM1], s);
+    }
+    FusedArgs fa = {};
+    fa.T = T;
+    fa.H = H;
+    fa.I = I;
+    fa.E = E;
+    fa.k = topk;
+    fa.renorm = renorm != 0;
+    fa.s1 = pl.s1;
+    fa.kbs1 = pl.kb1;
+    fa.s2 = pl.s2;
+    fa.kbs2 = pl.kb2;
+    fa.xbox = pl.xbox;
+    fa.gather = pl.gather_in_gemm;
+    fa.act_split = pl.act_split;
+    fa.cap = cap;
+    fa.combine_g = combine_lanes(T, H, topk);
+    fa.X = hidden;
+    fa.Wr = router_w;
+    fa.w13 = w13;
+    fa.w2 = w2;
+    fa.logits = logits;
+    fa.topk_w = tw;
+    fa.topk_ids = tid;
+    fa.Xs = xs;
+    fa.aint = aint;
+    fa.p1 = p1;
+    fa.p1_stride = pl.p1_stride;
+    fa.y = reinterpret_cast<float*>(y);
+    fa.y_stride = pl.y_stride;
+    fa.out = out;
+    fa.sync = ws + pl.o_sync;
+    fa.trace = o ? o->trace : nullptr;
+    fa.status = st;
+    fa.num_sms = sms;
+    if (launch_decode_fused(fa, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (o) {
+      record(o->stage_end[MOE_STAGE_GEMM1], s);
+      for (int st = MOE_STAGE_ACT; st < MOE_NUM_STAGES; ++st) {
+        record(o->stage_begin[st], s);
+        record(o->stage_end[st], s);
+      }
+    }
+    return MOE_OK;
+  }
 
   if (o && o->inject_timeout) {
     MOE_TRY(cudaMemsetAsync(flag, 0, sizeof(int), s));

@@ -114,6 +114,28 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// The same wait by all 32 lanes of a warp together: every lane polls, and
+// the outcome (done / gave up) is decided warp-wide each round, so the warp
+// never splits into a spinning lane and lanes parked elsewhere.  Roles that
+// issue from one lane wait this way and predicate only the issue itself.
+__device__ __forceinline__ bool mbar_wait_all(uint32_t bar, uint32_t parity, volatile int* abort, int* status) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    if (it == 0) t0 = globaltimer_ns();
+    if ((it & 31u) == 31u) {
+      const bool give_up = *abort || (globaltimer_ns() - t0 > kWaitLimitNs);
+      if (__any_sync(0xffffffffu, give_up)) {
+        if ((threadIdx.x & 31) == 0 && !*abort) {
+          *abort = 1;
+          report(status, MOE_ERR_DEVICE_TIMEOUT);
+        }
+        return false;
+      }
+    }
+  }
+}
+
 // Drain wait used on the abort path only: ignores the abort flag, own limit.
 __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
@@ -233,8 +255,32 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// CTA and named barriers for warp-specialised code.  Every lane of a warp
+// reaches the barrier, but possibly not together (lane 0 may still be issuing
+// MMAs or storing a flag): __syncwarp() first reconverges the warp, then the
+// .aligned barrier, whose arrivals count whole warps, is well defined.  (An
+// aligned barrier reached by a diverged warp can release early; the
+// non-aligned form is defined but can stall for microseconds while the warp
+// scheduler switches to the lagging lanes.)
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  __syncwarp();
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+__device__ __forceinline__ void cta_sync() {
+  __syncwarp();
+  __syncthreads();
+}
+// OR of a flag over the nthreads threads of named barrier id.
+__device__ __forceinline__ bool named_bar_any(int id, int nthreads, bool v) {
+  __syncwarp();
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\tbar.red.or.pred po, %2, %3, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
 }
 
 // Programmatic dependent launch: wait for the preceding kernel's results /

@@ -126,15 +126,7 @@ __device__ __forceinline__ Tile tile_at(const TcDev& p, int t) {
 }
 
 // OR of a flag over the 128 epilogue threads (named barrier 1).
-__device__ __forceinline__ bool epi_any(bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\tbar.red.or.pred po, 1, 128, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)v)
-      : "memory");
-  return r != 0;
-}
+__device__ __forceinline__ bool epi_any(bool v) { return named_bar_any(1, 128, v); }
 
 template <bool SWAP, bool FP8, int EPI>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -147,7 +139,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t bar_tfull = bar_empty + 8 * kMaxStages;
   const uint32_t bar_tempty = bar_tfull + 16;
   const uint32_t bar_drain = bar_tempty + 16;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + p.bar_off + 8 * (2 * kMaxStages + 5));
+  const uint32_t bar_exit = bar_drain + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + p.bar_off + 8 * (2 * kMaxStages + 6));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -161,6 +154,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(bar_tempty + 8 * b, 128);
     }  // (buffer 1 unused when nbuf == 1)
     mbar_init(bar_drain, 1);
+    mbar_init(bar_exit, kTcThreads / 32);
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmW);
@@ -168,7 +162,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
   tc_fence_before();
-  __syncthreads();
+  cta_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -183,8 +177,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (warp == 0) {
     // ---------------- TMA producer (warp 0) ----------------
-    // Lane 0 waits for free stages, arms their barriers and loads the weight
-    // tiles.  The activation tile is either one tiled load of consecutive
+    // The warp waits for free stages together; lane 0 arms their barriers and
+    // loads the weight tiles.  The activation tile is either one tiled load of consecutive
     // sorted rows (lane 0), or -- when the activations are gathered -- one
     // tile::gather4 load per group of 4 rows, issued by the 32 lanes in
     // parallel with the token row of each sorted (token, slot) pair.
@@ -205,6 +199,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tma_load_2d(sw + p.wbox * 128, &tmW, (d.kb0 + i) * KBLK, d.wr0 + p.w_pair_off, fb);
       }
     }
+    pre = __shfl_sync(0xffffffffu, pre, 0);
     pdl_wait();
     const int n_pairs = p.T * p.k;
     const int npp = (EPI == TC_EPI_LOGITS) ? 0 : p.meta[META_NPP];
@@ -228,20 +223,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int kb = d.kb0; kb < d.kb1; ++kb) {
         const uint32_t sw = sbase + stage * p.stage_bytes;
         const uint32_t fb = bar_full + 8 * stage;
-        uint32_t good = 1;
-        if (lane == 0 && (int)issued >= pre) {  // (the first `pre` stages already hold their weight tiles)
-          if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p.status)) {
-            good = 0;
-          } else {
+        if ((int)issued >= pre) {  // (the first `pre` stages already hold their weight tiles)
+          if (!mbar_wait_all(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
             mbar_arrive_expect_tx(fb, p.stage_bytes);
             tma_load_2d(sw, &tmW, kb * KBLK, d.wr0, fb);
             tma_load_2d(sw + p.wbox * 128, &tmW, kb * KBLK, d.wr0 + p.w_pair_off, fb);
           }
-        }
-        good = __shfl_sync(0xffffffffu, good, 0);
-        if (!good) {
-          ok = false;
-          break;
+          __syncwarp();
         }
         if (p.gather) {
 #pragma unroll
@@ -272,29 +264,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mbar_wait_drain(bar_full + 8 * (i % p.stages), (i / p.stages) & 1u, 100000000ull);
       }
     }
+    __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer ----------------
-      pdl_wait();
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      bool ok = true, any = false;
-      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-        const Tile d = tile_at<SWAP, EPI>(p, t);
-        const int N = SWAP ? d.npad : 2 * p.wbox;
-        const uint32_t idesc = idesc_make(128, N, FP8);
-        if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag, p.status)) {
+    // ---------------- MMA issuer ----------------
+    // The whole warp runs the loop and waits together; lane 0 issues the MMAs
+    // and their commits (a commit tracks the MMAs of its own thread).
+    pdl_wait();
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool ok = true, any = false;
+    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      const Tile d = tile_at<SWAP, EPI>(p, t);
+      const int N = SWAP ? d.npad : 2 * p.wbox;
+      const uint32_t idesc = idesc_make(128, N, FP8);
+      if (!mbar_wait_all(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t dt = tmem_base + (uint32_t)(acc * p.buf_cols);
+      for (int kb = d.kb0; kb < d.kb1; ++kb) {
+        if (!mbar_wait_all(bar_full + 8 * stage, phase, abort_flag, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t dt = tmem_base + (uint32_t)(acc * p.buf_cols);
-        for (int kb = d.kb0; kb < d.kb1; ++kb) {
-          if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+        if (lane == 0) {
           const uint32_t sw = sbase + stage * p.stage_bytes;
           const uint32_t sx = sw + p.w_bytes;
           // the optional low bf16 part of the activations goes into the same fp32
@@ -320,24 +315,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
           }
           tc_commit(bar_empty + 8 * stage);
-          any = true;
-          if (++stage == p.stages) {
-            stage = 0;
-            phase ^= 1u;
-          }
         }
-        if (!ok) break;
-        tc_commit(bar_tfull + 8 * acc);
-        if (++acc == p.nbuf) {
-          acc = 0;
-          acc_phase ^= 1u;
+        __syncwarp();
+        any = true;
+        if (++stage == p.stages) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
-      if (!ok && any) {  // the tensor core must be idle before tensor memory is freed
-        tc_commit(bar_drain);
-        mbar_wait_drain(bar_drain, 0, 100000000ull);
+      if (!ok) break;
+      if (lane == 0) tc_commit(bar_tfull + 8 * acc);
+      __syncwarp();
+      if (++acc == p.nbuf) {
+        acc = 0;
+        acc_phase ^= 1u;
       }
     }
+    if (!ok && any) {  // the tensor core must be idle before tensor memory is freed
+      if (lane == 0) tc_commit(bar_drain);
+      __syncwarp();
+      mbar_wait_drain(bar_drain, 0, 100000000ull);
+    }
+    __syncwarp();
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
     pdl_wait();
@@ -351,7 +350,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int n_pairs = p.T * p.k;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
       const Tile d = tile_at<SWAP, EPI>(p, t);
-      const bool ok = mbar_wait(bar_tfull + 8 * acc, acc_phase, abort_flag, p.status);
+      const bool ok = mbar_wait_all(bar_tfull + 8 * acc, acc_phase, abort_flag, p.status);
       if (epi_any(!ok)) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.buf_cols);
@@ -497,7 +496,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(bar_tempty + 8 * acc);
-      if (++acc == 2) {
+      if (++acc == p.nbuf) {
         acc = 0;
         acc_phase ^= 1u;
       }
@@ -509,9 +508,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   }
 
+  // Each warp reports the end of its role on an mbarrier; warp 1 frees tensor
+  // memory once every warp has.  (A CTA-wide bar.sync here, reached by warps
+  // coming out of different roles, was seen to release before all warps had
+  // arrived.)
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar_exit);
   if (warp == 1) {
+    mbar_wait_drain(bar_exit, 0, 2 * kWaitLimitNs);
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
@@ -520,38 +526,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
-
-// 2-D K-major tensor [rows][K] of 1- or 2-byte elements, box = 128 bytes of K x box_rows, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, int elem_bytes, uint64_t K, uint64_t rows, uint32_t box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {K, rows};
-  const cuuint64_t strides[1] = {K * (uint64_t)elem_bytes};
-  const cuuint32_t box[2] = {(cuuint32_t)(128 / elem_bytes), box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUtensorMapDataType dt = elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <bool SWAP, bool FP8, int EPI>
 cudaError_t launch_inst(const CUtensorMap& mw, const CUtensorMap& mx, const TcDev& p, int grid, size_t smem,
                         cudaStream_t s) {
@@ -579,16 +553,48 @@ cudaError_t launch_inst(const CUtensorMap& mw, const CUtensorMap& mx, const TcDe
 
 }  // namespace
 
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D K-major tensor [rows][K] of 1- or 2-byte elements, box = 128 bytes of K x box_rows, 128-byte swizzle.
+bool make_tensor_map_2d(CUtensorMap* m, const void* base, int elem_bytes, uint64_t K, uint64_t rows, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {K, rows};
+  const cuuint64_t strides[1] = {K * (uint64_t)elem_bytes};
+  const cuuint32_t box[2] = {(cuuint32_t)(128 / elem_bytes), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType dt = elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s) {
   const int eb = a.fp8 ? 1 : 2;
   CUtensorMap mw, mx;
-  if (!make_map(&mw, a.W, eb, (uint64_t)a.K, (uint64_t)a.E * a.w_rows_per_expert, (uint32_t)a.wbox))
+  if (!make_tensor_map_2d(&mw, a.W, eb, (uint64_t)a.K, (uint64_t)a.E * a.w_rows_per_expert, (uint32_t)a.wbox))
     return cudaErrorInvalidValue;
   if (a.gather) {
     // tile::gather4 needs a one-row box: 4 such rows per instruction
     if (a.xbox % 4 || a.xbox > 256 || a.x_lo_rows) return cudaErrorInvalidValue;
-    if (!make_map(&mx, a.X, eb, (uint64_t)a.K, (uint64_t)a.T, 1u)) return cudaErrorInvalidValue;
-  } else if (!make_map(&mx, a.X, eb, (uint64_t)a.K, (uint64_t)a.cap + (uint64_t)a.x_lo_rows, (uint32_t)a.xbox)) {
+    if (!make_tensor_map_2d(&mx, a.X, eb, (uint64_t)a.K, (uint64_t)a.T, 1u)) return cudaErrorInvalidValue;
+  } else if (!make_tensor_map_2d(&mx, a.X, eb, (uint64_t)a.K, (uint64_t)a.cap + (uint64_t)a.x_lo_rows, (uint32_t)a.xbox)) {
     return cudaErrorInvalidValue;
   }
 
@@ -625,7 +631,7 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s) {
 
   p.w_bytes = (uint32_t)(2 * a.wbox * 128);
   p.stage_bytes = p.w_bytes + (uint32_t)(a.xbox * 128) * (a.x_lo_rows ? 2u : 1u);
-  const uint32_t bar_bytes = 8 * (2 * kMaxStages + 5) + 16;
+  const uint32_t bar_bytes = 8 * (2 * kMaxStages + 6) + 16;
   const uint32_t budget = 227 * 1024 - 1024 - bar_bytes;
   int stages = (int)(budget / p.stage_bytes);
   if (stages > kMaxStages) stages = kMaxStages;

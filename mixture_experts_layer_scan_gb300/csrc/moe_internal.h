@@ -54,6 +54,8 @@ cudaError_t launch_quant_act(const float* A, int I, const int32_t* meta, int cap
 // out[t] = sum_j w[t][j] * sum_s Y[s][t*k+j]   (Y fp32 or bf16, out fp32 or bf16)
 cudaError_t launch_combine(const void* Y, int y_bf16, int splits, size_t split_stride, const float* w, int T, int k,
                            int H, void* out, int out_bf16, cudaStream_t s);
+// lanes G that share one output vector in the combine (H % 8 == 0); fixes its addition order
+int combine_lanes(int T, int H, int k);
 
 // ---- fp32 CUDA-core grouped GEMMs ---------------------------------------------
 cudaError_t launch_gemm1_simt(const float* Xs, const float* W13, int H, int I, int B, const int32_t* eids,
@@ -109,6 +111,45 @@ struct TcGemmArgs {
   int num_sms;
 };
 cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s);
+
+// 2-D K-major tensor map [rows][K] of 1- or 2-byte elements: box of 128 bytes
+// of K x box_rows, 128-byte swizzle.
+bool make_tensor_map_2d(CUtensorMap* m, const void* base, int elem_bytes, uint64_t K, uint64_t rows,
+                        uint32_t box_rows);
+
+// ---- single-launch decode layer (bf16, swap-AB) ----------------------------------
+struct FusedArgs {
+  int T, H, I, E, k, renorm;
+  int s1, kbs1, s2, kbs2;  // K splits and K blocks (128 bytes) per split of GEMM1 / GEMM2
+  int xbox;                // tokens rounded up to 16 (<= 64)
+  bool gather;             // GEMM1 gathers token rows itself (xbox <= 32); else rows go to Xs first
+  bool act_split;          // intermediate as bf16 hi + lo
+  int cap;                 // rows of Xs / of each intermediate part
+  int combine_g;           // lanes per output of the stand-alone combine (same sum order)
+  const void* X;           // [T][H] bf16
+  const void* Wr;          // [E][H] bf16
+  const void* w13;         // [E][2I][H] bf16
+  const void* w2;          // [E][H][I] bf16
+  float* logits;           // [T][E]
+  float* topk_w;           // [T][k]
+  int32_t* topk_ids;       // [T][k]
+  void* Xs;                // [cap][H] (gather == false)
+  void* aint;              // [cap][I] (x2 with act_split)
+  float* p1;               // [s1][T*k][2I] (s1 > 1)
+  size_t p1_stride;
+  float* y;                // [s2][T*k][H]
+  size_t y_stride;
+  void* out;               // [T][H] bf16
+  void* sync;              // fused_sync_bytes(E, I, H, T) bytes, 256-aligned
+  void* trace;             // nullable: MOE_TRACE_WORDS uint64 per CTA
+  int* status;
+  int num_sms;
+};
+// bytes of the launch tag and counters the single-launch kernel keeps in the workspace
+size_t fused_sync_bytes(int T, int H, int I, int E);
+// shared memory the single-launch kernel needs beyond its stage ring
+size_t fused_table_bytes(int T, int E, int k);
+cudaError_t launch_decode_fused(const FusedArgs& a, cudaStream_t s);
 
 // status word of the current device
 int* status_word();

@@ -544,12 +544,17 @@ cudaError_t launch_quant_act(const float* A, int I, const int32_t* meta, int cap
   return cudaGetLastError();
 }
 
+int combine_lanes(int T, int H, int k) {
+  // small batches: split each output's routed slots over G lanes for more parallelism
+  const size_t vecs = (size_t)T * (H / 8);
+  return vecs >= (size_t)152 * 2048 ? 1 : (k >= 4 ? 4 : (k >= 2 ? 2 : 1));
+}
+
 template <bool YB, bool OB>
 static cudaError_t combine_vec(const void* Y, int splits, size_t split_stride, const float* w, int T, int k, int H,
                                void* out, cudaStream_t s) {
-  // small batches: split each output's routed slots over G lanes for more parallelism
+  const int G = combine_lanes(T, H, k);
   const size_t vecs = (size_t)T * (H / 8);
-  const int G = vecs >= (size_t)152 * 2048 ? 1 : (k >= 4 ? 4 : (k >= 2 ? 2 : 1));
   const int grid = grid_for(vecs * G, 256);
   if (G == 4) MOE_LAUNCH(k_combine<YB, OB, 4>, dim3(grid), dim3(256), 0, s, Y, splits, split_stride, w, T, k, H, out);
   else if (G == 2) MOE_LAUNCH(k_combine<YB, OB, 2>, dim3(grid), dim3(256), 0, s, Y, splits, split_stride, w, T, k, H, out);

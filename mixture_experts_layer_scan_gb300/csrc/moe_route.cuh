@@ -1,0 +1,172 @@
+// Router building blocks shared by the stand-alone routing kernels and the
+// single-launch decode kernel, so both compute bit-identical logits, weights
+// and expert ids.
+//
+// "FusedMoE vs MegaMoE" (zwxr.cn), section 2: the router gives each token a
+// weight distribution over the experts, and the k highest-weight experts
+// process it.  The selection ranks the fp32 logits (softmax is strictly
+// increasing, so this is the ranking of the probabilities); equal logits rank
+// the lower expert index first.  Weights are softmax over all E experts,
+// renormalised over the k chosen ones on request.
+#pragma once
+
+#include "moe_device.cuh"
+
+namespace moe {
+
+constexpr int kRouterWarps = 8;  // threads of a router block: kRouterWarps * 32
+
+// 16-byte vector of router inputs, widened to fp32.
+__device__ __forceinline__ void router_load16(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = bf16_bits_to_f32(w[i] & 0xffffu);
+    v[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+  }
+}
+__device__ __forceinline__ void router_load16(const float* p, float (&v)[4]) {
+  const float4 u = *reinterpret_cast<const float4*>(p);
+  v[0] = u.x;
+  v[1] = u.y;
+  v[2] = u.z;
+  v[3] = u.w;
+}
+
+// logits[t][e] = sum_h X[t][h] * Wr[e][h] for tokens t0 .. t0+TT-1 (< T) of
+// one expert, by kRouterWarps * 32 threads (all threads of the block must
+// call).  The warps split H into interleaved 16-byte vectors (one pass over
+// Wr[e]); each lane accumulates its vectors in order with fma, each warp
+// reduces with a fixed butterfly and the warp sums are added in warp order,
+// so the value of a logit depends neither on TT nor on scheduling.
+// red: shared scratch of kRouterWarps * TT floats.
+template <typename TIn, int TT>
+__device__ __forceinline__ void router_block(const TIn* __restrict__ X, const TIn* __restrict__ Wr, int T, int H,
+                                             int E, int t0, int e, float* __restrict__ logits, float* red) {
+  constexpr int V = 16 / sizeof(TIn);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nt = min(TT, T - t0);
+  float acc[TT];
+#pragma unroll
+  for (int b = 0; b < TT; ++b) acc[b] = 0.0f;
+  const TIn* w = Wr + (size_t)e * H;
+  for (int h = (warp * 32 + lane) * V; h < H; h += kRouterWarps * 32 * V) {
+    float wv[V];
+    router_load16(w + h, wv);
+#pragma unroll
+    for (int b = 0; b < TT; ++b) {
+      if (b < nt) {
+        float xv[V];
+        router_load16(X + (size_t)(t0 + b) * H + h, xv);
+#pragma unroll
+        for (int q = 0; q < V; ++q) acc[b] = fmaf(wv[q], xv[q], acc[b]);
+      }
+    }
+  }
+#pragma unroll
+  for (int b = 0; b < TT; ++b) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], off);
+    if (lane == 0) red[warp * TT + b] = acc[b];
+  }
+  cta_sync();
+  if ((int)threadIdx.x < nt) {
+    float sum = 0.0f;
+#pragma unroll
+    for (int w8 = 0; w8 < kRouterWarps; ++w8) sum += red[w8 * TT + threadIdx.x];
+    logits[(size_t)(t0 + threadIdx.x) * E + e] = sum;
+  }
+  cta_sync();  // red is free again
+}
+
+constexpr int kTopkCache = 8;  // logits per lane kept in registers by the top-k
+
+// (value, index) order of the ranking: larger value first, lower index on ties.
+__device__ __forceinline__ bool ranks_before(float v, int i, float bv, int bi) {
+  return v > bv || (v == bv && i < bi);
+}
+
+// logit loads: through L1, or L2 only (CG) when another block of the same
+// kernel wrote them
+template <bool CG>
+__device__ __forceinline__ float topk_ld(const float* p) {
+  if constexpr (CG)
+    return __ldcg(p);
+  else
+    return *p;
+}
+
+// Top-k of one token's E logits by one warp (all 32 lanes call).  k rounds of
+// a warp arg-max over the experts not yet taken; each lane owns experts lane,
+// lane+32, ... and a bit mask of the ones already taken; lane j keeps the
+// j-th pick and writes ids[j], w[j].
+template <bool CG>
+__device__ __forceinline__ void topk_warp(const float* __restrict__ l, int E, int k, int renorm,
+                                          float* __restrict__ w_out, int32_t* __restrict__ id_out) {
+  const int lane = threadIdx.x & 31;
+  // the first kTopkCache logits of this lane stay in registers (all of them for E <= 256);
+  // the scan order and arithmetic are those of a plain loop over e = lane, lane+32, ...
+  float cache[kTopkCache];
+#pragma unroll
+  for (int q = 0; q < kTopkCache; ++q) cache[q] = (lane + 32 * q < E) ? topk_ld<CG>(l + lane + 32 * q) : -INFINITY;
+  uint32_t taken = 0;  // bit q: expert lane + 32*q taken
+  float my_v = 0.0f;
+  int my_i = 0;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int q = 0; q < kTopkCache; ++q) {
+      const int e = lane + 32 * q;
+      if (e < E && !(taken & (1u << q)) && ranks_before(cache[q], e, bv, bi)) {
+        bv = cache[q];
+        bi = e;
+      }
+    }
+    for (int q = kTopkCache, e = lane + 32 * kTopkCache; e < E; ++q, e += 32) {
+      if (taken & (1u << q)) continue;
+      const float v = topk_ld<CG>(l + e);
+      if (ranks_before(v, e, bv, bi)) {
+        bv = v;
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (ranks_before(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (bi < 0 || bi >= E) bi = 0;  // only reachable with NaN logits
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (lane == j) {
+      my_v = bv;
+      my_i = bi;
+    }
+  }
+  // softmax: m is the largest logit (the first pick); each lane sums its experts in ascending order
+  const float m = __shfl_sync(0xffffffffu, my_v, 0);
+  const float ex = (lane < k) ? expf(my_v - m) : 0.0f;
+  float denom;
+  if (renorm) {
+    denom = ex;
+  } else {
+    denom = 0.0f;
+#pragma unroll
+    for (int q = 0; q < kTopkCache; ++q)
+      if (lane + 32 * q < E) denom += expf(cache[q] - m);
+    for (int e = lane + 32 * kTopkCache; e < E; e += 32) denom += expf(topk_ld<CG>(l + e) - m);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) denom += __shfl_xor_sync(0xffffffffu, denom, off);
+  if (lane < k) {
+    id_out[lane] = my_i;
+    w_out[lane] = ex / denom;
+  }
+}
+
+}  // namespace moe

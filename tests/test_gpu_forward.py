@@ -62,6 +62,17 @@ def test_bf16_swap_ab(moe, T, H, I, E, k):
     assert rel_err(out.float().cpu().numpy(), _ref(L)) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("T", [200, 256])
+def test_bf16_swap_ab_wide_token_tiles(moe, T):
+    """Forced swap-AB beyond 128 tokens: one accumulator buffer per CTA (2 x 256 tensor-memory columns),
+    and more tiles than SMs, so CTAs run several tiles through that single buffer."""
+    L = _layer("prefill", T=T, H=512, I=512, E=64, k=8)
+    plan = moe.moe_plan_info(T, 512, 512, 64, 8, moe.MOE_BF16, moe.MOE_BF16, {"orientation": 1})
+    assert plan["orientation"] == moe.ORIENT_SWAP_AB
+    out = _run(moe, L, {"orientation": 1})
+    assert rel_err(out.float().cpu().numpy(), _ref(L), f"swap-AB T={T}") <= TOL["bf16"]
+
+
 @pytest.mark.parametrize("T,H,I,E,k", [(65, 256, 256, 8, 2), (200, 384, 256, 8, 2), (513, 256, 384, 16, 4),
                                        (300, 512, 128, 64, 8)])
 def test_bf16_token_major(moe, T, H, I, E, k):
