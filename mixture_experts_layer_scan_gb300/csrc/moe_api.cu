@@ -51,6 +51,8 @@ constexpr int kGatherInGemmMaxRows = 32;
 constexpr int kFusedMaxTokens = 64;
 constexpr int kFusedMaxPairs = 512;
 constexpr int kFusedMaxExperts = 256;
+// Largest batch whose single-launch GEMM1 keeps the K splits of the multi-kernel plan.
+constexpr int kFusedSplitMaxTokens = 8;
 // moe_options.single_launch == 0 picks the single-launch kernel for eligible shapes.
 constexpr bool kFusedAuto = false;
 
@@ -177,6 +179,13 @@ static int make_plan(int T, int H, int I, int E, int topk, moe_dtype act, moe_dt
                         E <= kFusedMaxExperts;
   if (single == 1 && !fused_ok) return MOE_ERR_UNSUPPORTED;
   p.fused = fused_ok && (single == 1 || (single == 0 && kFusedAuto));
+  if (p.fused && T > kFusedSplitMaxTokens && !(opts && opts->split_k > 0)) {
+    // in the single launch the CTA finishing a tile's last K split sums the
+    // splits for all of the expert's tokens; past a few tokens that serial
+    // reduction costs more than the splits gain, so GEMM1 runs unsplit
+    p.s1 = 1;
+    p.kb1 = H * (p.path == PATH_FP8 ? 1 : 2) / 128;
+  }
 
   const size_t A = 256;
   size_t o = 0;

@@ -14,7 +14,8 @@
 // Phases (every CTA, 256 threads):
 //   0  router logits, (expert, 4-token group) units spread over the CTAs
 //   -- grid barrier --
-//   1  top-k and softmax weights, one warp per token
+//   1  top-k and softmax weights, one warp per token (up to 8 tokens: every
+//      CTA ranks all tokens itself and skips the next barrier)
 //   -- grid barrier --
 //   2  every CTA builds the expert tables of the batch in shared memory
 //      (stable counting sort of the (token, slot) pairs); batches over 32
@@ -27,13 +28,15 @@
 //        GEMM1 tile (expert e, 128 intermediate columns, K split s): SiLU(gate)*up
 //          into the bf16 intermediate (hi + lo parts); with K splits, fp32
 //          partials, and the CTA that completes the last split of a tile sums
-//          them in split order.  A finished tile increments ready[e].
+//          them in split order.  A finished tile sets its ready flag.
 //        GEMM2 tile (expert e, 256 hidden rows, K split s): fp32 Y rows; its
 //          producer streams the W2 tiles at once and loads the intermediate
-//          only once ready[e] shows all of expert e's GEMM1 tiles.  For every
-//          token of the tile a counter per (token, 256 hidden rows) counts the
-//          arrived (slot, split) outputs; the tile that completes a token's
-//          count computes its weighted sum over the k slots.
+//          columns of each K block once the GEMM1 tile that produces them is
+//          final.  For every token of the tile a counter per (token, 256
+//          hidden rows) counts the arrived (slot, split) outputs.
+//      Warps 6-7, and every other warp once its role is done, run the combine:
+//      they claim (token, 128 hidden rows) units from a grid-wide counter, wait
+//      for the unit's count and write the weighted sum over the k slots.
 //
 // Every arithmetic step is the one the multi-kernel path performs, in the same
 // order (same tiles, K splits, MMA sequence, split-order sums, combine order),
@@ -61,8 +64,9 @@ constexpr int kFRouterTT = 16;  // tokens per router unit
 constexpr uint32_t kFTmemCols = 512;
 constexpr int kFBarBytes = 256;  // mbarriers + small shared words
 
-// words of the sync region: three grid barriers, the exit count, then the dependency counters
-enum { SYNC_BAR0 = 0, SYNC_EXIT = 3, SYNC_NBAR = 4 };
+// words of the sync region: three grid barriers, the exit count, the next free
+// combine unit, then the dependency counters
+enum { SYNC_BAR0 = 0, SYNC_EXIT = 3, SYNC_CNEXT = 4, SYNC_NBAR = 8 };
 
 struct FusedDev {
   int T, H, I, E, k, renorm;
@@ -89,7 +93,7 @@ struct FusedDev {
   __nv_bfloat16* out;    // [T][H]
   unsigned long long* trace;  // nullable: MOE_TRACE_WORDS %globaltimer stamps per CTA
   unsigned long long* go;  // grid id of the launch whose counters are zeroed
-  unsigned* sync;          // SYNC_NBAR barrier words, arr1[E*n1], ready[E], cnt2[T*n2]
+  unsigned* sync;          // SYNC_NBAR barrier words, arr1[E*n1], ready1[E*n1], cnt2[T*n2]
   int nsync;
   int* status;
 };
@@ -242,69 +246,99 @@ __device__ __forceinline__ FTile ftile_at(const FusedDev& p, int t, int n_g1, co
 __device__ __forceinline__ bool f_epi_any(bool v) { return named_bar_any(1, 128, v); }
 __device__ __forceinline__ bool f_comb_any(bool v) { return named_bar_any(2, 64, v); }
 
-// out[t][h] for one token and the four hidden indices h0 + 64 q of this thread,
-// with the arithmetic of the stand-alone combine: lane g of G sums the slots
-// j = g, g+G, ... (each the sum of its K-split outputs in split order) with
-// fma, then the G partial sums are added in its butterfly order.  The (slot,
-// split) rows are visited in their natural order, which keeps every lane's
-// chain in order; their loads go out eight rows at a time.
+// out[t][h4 .. h4+3] for one token, with the arithmetic of the stand-alone
+// combine: lane g of G sums the slots j = g, g+G, ... (each the sum of its
+// K-split outputs in split order) with fma, then the G partial sums are added
+// in its butterfly order.  The (slot, split) rows are visited in their natural
+// order, which keeps every lane's chain in order; their 16-byte loads go out
+// eight rows at a time (the tail of a batch re-reads the last row).
 template <int G>
-__device__ __forceinline__ void combine_unit(const FusedDev& p, int t, int h0, const float* wsm) {
-  float acc[G][4], yj[G][4];
+__device__ __forceinline__ void combine_unit(const FusedDev& p, int t, int h4, const float* wsm) {
+  float acc[G][4];
 #pragma unroll
   for (int g = 0; g < G; ++g)
 #pragma unroll
-    for (int q = 0; q < 4; ++q) acc[g][q] = yj[g][q] = 0.0f;
+    for (int q = 0; q < 4; ++q) acc[g][q] = 0.0f;
+  float yj[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   const int rows = p.k * p.s2;
+  const float* ybase = p.y + (size_t)t * p.k * p.H + h4;
   for (int r0 = 0; r0 < rows; r0 += 8) {
-    float v[8][4];
+    float4 v[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const int r = r0 + i;
-      if (r < rows) {
-        const int j = r / p.s2, sp = r - j * p.s2;
-        const float* y = p.y + (size_t)sp * p.y_stride + ((size_t)t * p.k + j) * p.H;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) v[i][q] = (h0 + 64 * q < p.H) ? __ldcg(y + h0 + 64 * q) : 0.0f;
-      }
+      const int r = min(r0 + i, rows - 1);
+      const int j = r / p.s2, sp = r - j * p.s2;
+      v[i] = __ldcg(reinterpret_cast<const float4*>(ybase + (size_t)sp * p.y_stride + (size_t)j * p.H));
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int r = r0 + i;
       if (r < rows) {
         const int j = r / p.s2, sp = r - j * p.s2;
-        const int gj = j % G;
+        yj[0] += v[i].x;
+        yj[1] += v[i].y;
+        yj[2] += v[i].z;
+        yj[3] += v[i].w;
+        if (sp == p.s2 - 1) {
+          const float w = wsm[j];
+          const int gj = j % G;
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          if (g == gj) {
+          for (int g = 0; g < G; ++g) {
+            if (g == gj) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) yj[g][q] += v[i][q];
-            if (sp == p.s2 - 1) {
-              const float w = wsm[j];
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                acc[g][q] = fmaf(w, yj[g][q], acc[g][q]);
-                yj[g][q] = 0.0f;
-              }
+              for (int q = 0; q < 4; ++q) acc[g][q] = fmaf(w, yj[q], acc[g][q]);
             }
           }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) yj[q] = 0.0f;
         }
       }
     }
   }
+  float o[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const int h = h0 + 64 * q;
-    if (h < p.H) {
-      float o;
-      if constexpr (G == 4)
-        o = (acc[0][q] + acc[1][q]) + (acc[2][q] + acc[3][q]);
-      else if constexpr (G == 2)
-        o = acc[0][q] + acc[1][q];
+    if constexpr (G == 4)
+      o[q] = (acc[0][q] + acc[1][q]) + (acc[2][q] + acc[3][q]);
+    else if constexpr (G == 2)
+      o[q] = acc[0][q] + acc[1][q];
+    else
+      o[q] = acc[0][q];
+  }
+  *reinterpret_cast<uint2*>(p.out + (size_t)t * p.H + h4) = make_uint2(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]));
+}
+
+// The combine as a pool of work: a warp whose own role is finished claims the
+// next unit (token t, 128 hidden rows) from a grid-wide counter, waits until
+// all k slots x s2 splits of GEMM2 output for those rows have arrived, and
+// writes their weighted sum (4 hidden rows per lane).
+__device__ __forceinline__ void combine_worker(const FusedDev& p, const unsigned* cnt2, const float* tws, bool ok,
+                                               volatile int* abort_flag, bool stamp_first) {
+  const int lane = threadIdx.x & 31;
+  const int units = ok ? p.T * p.n2 * 2 : 0;
+  const unsigned target = (unsigned)(p.k * p.s2);
+  bool first = stamp_first;
+  for (;;) {
+    unsigned u = 0;
+    if (lane == 0) u = atomicAdd(p.sync + SYNC_CNEXT, 1u);
+    u = __shfl_sync(0xffffffffu, u, 0);
+    if ((int)u >= units) break;
+    const int t = (int)u / (2 * p.n2);
+    const int rem = (int)u - t * 2 * p.n2;
+    const int nn = rem >> 1, half = rem & 1;
+    if (!warp_wait_geq(cnt2 + t * p.n2 + nn, target, abort_flag, p.status)) break;
+    if (first && lane == 0) stamp(p, MOE_TRACE_COMB_FIRST);
+    first = false;
+    const int h4 = nn * 256 + half * 128 + 4 * lane;
+    if (h4 < p.H) {
+      if (p.combine_g == 4)
+        combine_unit<4>(p, t, h4, tws + t * p.k);
+      else if (p.combine_g == 2)
+        combine_unit<2>(p, t, h4, tws + t * p.k);
       else
-        o = acc[0][q];
-      p.out[(size_t)t * p.H + h] = __float2bfloat16_rn(o);
+        combine_unit<1>(p, t, h4, tws + t * p.k);
     }
+    __syncwarp();
   }
 }
 
@@ -339,8 +373,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
   float* tws = reinterpret_cast<float*>(act + E);  // [n] routing weights of every pair
 
   unsigned* arr1 = p.sync + SYNC_NBAR;        // [E * n1] GEMM1 split arrivals
-  unsigned* ready = arr1 + E * p.n1;          // [E] finished GEMM1 tiles
-  unsigned* cnt2 = ready + E;                 // [T * n2] arrived GEMM2 outputs per (token, hidden tile)
+  unsigned* ready1 = arr1 + E * p.n1;         // [E * n1] 1 once a GEMM1 tile's intermediate columns are final
+  unsigned* cnt2 = ready1 + E * p.n1;         // [T * n2] arrived GEMM2 outputs per (token, hidden tile)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -540,35 +574,43 @@ __global__ void __launch_bounds__(kFThreads, 1)
           rows[i] = (r < d.ntok) ? plist[d.lbase + r] / k : 0;  // padding rows read token 0; never stored
         }
       }
-      // GEMM2: weight tiles go out at once; the intermediate only once ready[e] is complete
-      bool x_ready = !d.g2;
-      int npend = 0;
+      // GEMM2: weight tiles go out at once; the intermediate columns of K block kb
+      // (GEMM1 tile kb/2 of the expert) once that tile is final.  Stages still
+      // waiting for their columns queue up in order (lane 0 keeps the queue).
+      int qhead = 0, npend = 0;
+      const unsigned* rdy = ready1 + d.e * p.n1;
       auto load_a = [&](int st, int kb) {
+        if (!ready_stamped) {
+          stamp(p, MOE_TRACE_G2_READY);
+          ready_stamped = true;
+        }
         const uint32_t sx = sbase + st * p.stage_bytes + kWBytes;
         const uint32_t fb = bar_full + 8 * st;
         tma_load_2d(sx, &tmA, kb * 64, d.xrow, fb);
         if (p.act_split) tma_load_2d(sx + x1_bytes, &tmA, kb * 64, d.xrow + p.cap, fb);
       };
-      auto flush = [&]() {
-        if (!ready_stamped) {
-          stamp(p, MOE_TRACE_G2_READY);
-          ready_stamped = true;
+      auto flush_ready = [&]() {  // lane 0: the queued loads whose columns are final, in order
+        bool fenced = false;
+        while (npend > 0 && ld_acquire_u32(rdy + (pend_kb[qhead] >> 1)) != 0u) {
+          if (!fenced) {
+            fence_proxy_async_global();
+            fenced = true;
+          }
+          load_a(pend_stage[qhead], pend_kb[qhead]);
+          qhead = (qhead + 1) % kFMaxStages;
+          --npend;
         }
-        fence_proxy_async_global();
-        for (int i = 0; i < npend; ++i) load_a(pend_stage[i], pend_kb[i]);
-        npend = 0;
-        x_ready = true;
       };
       for (int kb = d.kb0; kb < d.kb1; ++kb) {
-        if (!x_ready && npend == p.stages) {
-          // every stage holds weights waiting for the intermediate: it is needed now
-          if (!warp_wait_geq(ready + d.e, (unsigned)p.n1, abort_flag, p.status)) {
+        if (npend == p.stages) {
+          // every stage holds weights waiting for intermediate columns: wait for the oldest
+          const int head_kb = __shfl_sync(0xffffffffu, pend_kb[qhead], 0);
+          if (!warp_wait_geq(rdy + (head_kb >> 1), 1u, abort_flag, p.status)) {
             okp = false;
             break;
           }
-          if (lane == 0) flush();
-          x_ready = true;
-          npend = 0;
+          if (lane == 0) flush_ready();
+          npend = __shfl_sync(0xffffffffu, npend, 0);
         }
         if (!mbar_wait_all(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p.status)) {
           okp = false;
@@ -581,19 +623,20 @@ __global__ void __launch_bounds__(kFThreads, 1)
           tma_load_2d(sws, tmw, kb * 64, d.wr0, fb);
           tma_load_2d(sws + kWBytes / 2, tmw, kb * 64, d.wr0 + d.pair_off, fb);
           if (d.g2) {
-            if (!x_ready && ld_acquire_u32(ready + d.e) >= (unsigned)p.n1) flush();
-            if (x_ready) {
+            flush_ready();
+            if (npend == 0 && ld_acquire_u32(rdy + (kb >> 1)) != 0u) {
+              fence_proxy_async_global();
               load_a(stage, kb);
             } else {
-              pend_stage[npend] = stage;
-              pend_kb[npend] = kb;
+              const int slot = (qhead + npend) % kFMaxStages;
+              pend_stage[slot] = stage;
+              pend_kb[slot] = kb;
               ++npend;
             }
           } else if (!p.gather) {
             tma_load_2d(sws + kWBytes, &tmX, kb * 64, d.xrow, fb);
           }
         }
-        x_ready = __shfl_sync(0xffffffffu, x_ready, 0);
         npend = __shfl_sync(0xffffffffu, npend, 0);
         if (!d.g2 && p.gather && lane < groups)
           tma_gather4(sbase + stage * p.stage_bytes + kWBytes + (uint32_t)lane * 512u, &tmX, kb * 64, rows[0],
@@ -605,14 +648,14 @@ __global__ void __launch_bounds__(kFThreads, 1)
           phase ^= 1u;
         }
       }
-      if (okp && npend > 0) {
-        if (warp_wait_geq(ready + d.e, (unsigned)p.n1, abort_flag, p.status)) {
-          if (lane == 0) flush();
-          x_ready = true;
-          npend = 0;
-        } else {
+      while (okp && npend > 0) {
+        const int head_kb = __shfl_sync(0xffffffffu, pend_kb[qhead], 0);
+        if (!warp_wait_geq(rdy + (head_kb >> 1), 1u, abort_flag, p.status)) {
           okp = false;
+          break;
         }
+        if (lane == 0) flush_ready();
+        npend = __shfl_sync(0xffffffffu, npend, 0);
       }
       __syncwarp();
     }
@@ -628,6 +671,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
         mbar_wait_drain(bar_full + 8 * (i % p.stages), (i / p.stages) & 1u, 100000000ull);
     }
     __syncwarp();
+    combine_worker(p, cnt2, tws, ok, abort_flag, false);
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     // the whole warp runs the loop and waits together; lane 0 issues the MMAs and their commits
@@ -688,6 +732,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
       mbar_wait_drain(bar_drain, 0, 100000000ull);
     }
     __syncwarp();
+    combine_worker(p, cnt2, tws, ok, abort_flag, false);
   } else if (warp < 6) {
     // ---------------- epilogue (warps 2..5) ----------------
     const int q = warp & 3;          // tensor-memory lane quadrant of this warp
@@ -778,13 +823,11 @@ __global__ void __launch_bounds__(kFThreads, 1)
               float pg[8], pu[8];
 #pragma unroll
               for (int q2 = 0; q2 < 8; ++q2) {
-                const int r = r0 + q2;
-                if (r < rows) {
-                  const int c = r / p.s1, sp = r - c * p.s1;
-                  const float* row = p.p1 + (size_t)sp * p.p1_stride + (size_t)plist[d.lbase + c] * 2 * I;
-                  pg[q2] = __ldcg(row + i);
-                  pu[q2] = __ldcg(row + I + i);
-                }
+                const int r = min(r0 + q2, rows - 1);  // (the tail of a batch re-reads the last row)
+                const int c = r / p.s1, sp = r - c * p.s1;
+                const float* row = p.p1 + (size_t)sp * p.p1_stride + (size_t)plist[d.lbase + c] * 2 * I;
+                pg[q2] = __ldcg(row + i);
+                pu[q2] = __ldcg(row + I + i);
               }
 #pragma unroll
               for (int q2 = 0; q2 < 8; ++q2) {
@@ -812,7 +855,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
           // the intermediate columns of this tile are complete: count the tile for GEMM2 (read by TMA)
           fence_proxy_async_global();
           named_bar_sync(1, 128);
-          if (lrow == 0) red_release_add(ready + d.e, 1u);
+          if (lrow == 0) red_release_add(ready1 + d.e * p.n1 + d.n, 1u);
         }
         if (lrow == 0) stamp(p, MOE_TRACE_G1_DONE);
       } else {
@@ -822,27 +865,11 @@ __global__ void __launch_bounds__(kFThreads, 1)
       }
     }
     if (lrow == 0) stamp(p, MOE_TRACE_EPI_DONE);
+    combine_worker(p, cnt2, tws, ok, abort_flag, false);
   } else {
-    // ---------------- combine (warps 6, 7) ----------------
-    // unit (token t, 256 hidden rows n): once all k slots x s2 splits of its
-    // GEMM2 outputs have arrived, the weighted sum of those rows
-    const int ct = threadIdx.x - 192;
-    const int units = ok ? T * p.n2 : 0;
-    const unsigned target = (unsigned)(k * p.s2);
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
-      const int t = u / p.n2, nn = u - t * p.n2;
-      const bool good = warp_wait_geq(cnt2 + u, target, abort_flag, p.status);
-      if (ct == 0 && u == (int)blockIdx.x) stamp(p, MOE_TRACE_COMB_FIRST);
-      if (f_comb_any(!good)) break;
-      const int h0 = nn * 256 + ct;
-      if (p.combine_g == 4)
-        combine_unit<4>(p, t, h0, tws + t * k);
-      else if (p.combine_g == 2)
-        combine_unit<2>(p, t, h0, tws + t * k);
-      else
-        combine_unit<1>(p, t, h0, tws + t * k);
-    }
-    if (ct == 0) stamp(p, MOE_TRACE_COMB_DONE);
+    // ---------------- combine (warps 6, 7; every other warp once its role is done) ----------------
+    combine_worker(p, cnt2, tws, ok, abort_flag, warp == 6);
+    if (lane == 0 && warp == 6) stamp(p, MOE_TRACE_COMB_DONE);
   }
 
   // Each warp reports the end of its role on an mbarrier; warp 1 frees tensor
@@ -875,7 +902,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
 namespace moe {
 
 size_t fused_sync_bytes(int T, int H, int I, int E) {
-  const size_t words = SYNC_NBAR + (size_t)E * (I / 128) + E + (size_t)T * ((H + 255) / 256);
+  const size_t words = SYNC_NBAR + 2 * (size_t)E * (I / 128) + (size_t)T * ((H + 255) / 256);
   return 256 + (words * 4 + 255) / 256 * 256;  // launch tag in the first 256 bytes, then the counters
 }
 
@@ -933,7 +960,7 @@ cudaError_t launch_decode_fused(const FusedArgs& a, cudaStream_t s) {
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.go = static_cast<unsigned long long*>(a.sync);
   p.sync = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(a.sync) + 256);
-  p.nsync = SYNC_NBAR + a.E * p.n1 + a.E + a.T * p.n2;
+  p.nsync = SYNC_NBAR + 2 * a.E * p.n1 + a.T * p.n2;
   p.status = a.status;
   p.trace = static_cast<unsigned long long*>(a.trace);
 

@@ -54,15 +54,15 @@ __device__ __forceinline__ void router_block(const TIn* __restrict__ X, const TI
   for (int h = (warp * 32 + lane) * V; h < H; h += kRouterWarps * 32 * V) {
     float wv[V];
     router_load16(w + h, wv);
+    // every token row is loaded (rows past the batch re-read its last row), so
+    // the loads go out together; only the batch's tokens are stored
+    float xv[TT][V];
 #pragma unroll
-    for (int b = 0; b < TT; ++b) {
-      if (b < nt) {
-        float xv[V];
-        router_load16(X + (size_t)(t0 + b) * H + h, xv);
+    for (int b = 0; b < TT; ++b) router_load16(X + (size_t)(t0 + min(b, nt - 1)) * H + h, xv[b]);
 #pragma unroll
-        for (int q = 0; q < V; ++q) acc[b] = fmaf(wv[q], xv[q], acc[b]);
-      }
-    }
+    for (int b = 0; b < TT; ++b)
+#pragma unroll
+      for (int q = 0; q < V; ++q) acc[b] = fmaf(wv[q], xv[b][q], acc[b]);
   }
 #pragma unroll
   for (int b = 0; b < TT; ++b) {
@@ -109,7 +109,10 @@ __device__ __forceinline__ void topk_warp(const float* __restrict__ l, int E, in
   // the scan order and arithmetic are those of a plain loop over e = lane, lane+32, ...
   float cache[kTopkCache];
 #pragma unroll
-  for (int q = 0; q < kTopkCache; ++q) cache[q] = (lane + 32 * q < E) ? topk_ld<CG>(l + lane + 32 * q) : -INFINITY;
+  for (int q = 0; q < kTopkCache; ++q) cache[q] = topk_ld<CG>(l + min(lane + 32 * q, E - 1));  // loads go out together
+#pragma unroll
+  for (int q = 0; q < kTopkCache; ++q)
+    if (lane + 32 * q >= E) cache[q] = -INFINITY;
   uint32_t taken = 0;  // bit q: expert lane + 32*q taken
   float my_v = 0.0f;
   int my_i = 0;

@@ -166,15 +166,38 @@ def test_single_launch_refuses_unsupported_shapes(moe):
     assert e.value.code == moe.MOE_ERR_UNSUPPORTED
 
 
-@pytest.mark.parametrize("name,M", [("mixtral_decode", 1), ("mixtral_decode", 64), ("fine_decode", 1),
-                                    ("fine_decode", 8), ("fine_decode", 64)])
-def test_single_launch_full_size_bit_identical(moe, name, M):
-    """At the workloads' full sizes the single launch reproduces the multi-kernel output bit for bit
-    (the multi-kernel path is checked against the oracle at these sizes in test_gpu_configs)."""
+@pytest.mark.parametrize("name,M", [("mixtral_decode", 1), ("mixtral_decode", 16), ("mixtral_decode", 64),
+                                    ("fine_decode", 1), ("fine_decode", 8), ("fine_decode", 64)])
+def test_single_launch_full_size(moe, name, M):
+    """The workloads at full size: every output token against the oracle, and bit for bit against the
+    multi-kernel sequence whenever both plans use the same K splits (the single launch runs GEMM1
+    unsplit above 8 tokens)."""
     sp = spec(name, T=M)
     L = make_layer(sp, device="cuda")
+    make_tie_free(L)
     f = moe.moe_forward(L["X"], L["Wr"], L["W13"], L["W2"], sp.k, sp.renorm, options=FUSED)
     m = moe.moe_forward(L["X"], L["Wr"], L["W13"], L["W2"], sp.k, sp.renorm, options=MULTI)
+    torch.cuda.synchronize()
+    assert moe.moe_get_status() == 0
+    pf = moe.moe_plan_info(M, sp.H, sp.I, sp.E, sp.k, moe.MOE_BF16, moe.MOE_BF16, FUSED)
+    pm = moe.moe_plan_info(M, sp.H, sp.I, sp.E, sp.k, moe.MOE_BF16, moe.MOE_BF16, MULTI)
+    if (pf["splits_gemm1"], pf["splits_gemm2"]) == (pm["splits_gemm1"], pm["splits_gemm2"]):
+        assert torch.equal(f, m)
+    cpu = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in L.items()}
+    ref = oracle.moe_forward(cpu["X"], cpu["Wr"], cpu["W13"], cpu["W2"], sp.k, sp.renorm)["out"]
+    assert rel_err(f.float().cpu().numpy(), ref, f"single launch {name} M={M}") <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("M", [16, 64])
+def test_single_launch_unsplit_gemm1_matches_forced_plan(moe, M):
+    """Above 8 tokens the single launch runs GEMM1 unsplit: the same as both paths forced to one split."""
+    sp = spec("fine_decode", T=M, H=1024, I=512, E=64)
+    L = make_layer(sp, device="cuda")
+    pf = moe.moe_plan_info(M, sp.H, sp.I, sp.E, sp.k, moe.MOE_BF16, moe.MOE_BF16, FUSED)
+    assert pf["splits_gemm1"] == 1
+    opts = {"split_k": 1}
+    f = moe.moe_forward(L["X"], L["Wr"], L["W13"], L["W2"], sp.k, sp.renorm, options={**FUSED, **opts})
+    m = moe.moe_forward(L["X"], L["Wr"], L["W13"], L["W2"], sp.k, sp.renorm, options={**MULTI, **opts})
     torch.cuda.synchronize()
     assert moe.moe_get_status() == 0
     assert torch.equal(f, m)
