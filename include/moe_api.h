@@ -239,6 +239,31 @@ MOE_API int moe_forward(const void* hidden, const void* router_w, const void* w1
                 const float* w2_scale, void* out, void* workspace, size_t workspace_bytes, const moe_options* opts,
                 moe_stream_t stream);
 
+/* Inverse rotary position embedding fused with per-head FP8 quantisation
+ *   ("Mixture-of-Experts kernel engineering on Amazon SageMaker AI", section on
+ *    the Triton JIT: the serving stack's _fused_inv_rope_fp8_quant_per_head kernel,
+ *    rotary embedding + FP8 quantisation fused; here every shape is a runtime argument).
+ * For token t, head h, x = x[t][h][0:head_dim] (bf16), R = rot_dim, half = R/2 and
+ * (c_i, s_i) = (cos_sin[positions[t]][i], cos_sin[positions[t]][half + i]):
+ *   y_i = x_i c_i + x_{half+i} s_i,  y_{half+i} = x_{half+i} c_i - x_i s_i   (i < half: the
+ *   rotation by minus the position's angle, rotate-half pairing), y_j = x_j for j >= R;
+ *   scale_out[t][h] = max_j |y_j| / 448 (1.0 when that is 0), fp32;
+ *   q_out[t][h][j] = e4m3(y_j * r), r = 1 / scale_out[t][h] once per vector (round to nearest
+ *   even, saturating to +-448).
+ * Every product, sum and the reciprocal is one fp32 rounding (no fused multiply-add).
+ * Arguments:
+ *   x          [T][heads][head_dim] bf16, 4-byte aligned
+ *   positions  [T] int32, each in [0, max_pos); others are clamped and flagged
+ *              MOE_ERR_DEVICE_INDEX (moe_get_status)
+ *   cos_sin    [max_pos][rot_dim] fp32, 16-byte aligned: cos of the rot_dim/2 angles, then their sin
+ *              (may be NULL when rot_dim == 0)
+ *   q_out      [T][heads][head_dim] e4m3 codes;  scale_out [T][heads] fp32
+ * Limits: head_dim even, rot_dim % 4 == 0, rot_dim <= min(head_dim, 1024),
+ *   head_dim - rot_dim <= 512.  T = 0 is a successful no-op. */
+MOE_API int moe_inv_rope_fp8_quant(const void* x, int T, int heads, int head_dim, int rot_dim,
+                                   const int32_t* positions, const float* cos_sin, int max_pos, uint8_t* q_out,
+                                   float* scale_out, moe_stream_t stream);
+
 /* Allocation-free form of moe_forward (the pages have no counterpart; it is an
  * interface convenience of this library).
  *

@@ -31,7 +31,7 @@ TRACE_WORDS = len(TRACE_EVENTS)
 # every entry point include/moe_api.h declares
 EXPORTS = ("moe_strerror", "moe_workspace_size", "moe_plan_info", "moe_align_capacity", "moe_route",
            "moe_topk_from_logits", "moe_align", "moe_forward", "moe_forward_noalloc", "moe_get_status",
-           "moe_version")
+           "moe_version", "moe_inv_rope_fp8_quant")
 NOALLOC_MAX_WORKSPACE = 32 << 20
 
 
@@ -81,6 +81,8 @@ def _load():
     lib.moe_forward_noalloc.argtypes = [P, P, P, P, i, i, i, i, i, i, i, i, P, P, P, P, P]
     lib.moe_get_status.restype = i
     lib.moe_get_status.argtypes = [P]
+    lib.moe_inv_rope_fp8_quant.restype = i
+    lib.moe_inv_rope_fp8_quant.argtypes = [P, i, i, i, i, P, P, i, P, P, P]
     return lib
 
 
@@ -242,3 +244,18 @@ def moe_forward_noalloc(hidden: torch.Tensor, router_w: torch.Tensor, w13: torch
 
 def moe_get_status(stream=None) -> int:
     return int(_lib.moe_get_status(_stream(stream)))
+
+
+def moe_inv_rope_fp8_quant(x: torch.Tensor, positions: torch.Tensor, cos_sin: torch.Tensor, rot_dim: int,
+                           q_out=None, scale_out=None, stream=None):
+    """Inverse rotary embedding + per-head e4m3 quantisation of x [T, heads, head_dim] (bf16):
+    (codes uint8 [T, heads, head_dim], scales float32 [T, heads])."""
+    T, heads, D = x.shape
+    assert x.dtype == torch.bfloat16 and x.is_contiguous()
+    dev = x.device
+    q_out = torch.empty(T, heads, D, dtype=torch.uint8, device=dev) if q_out is None else q_out
+    scale_out = torch.empty(T, heads, dtype=torch.float32, device=dev) if scale_out is None else scale_out
+    _check(_lib.moe_inv_rope_fp8_quant(_p(x), T, heads, D, int(rot_dim), _p(positions), _p(cos_sin),
+                                       cos_sin.shape[0], _p(q_out), _p(scale_out), _stream(stream)),
+           "moe_inv_rope_fp8_quant")
+    return q_out, scale_out

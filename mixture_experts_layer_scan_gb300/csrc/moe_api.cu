@@ -608,6 +608,24 @@ int moe_forward(const void* hidden, const void* router_w, const void* w13, const
   return MOE_OK;
 }
 
+int moe_inv_rope_fp8_quant(const void* x, int T, int heads, int head_dim, int rot_dim, const int32_t* positions,
+                           const float* cos_sin, int max_pos, uint8_t* q_out, float* scale_out, moe_stream_t stream) {
+  if (T < 0 || heads < 1 || head_dim < 2 || head_dim % 2 || rot_dim < 0 || rot_dim % 4 || rot_dim > head_dim ||
+      rot_dim > 1024 || head_dim - rot_dim > 512 || max_pos < 1)
+    return MOE_ERR_ARG;
+  if ((long long)T * heads * head_dim >= (1ll << 40)) return MOE_ERR_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !positions || (rot_dim > 0 && !cos_sin) || !q_out || !scale_out) return MOE_ERR_ARG;
+  if (misaligned(x, 4) || misaligned(positions, 4) || (cos_sin && misaligned(cos_sin, 16)) || misaligned(q_out, 2) ||
+      misaligned(scale_out, 4))
+    return MOE_ERR_ALIGNMENT;
+  int* st = status_word();
+  const int sms = num_sms();
+  if (!st) return MOE_ERR_CUDA;
+  return cuda_rc(launch_inv_rope_fp8(x, T, heads, head_dim, rot_dim, positions, cos_sin, max_pos, q_out, scale_out,
+                                     st, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int moe_get_status(moe_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ERR_CUDA;
   int* st = status_word();

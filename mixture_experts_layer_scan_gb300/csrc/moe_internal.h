@@ -117,6 +117,11 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s);
 bool make_tensor_map_2d(CUtensorMap* m, const void* base, int elem_bytes, uint64_t K, uint64_t rows,
                         uint32_t box_rows);
 
+// ---- inverse rotary embedding + per-head FP8 quantisation ----------------------------
+cudaError_t launch_inv_rope_fp8(const void* X, int T, int heads, int D, int R, const int32_t* pos,
+                                const float* cos_sin, int max_pos, uint8_t* Q, float* scale, int* status,
+                                int num_sms, cudaStream_t s);
+
 // ---- single-launch decode layer (bf16, swap-AB) ----------------------------------
 struct FusedArgs {
   int T, H, I, E, k, renorm;

@@ -186,3 +186,52 @@ def to_device(layer: dict, device) -> dict:
         if out.get(key) is not None:
             out[key] = out[key].to(device)
     return out
+
+
+# -- inverse rotary embedding + per-head FP8 quantisation inputs -------------------
+
+@dataclass
+class RopeSpec:
+    name: str
+    T: int
+    heads: int
+    head_dim: int
+    rot_dim: int
+    max_pos: int = 8192
+    theta: float = 10000.0
+    seed: int = 4321
+
+
+def rope_spec(name: str, **over) -> RopeSpec:
+    """Head layouts of attention blocks around MoE layers: a Llama-style query (32 heads of 128,
+    fully rotated) and an MLA-style query (128 heads of 576: 64 rotated, 512 not)."""
+    base = {
+        "gqa_prefill": dict(T=8192, heads=32, head_dim=128, rot_dim=128),
+        "gqa_decode": dict(T=64, heads=32, head_dim=128, rot_dim=128),
+        "mla_decode": dict(T=64, heads=128, head_dim=576, rot_dim=64),
+    }[name]
+    base = dict(base)
+    base.update(over)
+    return RopeSpec(name=name, **base)
+
+
+def make_rope_inputs(rs: RopeSpec, device="cpu") -> dict:
+    """x [T, heads, head_dim] bf16 ~ N(0,1) with a few large outliers per vector, positions [T] int32
+    uniform in [0, max_pos), and the cos/sin table [max_pos, rot_dim] fp32 of the standard rotary
+    frequencies theta^(-2i/rot_dim) (the table a serving stack precomputes: an input here)."""
+    g = _gen(rs.seed, "cpu")
+    x = torch.randn(rs.T, rs.heads, rs.head_dim, generator=g, dtype=torch.float32)
+    spikes = torch.rand(rs.T, rs.heads, rs.head_dim, generator=g) < 0.01
+    x = torch.where(spikes, x * 8.0, x)
+    pos = torch.randint(0, rs.max_pos, (rs.T,), generator=g, dtype=torch.int32)
+    half = rs.rot_dim // 2
+    if half > 0:
+        inv = rs.theta ** (-torch.arange(half, dtype=torch.float64) * 2.0 / rs.rot_dim)
+        ang = torch.arange(rs.max_pos, dtype=torch.float64)[:, None] * inv[None, :]
+        cos_sin = torch.cat([torch.cos(ang), torch.sin(ang)], dim=1).to(torch.float32)
+    else:
+        cos_sin = torch.zeros(rs.max_pos, 0, dtype=torch.float32)
+    d = {"spec": rs, "x": x.to(torch.bfloat16), "pos": pos, "cos_sin": cos_sin.contiguous()}
+    if device != "cpu":
+        d = {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+    return d

@@ -30,7 +30,8 @@ def build(force: bool = False) -> str:
     """Compile the oracle with gcc into oracle/libmoe_oracle.so (plain C, OpenMP)."""
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-o", tmp, _SRC, "-lm"])
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-fopenmp", "-o", tmp,
+                               _SRC, "-lm"])
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -65,6 +66,8 @@ def _load():
         lib.oracle_align.argtypes = [P, i, i, i, i, P, P, P, P]
         lib.oracle_moe_forward.restype = i
         lib.oracle_moe_forward.argtypes = [P, P, P, P, i, i, i, i, i, i, i, i, P, P, P, i, P, P, P, P]
+        lib.oracle_inv_rope_fp8.restype = i
+        lib.oracle_inv_rope_fp8.argtypes = [P, i, i, i, i, P, P, i, P, P, P]
         lib.oracle_set_threads.restype = None
         lib.oracle_set_threads.argtypes = [i]
         lib.oracle_get_threads.restype = i
@@ -212,3 +215,21 @@ def moe_forward(X, Wr, W13, W2, topk_k: int, renorm: bool, w13_scale=None, w2_sc
     if rc != 0:
         raise ValueError(f"oracle_moe_forward failed ({rc})")
     return {"out": out, "ids": ids, "w": w, "act_scales": scales}
+
+
+def inv_rope_fp8_quant(X, positions, cos_sin, rot_dim: int, return_rotated: bool = False):
+    """(codes uint8 [T,heads,D], scales float32 [T,heads][, rotated float32 [T,heads,D]]) of the inverse
+    rotary embedding + per-head e4m3 quantisation; X is bf16 [T,heads,D] (bit patterns or a torch tensor)."""
+    x = np.ascontiguousarray(_np(X), dtype=np.uint16)
+    T, heads, D = x.shape
+    pos = np.ascontiguousarray(_np(positions), dtype=np.int32)
+    cs = np.ascontiguousarray(_np(cos_sin), dtype=np.float32)
+    max_pos = cs.shape[0]
+    q = np.empty((T, heads, D), dtype=np.uint8)
+    sc = np.empty((T, heads), dtype=np.float32)
+    y = np.empty((T, heads, D), dtype=np.float32) if return_rotated else None
+    rc = _load().oracle_inv_rope_fp8(_ptr(x), T, heads, D, int(rot_dim), _ptr(pos), _ptr(cs), max_pos,
+                                     None if y is None else _ptr(y), _ptr(q), _ptr(sc))
+    if rc != 0:
+        raise ValueError(f"oracle_inv_rope_fp8 failed ({rc})")
+    return (q, sc, y) if return_rotated else (q, sc)

@@ -382,3 +382,66 @@ int oracle_get_threads(void) {
   return 1;
 #endif
 }
+
+/*
+ * Inverse rotary position embedding with per-head FP8 quantisation
+ * ("Mixture-of-Experts kernel engineering on Amazon SageMaker AI", section on
+ * the Triton JIT: the serving stack's _fused_inv_rope_fp8_quant_per_head kernel
+ * fuses rotary embedding with FP8 quantisation; the pages give no formula).
+ *
+ * Readings: the rotate-half pairing (element i with element i + R/2) over the
+ * first R = rot_dim elements of each head vector; "inverse" is the rotation by
+ * minus the position's angle; the elements from R on pass through; "per head"
+ * is one dynamic scale per (token, head) vector, amax / 448 (1 when amax is 0);
+ * codes of y * (1 / scale), the reciprocal taken once per vector (the practice
+ * of serving stacks' FP8 quantisation kernels), by round-to-nearest-even with
+ * saturation.  The cos/sin of each
+ * position's R/2 angles are an input table (as a serving stack passes them).
+ *
+ * Precision: the kernel takes the code decisions in fp32, so this function
+ * does the same arithmetic in fp32, one rounding per product, sum and
+ * division, in this order (the build disables floating-point contraction).
+ *
+ *   x:  [T][heads][D] bf16 bit patterns     pos: [T]     cos_sin: [max_pos][R]
+ *   y:  [T][heads][D] fp32 rotated values (nullable)
+ *   q:  [T][heads][D] e4m3 codes            scale: [T][heads]
+ * Returns -1 when a position is outside [0, max_pos).
+ */
+int oracle_inv_rope_fp8(const uint16_t* x, int T, int heads, int D, int R, const int32_t* pos, const float* cos_sin,
+                        int max_pos, float* y, uint8_t* q, float* scale) {
+  const int half = R / 2;
+  for (int t = 0; t < T; ++t) {
+    if (pos[t] < 0 || pos[t] >= max_pos) return -1;
+    const float* c = cos_sin + (size_t)pos[t] * R;
+    const float* s = c + half;
+    for (int h = 0; h < heads; ++h) {
+      const size_t base = ((size_t)t * heads + h) * D;
+      float* v = (float*)malloc(sizeof(float) * (size_t)D);
+      if (!v) return -2;
+      for (int i = 0; i < half; ++i) {
+        const float x1 = (float)oracle_bf16_to_f64(x[base + i]);
+        const float x2 = (float)oracle_bf16_to_f64(x[base + half + i]);
+        const float p11 = x1 * c[i], p22 = x2 * s[i];
+        const float p21 = x2 * c[i], p12 = x1 * s[i];
+        v[i] = p11 + p22;
+        v[half + i] = p21 - p12;
+      }
+      for (int j = R; j < D; ++j) v[j] = (float)oracle_bf16_to_f64(x[base + j]);
+      float amax = 0.0f;
+      for (int j = 0; j < D; ++j) {
+        const float a = fabsf(v[j]);
+        if (a > amax) amax = a;
+      }
+      const float sc = oracle_e4m3_scale(amax);
+      const float r = 1.0f / sc;
+      scale[(size_t)t * heads + h] = sc;
+      for (int j = 0; j < D; ++j) {
+        const float z = v[j] * r;
+        q[base + j] = oracle_f32_to_e4m3_satfinite(z);
+        if (y) y[base + j] = v[j];
+      }
+      free(v);
+    }
+  }
+  return 0;
+}
