@@ -30,7 +30,7 @@ sys.path.insert(0, ROOT)
 
 import torch  # noqa: E402
 
-from moe_synth import make_layer, spec  # noqa: E402
+from moe_synth import make_layer, resample_tokens, spec  # noqa: E402
 
 L2_BYTES = 129 * 1024 * 1024
 METRIC = "MoE-layer tokens/s; decode weight-stream HBM GB/s, prefill TFLOP/s vs peak"
@@ -406,6 +406,68 @@ def run_rope(dev, pk, steps=200):
     return out
 
 
+def run_offload(dev, steps=48, warm=8, slots=48, M=8):
+    """The expert cache on the fine-grained decode layer (128 experts of 9.4 MB, all in pinned host
+    memory; `slots` of them in HBM): a sequence of Zipf-routed batches, each call timed end to end
+    (routing, the host read-back and slot plan, the copies of missing experts, the expert steps),
+    against the same batches with every expert resident."""
+    import time
+
+    import mixture_experts_layer_scan_gb300 as moe
+
+    sp = spec("fine_decode", T=M)
+    L = make_layer(sp, device="cpu")
+    w13h, w2h = L["W13"].pin_memory(), L["W2"].pin_memory()
+    W13, W2, Wr = L["W13"].to(dev), L["W2"].to(dev), L["Wr"].to(dev)
+    batches = []
+    for b in range(warm + steps):
+        resample_tokens(L, torch.arange(M), 7000 + b)
+        batches.append(L["X"].to(dev))
+    cache = moe.ExpertCache(w13h, w2h, n_slots=slots, max_tokens=M, topk=sp.k)
+    ws = torch.empty(cache.workspace_size(M), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(batches[0])
+    for X in batches[:warm]:
+        cache.forward(X, Wr, sp.renorm, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    st0 = cache.stats()
+    t0 = time.perf_counter()
+    for X in batches[warm:]:
+        cache.forward(X, Wr, sp.renorm, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    cached_ms = (time.perf_counter() - t0) / steps * 1e3
+    st1 = cache.stats()
+    assert moe.moe_get_status() == 0
+    wsr = torch.empty(moe.moe_workspace_size(M, sp.H, sp.I, sp.E, sp.k, moe.MOE_BF16, moe.MOE_BF16), dtype=torch.uint8,
+                      device=dev)
+    for X in batches[:warm]:
+        moe.moe_forward(X, Wr, W13, W2, sp.k, sp.renorm, out=out, workspace=wsr)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for X in batches[warm:]:
+        moe.moe_forward(X, Wr, W13, W2, sp.k, sp.renorm, out=out, workspace=wsr)
+    torch.cuda.synchronize()
+    resident_ms = (time.perf_counter() - t0) / steps * 1e3
+    # host -> device copy bandwidth of one expert's weights (pinned source)
+    dst = torch.empty(W13[0].numel() + W2[0].numel(), dtype=torch.bfloat16, device=dev)
+    src = torch.cat([w13h[0].flatten(), w2h[0].flatten()]).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(20):
+        dst.copy_(src, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    h2d_gbs = 20 * src.numel() * 2 / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    d = {k: st1[k] - st0[k] for k in st1}
+    cache.close()
+    distinct = d["hits"] + d["misses"]
+    return {"workload": f"fine_decode_M{M}", "experts": sp.E, "expert_mb": round((3 * sp.H * sp.I * 2) / 2 ** 20, 2),
+            "slots": slots, "steps": steps, "cached_ms_per_call": cached_ms, "resident_ms_per_call": resident_ms,
+            "cached_tokens_per_s": M / (cached_ms * 1e-3), "resident_tokens_per_s": M / (resident_ms * 1e-3),
+            "hit_rate": d["hits"] / max(1, distinct), "misses_per_call": d["misses"] / steps,
+            "h2d_bytes_per_call": d["bytes_h2d"] / steps, "h2d_gbs_pinned_copy": h2d_gbs,
+            "timing": "host wall clock per call, eager, both paths (the cached call synchronises on its routing)"}
+
+
 def cpu_baseline(L, sp, budget_s=20.0):
     """The CPU oracle, as it stands, on a bounded token sample of the workload, on all host cores."""
     import oracle
@@ -537,6 +599,7 @@ def main():
         line["sweep"] = sweep
     if not args.no_sweep:
         line["inv_rope_fp8"] = run_rope(dev, pk)
+        line["expert_offload"] = run_offload(dev)
     print(json.dumps(line, default=float))
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -264,6 +264,63 @@ MOE_API int moe_inv_rope_fp8_quant(const void* x, int T, int heads, int head_dim
                                    const int32_t* positions, const float* cos_sin, int max_pos, uint8_t* q_out,
                                    float* scale_out, moe_stream_t stream);
 
+/* Steps 3-7 of the layer on a routing the caller provides (its own router, or
+ * expert ids remapped to the slots of an expert cache): the same permutation,
+ * expert GEMMs and combine as moe_forward, which it matches bit for bit given
+ * moe_forward's routing.
+ *   topk_w   [T][topk] fp32 routing weights (used as given, no renormalisation)
+ *   topk_ids [T][topk] int32 expert ids in [0, E); ids outside are dropped and flagged
+ *            MOE_ERR_DEVICE_INDEX
+ * Other arguments, the workspace (moe_workspace_size with the same E) and the options
+ * as moe_forward; the multi-kernel sequence always (single_launch = 1 is refused). */
+MOE_API int moe_forward_routed(const void* hidden, const float* topk_w, const int32_t* topk_ids, const void* w13,
+                               const void* w2, int T, int H, int I, int E, int topk, moe_dtype act_dtype,
+                               moe_dtype w_dtype, const float* w13_scale, const float* w2_scale, void* out,
+                               void* workspace, size_t workspace_bytes, const moe_options* opts, moe_stream_t stream);
+
+/* Expert cache ("FusedMoE vs MegaMoE", section 4: MegaMoE keeps expert weights
+ * in host memory and stages the experts a batch needs into GPU memory, loading
+ * synchronously on a miss).  The cache owns a pool of n_slots expert slots in
+ * device memory; the full weights stay in host memory (on a GB300 the Grace
+ * CPU's, over NVLink-C2C).  Each moe_forward_cached call routes the batch on
+ * the GPU, reads the expert ids back (one host synchronisation per call), keeps
+ * the experts already resident, copies the missing ones into free slots or the
+ * slots of the least recently used experts this call does not need (one
+ * cudaMemcpyAsync per weight matrix on the cache's copy stream), and runs the
+ * expert part of the layer over the slots (moe_forward_routed).  Results equal
+ * moe_forward's on the same weights.  Prediction of future experts is not built. */
+typedef struct moe_expert_cache moe_expert_cache;
+typedef struct {
+  unsigned long long calls, hits, misses, evictions, bytes_h2d;
+} moe_cache_stats_t;
+
+/* host_w13 [E][2I][H], host_w2 [E][H][I] in host memory (registered as page-locked
+ * by the cache unless already pinned, unregistered at destroy); w_dtype MOE_BF16 or
+ * MOE_E4M3 (then host_w13_scale / host_w2_scale [E] fp32, read at each miss).
+ * topk <= n_slots <= E device slots; calls take T <= max_tokens tokens and need at most
+ * n_slots distinct experts (else MOE_ERR_UNSUPPORTED).  H % 128 == 0, I % 128 == 0.
+ * The cache allocates its device and pinned buffers here (cudaMalloc), none per call. */
+MOE_API int moe_cache_create(const void* host_w13, const void* host_w2, const float* host_w13_scale,
+                             const float* host_w2_scale, int E, int H, int I, moe_dtype w_dtype, int n_slots,
+                             int max_tokens, int topk, moe_expert_cache** cache);
+MOE_API int moe_cache_destroy(moe_expert_cache* cache);
+/* Workspace bytes of a moe_forward_cached call with T tokens. */
+MOE_API int moe_cache_workspace_size(const moe_expert_cache* cache, int T, moe_dtype act_dtype,
+                                     const moe_options* opts, size_t* bytes);
+/* The layer on hidden [T][H] with router_w [E][H] (act_dtype) into out [T][H]; the
+ * call blocks until the batch's routing is known.  Calls on one cache are serialised. */
+MOE_API int moe_forward_cached(moe_expert_cache* cache, const void* hidden, const void* router_w, int T, int renorm,
+                               moe_dtype act_dtype, void* out, void* workspace, size_t workspace_bytes,
+                               const moe_options* opts, moe_stream_t stream);
+MOE_API int moe_cache_stats(const moe_expert_cache* cache, moe_cache_stats_t* stats);
+/* The cache's slot policy alone, host only (no device work): over n_calls calls of
+ * `pairs` expert ids each (ids [n_calls][pairs]), writes the slot of every id
+ * (slot_ids [n_calls][pairs]) and, per call, the expert copied into each slot or -1
+ * (loaded_expert [n_calls][n_slots]); totals of hits and misses (distinct experts
+ * per call found / not found in a slot). */
+MOE_API int moe_cache_lru_plan(int E, int n_slots, int n_calls, int pairs, const int32_t* ids, int32_t* slot_ids,
+                               int32_t* loaded_expert, unsigned long long* hits, unsigned long long* misses);
+
 /* Allocation-free form of moe_forward (the pages have no counterpart; it is an
  * interface convenience of this library).
  *

@@ -31,7 +31,8 @@ TRACE_WORDS = len(TRACE_EVENTS)
 # every entry point include/moe_api.h declares
 EXPORTS = ("moe_strerror", "moe_workspace_size", "moe_plan_info", "moe_align_capacity", "moe_route",
            "moe_topk_from_logits", "moe_align", "moe_forward", "moe_forward_noalloc", "moe_get_status",
-           "moe_version", "moe_inv_rope_fp8_quant")
+           "moe_version", "moe_inv_rope_fp8_quant", "moe_forward_routed", "moe_cache_create", "moe_cache_destroy",
+           "moe_cache_workspace_size", "moe_forward_cached", "moe_cache_stats", "moe_cache_lru_plan")
 NOALLOC_MAX_WORKSPACE = 32 << 20
 
 
@@ -52,6 +53,10 @@ class moe_plan(ctypes.Structure):
     _fields_ = [("orientation", ctypes.c_int), ("block", ctypes.c_int), ("splits_gemm1", ctypes.c_int),
                 ("splits_gemm2", ctypes.c_int), ("act_split", ctypes.c_int), ("kernel_launches", ctypes.c_int),
                 ("single_launch", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t)]
+
+
+class moe_cache_stats_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_ulonglong) for n in ("calls", "hits", "misses", "evictions", "bytes_h2d")]
 
 
 def _load():
@@ -81,6 +86,21 @@ def _load():
     lib.moe_forward_noalloc.argtypes = [P, P, P, P, i, i, i, i, i, i, i, i, P, P, P, P, P]
     lib.moe_get_status.restype = i
     lib.moe_get_status.argtypes = [P]
+    lib.moe_forward_routed.restype = i
+    lib.moe_forward_routed.argtypes = [P, P, P, P, P, i, i, i, i, i, i, i, P, P, P, P, sz, P, P]
+    lib.moe_cache_create.restype = i
+    lib.moe_cache_create.argtypes = [P, P, P, P, i, i, i, i, i, i, i, ctypes.POINTER(P)]
+    lib.moe_cache_destroy.restype = i
+    lib.moe_cache_destroy.argtypes = [P]
+    lib.moe_cache_workspace_size.restype = i
+    lib.moe_cache_workspace_size.argtypes = [P, i, i, P, ctypes.POINTER(sz)]
+    lib.moe_forward_cached.restype = i
+    lib.moe_forward_cached.argtypes = [P, P, P, i, i, i, P, P, sz, P, P]
+    lib.moe_cache_stats.restype = i
+    lib.moe_cache_stats.argtypes = [P, ctypes.POINTER(moe_cache_stats_t)]
+    lib.moe_cache_lru_plan.restype = i
+    lib.moe_cache_lru_plan.argtypes = [i, i, i, i, P, P, P, ctypes.POINTER(ctypes.c_ulonglong),
+                                       ctypes.POINTER(ctypes.c_ulonglong)]
     lib.moe_inv_rope_fp8_quant.restype = i
     lib.moe_inv_rope_fp8_quant.argtypes = [P, i, i, i, i, P, P, i, P, P, P]
     return lib
@@ -259,3 +279,96 @@ def moe_inv_rope_fp8_quant(x: torch.Tensor, positions: torch.Tensor, cos_sin: to
                                        cos_sin.shape[0], _p(q_out), _p(scale_out), _stream(stream)),
            "moe_inv_rope_fp8_quant")
     return q_out, scale_out
+
+
+def moe_forward_routed(hidden: torch.Tensor, topk_w: torch.Tensor, topk_ids: torch.Tensor, w13: torch.Tensor,
+                       w2: torch.Tensor, w13_scale=None, w2_scale=None, out=None, workspace=None, options=None,
+                       stream=None):
+    """Steps 3-7 of the layer on a given routing (topk_w fp32 [T,k], topk_ids int32 [T,k])."""
+    T, H = hidden.shape
+    E, twoI, _ = w13.shape
+    I = twoI // 2
+    k = topk_ids.shape[1]
+    act, wdt = _dt(hidden), _dt(w13)
+    o = dict(options or {})
+    o["single_launch"] = 2
+    need = moe_workspace_size(T, H, I, E, k, act, wdt, o)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=hidden.device)
+    out = torch.empty_like(hidden) if out is None else out
+    _check(_lib.moe_forward_routed(_p(hidden), _p(topk_w), _p(topk_ids), _p(w13), _p(w2), T, H, I, E, k, act, wdt,
+                                   _p(w13_scale), _p(w2_scale), _p(out), _p(workspace), workspace.numel(), _opts(o),
+                                   _stream(stream)), "moe_forward_routed")
+    return out
+
+
+class ExpertCache:
+    """Host-resident expert weights with a pool of `n_slots` device slots (moe_cache_* in the C ABI).
+
+    w13 [E,2I,H] and w2 [E,H,I] are CPU tensors (pinned ones avoid a registration); the cache keeps
+    references to them for its lifetime.
+    """
+
+    def __init__(self, w13: torch.Tensor, w2: torch.Tensor, n_slots: int, max_tokens: int, topk: int, w13_scale=None,
+                 w2_scale=None):
+        if w13.is_cuda or w2.is_cuda:
+            raise ValueError("expert weights must be host tensors")
+        E, twoI, H = w13.shape
+        self.E, self.H, self.I, self.topk, self.n_slots = E, H, twoI // 2, topk, n_slots
+        self._keep = (w13.contiguous(), w2.contiguous(),
+                      None if w13_scale is None else w13_scale.float().contiguous(),
+                      None if w2_scale is None else w2_scale.float().contiguous())
+        h = ctypes.c_void_p(0)
+        _check(_lib.moe_cache_create(_p(self._keep[0]), _p(self._keep[1]), _p(self._keep[2]), _p(self._keep[3]), E, H,
+                                     self.I, _dt(w13), n_slots, max_tokens, topk, ctypes.byref(h)), "moe_cache_create")
+        self._h = h
+
+    def close(self):
+        if self._h is not None and self._h.value:
+            _lib.moe_cache_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def workspace_size(self, T: int, act_dtype: int = MOE_BF16, options=None) -> int:
+        n = ctypes.c_size_t(0)
+        _check(_lib.moe_cache_workspace_size(self._h, T, act_dtype, _opts(options), ctypes.byref(n)),
+               "moe_cache_workspace_size")
+        return int(n.value)
+
+    def forward(self, hidden: torch.Tensor, router_w: torch.Tensor, renorm: bool, out=None, workspace=None,
+                options=None, stream=None) -> torch.Tensor:
+        T = hidden.shape[0]
+        if workspace is None:
+            workspace = torch.empty(self.workspace_size(T, _dt(hidden), options), dtype=torch.uint8,
+                                    device=hidden.device)
+        out = torch.empty_like(hidden) if out is None else out
+        _check(_lib.moe_forward_cached(self._h, _p(hidden), _p(router_w), T, int(bool(renorm)), _dt(hidden), _p(out),
+                                       _p(workspace), workspace.numel(), _opts(options), _stream(stream)),
+               "moe_forward_cached")
+        return out
+
+    def stats(self) -> dict:
+        st = moe_cache_stats_t()
+        _check(_lib.moe_cache_stats(self._h, ctypes.byref(st)), "moe_cache_stats")
+        return {n: int(getattr(st, n)) for n, _ in moe_cache_stats_t._fields_}
+
+
+def moe_cache_lru_plan(E: int, n_slots: int, ids):
+    """The cache's slot policy on a sequence of calls (ids int32 [n_calls, pairs]), host only:
+    (slot_ids [n_calls, pairs], loaded_expert [n_calls, n_slots], hits, misses)."""
+    import numpy as np
+
+    ids = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+    n_calls, pairs = ids.shape
+    slot_ids = np.empty_like(ids)
+    loaded = np.empty((n_calls, n_slots), dtype=np.int32)
+    hits, misses = ctypes.c_ulonglong(0), ctypes.c_ulonglong(0)
+    _check(_lib.moe_cache_lru_plan(E, n_slots, n_calls, pairs, ids.ctypes.data_as(ctypes.c_void_p),
+                                   slot_ids.ctypes.data_as(ctypes.c_void_p), loaded.ctypes.data_as(ctypes.c_void_p),
+                                   ctypes.byref(hits), ctypes.byref(misses)), "moe_cache_lru_plan")
+    return slot_ids, loaded, int(hits.value), int(misses.value)

@@ -265,6 +265,236 @@ static cudaError_t launch_router(const void* X, const void* Wr, int T, int H, in
   return launch_router_logits(X, Wr, T, H, E, act == MOE_BF16, logits, s);
 }
 
+enum { STEPS_ROUTE = 1, STEPS_EXPERTS = 2, STEPS_ALL = 3 };
+
+// The launch sequence of one layer call on a planned, validated workspace.
+// steps selects routing (S1-S2) and/or the expert part (S3-S7, which reads
+// the routing from the workspace).  E_router is the router's expert count
+// and logits_override an optional logits buffer (both differ from the plan's
+// when the experts are cache slots).
+static int forward_steps(const Plan& pl, int steps, const void* hidden, const void* router_w, int E_router,
+                         float* logits_override, const float* tw_in, const int32_t* tid_in, const void* w13,
+                         const void* w2, int T, int H, int I, int E, int topk, int renorm, moe_dtype act_dtype,
+                         const float* w13_scale, const float* w2_scale, void* out, void* workspace,
+                         const moe_options* opts, int* st, int sms, cudaStream_t s) {
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* logits = logits_override ? logits_override : reinterpret_cast<float*>(ws + pl.o_logits);
+  // the routing: written here by steps 1-2, or given by the caller for the expert steps alone
+  float* tw = tw_in ? const_cast<float*>(tw_in) : reinterpret_cast<float*>(ws + pl.o_tw);
+  int32_t* tid = tid_in ? const_cast<int32_t*>(tid_in) : reinterpret_cast<int32_t*>(ws + pl.o_tid);
+  int32_t* meta = reinterpret_cast<int32_t*>(ws + pl.o_meta);
+  int32_t* sorted = reinterpret_cast<int32_t*>(ws + pl.o_sorted);
+  int32_t* eids = reinterpret_cast<int32_t*>(ws + pl.o_eids);
+  void* xs = ws + pl.o_xs;
+  void* aint = ws + pl.o_aint;
+  float* af32 = reinterpret_cast<float*>(ws + pl.o_af32);
+  float* p1 = reinterpret_cast<float*>(ws + pl.o_p1);
+  void* y = ws + pl.o_y;
+  unsigned* amax = reinterpret_cast<unsigned*>(ws + pl.o_misc);  // [0] input amax, [1] intermediate amax
+  int* flag = reinterpret_cast<int*>(ws + pl.o_misc + 64);
+  const moe_options* o = opts;
+  const int cap = (int)pl.cap;
+  const int n = T * topk;
+  cudaError_t e = cudaSuccess;
+#define MOE_TRY(x)                 \
+  do {                             \
+    e = (x);                       \
+    if (e != cudaSuccess) return MOE_ERR_CUDA; \
+  } while (0)
+
+  if (steps == STEPS_ALL && pl.fused && !(o && o->inject_timeout)) {
+    // steps 1-7 in one cooperative kernel; its events bracket the kernel as GEMM1
+    if (o) {
+      for (int st = MOE_STAGE_ROUTE; st < MOE_STAGE_GEMM1; ++st) {
+        record(o->stage_begin[st], s);
+        record(o->stage_end[st], s);
+      }
+      record(o->stage_begin[MOE_STAGE_GEMM1], s);
+    }
+    FusedArgs fa = {};
+    fa.T = T;
+    fa.H = H;
+    fa.I = I;
+    fa.E = E;
+    fa.k = topk;
+    fa.renorm = renorm != 0;
+    fa.s1 = pl.s1;
+    fa.kbs1 = pl.kb1;
+    fa.s2 = pl.s2;
+    fa.kbs2 = pl.kb2;
+    fa.xbox = pl.xbox;
+    fa.gather = pl.gather_in_gemm;
+    fa.act_split = pl.act_split;
+    fa.cap = cap;
+    fa.combine_g = combine_lanes(T, H, topk);
+    fa.X = hidden;
+    fa.Wr = router_w;
+    fa.w13 = w13;
+    fa.w2 = w2;
+    fa.logits = logits;
+    fa.topk_w = tw;
+    fa.topk_ids = tid;
+    fa.Xs = xs;
+    fa.aint = aint;
+    fa.p1 = p1;
+    fa.p1_stride = pl.p1_stride;
+    fa.y = reinterpret_cast<float*>(y);
+    fa.y_stride = pl.y_stride;
+    fa.out = out;
+    fa.sync = ws + pl.o_sync;
+    fa.trace = o ? o->trace : nullptr;
+    fa.status = st;
+    fa.num_sms = sms;
+    if (launch_decode_fused(fa, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (o) {
+      record(o->stage_end[MOE_STAGE_GEMM1], s);
+      for (int st = MOE_STAGE_ACT; st < MOE_NUM_STAGES; ++st) {
+        record(o->stage_begin[st], s);
+        record(o->stage_end[st], s);
+      }
+    }
+    return MOE_OK;
+  }
+
+  if ((steps & STEPS_ROUTE) && o && o->inject_timeout) {
+    MOE_TRY(cudaMemsetAsync(flag, 0, sizeof(int), s));
+    MOE_TRY(launch_inject_timeout(flag, st, s));
+    return MOE_OK;
+  }
+
+  // 1-2. router
+  if (steps & STEPS_ROUTE) {
+    if (o) record(o->stage_begin[MOE_STAGE_ROUTE], s);
+    MOE_TRY(launch_router(hidden, router_w, T, H, E_router, act_dtype, logits, st, s));
+    MOE_TRY(launch_topk(logits, T, E_router, topk, renorm != 0, tw, tid, s));
+    if (o) record(o->stage_end[MOE_STAGE_ROUTE], s);
+  }
+  if (!(steps & STEPS_EXPERTS)) return MOE_OK;
+
+  // 3. permutation
+  if (o) record(o->stage_begin[MOE_STAGE_ALIGN], s);
+  MOE_TRY(launch_align(tid, T, topk, E, pl.B, sorted, eids, meta + META_NPP, nullptr, meta, st, s));
+  if (o) record(o->stage_end[MOE_STAGE_ALIGN], s);
+
+  // 4. activations: the fp32 path gathers rows into expert order here; the
+  // tensor-core paths gather inside GEMM1 (FP8: quantise the input to e4m3 first)
+  if (o) record(o->stage_begin[MOE_STAGE_GATHER], s);
+  if (pl.path == PATH_FP8) {
+    MOE_TRY(cudaMemsetAsync(amax, 0, 2 * sizeof(unsigned), s));
+    MOE_TRY(launch_amax_bf16(hidden, (size_t)T * H, amax, s));
+    if (pl.gather_in_gemm)
+      MOE_TRY(launch_quant_x(hidden, (size_t)T * H, amax, (uint8_t*)xs, s));
+    else
+      MOE_TRY(launch_gather(hidden, T, H, topk, 2, 1, amax, sorted, meta, cap, xs, s));
+  } else if (!pl.gather_in_gemm) {
+    MOE_TRY(launch_gather(hidden, T, H, topk, pl.path == PATH_F32 ? 4 : 2, 0, nullptr, sorted, meta, cap, xs, s));
+  }
+  if (o) record(o->stage_end[MOE_STAGE_GATHER], s);
+
+  if (pl.path == PATH_F32) {
+    if (o) record(o->stage_begin[MOE_STAGE_GEMM1], s);
+    MOE_TRY(launch_gemm1_simt((const float*)xs, (const float*)w13, H, I, pl.B, eids, meta, cap, (float*)aint, s));
+    if (o) record(o->stage_end[MOE_STAGE_GEMM1], s);
+    if (o) record(o->stage_begin[MOE_STAGE_ACT], s);
+    if (o) record(o->stage_end[MOE_STAGE_ACT], s);
+    if (o) record(o->stage_begin[MOE_STAGE_GEMM2], s);
+    MOE_TRY(launch_gemm2_simt((const float*)aint, (const float*)w2, H, I, pl.B, T, topk, sorted, eids, meta, cap,
+                              (float*)y, s));
+    if (o) record(o->stage_end[MOE_STAGE_GEMM2], s);
+  } else {
+    const bool fp8 = pl.path == PATH_FP8;
+    TcGemmArgs g = {};
+    g.swap = pl.swap;
+    g.fp8 = fp8;
+    g.T = T;
+    g.k = topk;
+    g.E = E;
+    g.I = I;
+    g.H = H;
+    g.cap = cap;
+    g.sorted = sorted;
+    g.eids = eids;
+    g.meta = meta;
+    g.status = st;
+    g.num_sms = sms;
+
+    // 5. GEMM1 on w13 (+ SiLU(gate)*up)
+    TcGemmArgs g1 = g;
+    g1.K = H;
+    g1.W = w13;
+    g1.X = (fp8 || !pl.gather_in_gemm) ? (const void*)xs : hidden;
+    g1.gather = pl.gather_in_gemm;
+    g1.w_rows_per_expert = 2 * I;
+    g1.w_pair_off = I;
+    g1.wbox = 128;
+    g1.w_tile_rows = 128;
+    g1.xbox = pl.xbox;
+    g1.n_tiles = I / 128;
+    g1.splits = pl.s1;
+    g1.kb_per_split = pl.kb1;
+    g1.w_scale = w13_scale;
+    g1.a_amax = amax;
+    g1.amax_out = amax + 1;
+    void* aint_lo = pl.act_split ? (void*)((uint16_t*)aint + (size_t)cap * I) : nullptr;
+    if (pl.s1 > 1) {
+      g1.epi = TC_EPI_G1_PART;
+      g1.out = p1;
+      g1.out_split_stride = pl.p1_stride;
+    } else {
+      g1.epi = fp8 ? TC_EPI_G1_F32AMAX : TC_EPI_G1_BF16;
+      g1.out = fp8 ? (void*)af32 : aint;
+      g1.out_lo = aint_lo;
+    }
+    if (o) record(o->stage_begin[MOE_STAGE_GEMM1], s);
+    MOE_TRY(launch_gemm_tc(g1, s));
+    if (o) record(o->stage_end[MOE_STAGE_GEMM1], s);
+
+    // split-K reduction / FP8 quantisation of the intermediate
+    if (o) record(o->stage_begin[MOE_STAGE_ACT], s);
+    if (pl.s1 > 1)
+      MOE_TRY(launch_reduce_act(p1, pl.s1, pl.p1_stride, I, pl.B, n, sorted, eids, meta, cap,
+                                fp8 ? w13_scale : nullptr, amax, fp8 ? 1 : 0, fp8 ? (void*)af32 : aint, aint_lo, amax + 1,
+                                s));
+    if (fp8) MOE_TRY(launch_quant_act(af32, I, meta, cap, amax + 1, (uint8_t*)aint, s));
+    if (o) record(o->stage_end[MOE_STAGE_ACT], s);
+
+    // 6. GEMM2 on w2
+    TcGemmArgs g2 = g;
+    g2.K = I;
+    g2.W = w2;
+    g2.X = aint;
+    g2.x_lo_rows = pl.act_split ? cap : 0;
+    g2.w_rows_per_expert = H;
+    g2.wbox = pl.swap ? 128 : pl.wbox2;
+    g2.w_pair_off = g2.wbox;
+    g2.w_tile_rows = 2 * g2.wbox;
+    g2.xbox = pl.xbox;
+    g2.n_tiles = (H + g2.w_tile_rows - 1) / g2.w_tile_rows;
+    g2.splits = pl.s2;
+    g2.kb_per_split = pl.kb2;
+    g2.w_scale = w2_scale;
+    g2.a_amax = amax + 1;
+    g2.out = y;
+    g2.out_split_stride = pl.y_stride;
+    g2.epi = pl.y_bf16 ? TC_EPI_G2_BF16 : TC_EPI_G2_F32;
+    // GEMM2's predecessor is GEMM1 or a kernel GEMM1 let launch, and GEMM1 lets
+    // its dependents launch only after its own dependency wait: the permutation
+    // metadata is complete by then, so GEMM2 may stream weights early.
+    g2.early = true;
+    if (o) record(o->stage_begin[MOE_STAGE_GEMM2], s);
+    MOE_TRY(launch_gemm_tc(g2, s));
+    if (o) record(o->stage_end[MOE_STAGE_GEMM2], s);
+  }
+
+  // 7. combine
+  if (o) record(o->stage_begin[MOE_STAGE_COMBINE], s);
+  MOE_TRY(launch_combine(y, pl.y_bf16 ? 1 : 0, pl.s2, pl.y_stride, tw, T, topk, H, out, act_dtype == MOE_BF16 ? 1 : 0,
+                         s));
+  if (o) record(o->stage_end[MOE_STAGE_COMBINE], s);
+#undef MOE_TRY
+  return MOE_OK;
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -393,219 +623,36 @@ int moe_forward(const void* hidden, const void* router_w, const void* w13, const
   const int sms = num_sms();
   if (!st || sms <= 0) return MOE_ERR_CUDA;
 
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  float* logits = reinterpret_cast<float*>(ws + pl.o_logits);
-  float* tw = reinterpret_cast<float*>(ws + pl.o_tw);
-  int32_t* tid = reinterpret_cast<int32_t*>(ws + pl.o_tid);
-  int32_t* meta = reinterpret_cast<int32_t*>(ws + pl.o_meta);
-  int32_t* sorted = reinterpret_cast<int32_t*>(ws + pl.o_sorted);
-  int32_t* eids = reinterpret_cast<int32_t*>(ws + pl.o_eids);
-  void* xs = ws + pl.o_xs;
-  void* aint = ws + pl.o_aint;
-  float* af32 = reinterpret_cast<float*>(ws + pl.o_af32);
-  float* p1 = reinterpret_cast<float*>(ws + pl.o_p1);
-  void* y = ws + pl.o_y;
-  unsigned* amax = reinterpret_cast<unsigned*>(ws + pl.o_misc);  // [0] input amax, [1] intermediate amax
-  int* flag = reinterpret_cast<int*>(ws + pl.o_misc + 64);
-  const moe_options* o = opts;
-  const int cap = (int)pl.cap;
-  const int n = T * topk;
-  cudaError_t e = cudaSuccess;
-#define MOE_TRY(x)                 \
-  do {                             \
-    e = (x);                       \
-    if (e != cudaSuccess) return MOE_ERR_CUDA; \
-  } while (0)
+  return forward_steps(pl, STEPS_ALL, hidden, router_w, E, nullptr, nullptr, nullptr, w13, w2, T, H, I, E, topk, renorm,
+                       act_dtype, w13_scale, w2_scale, out, workspace, opts, st, sms,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
 
-  if (pl.fused && !(o && o->inject_timeout)) {
-    // steps 1-7 in one cooperative kernel; its events bracket the kernel as GEMM1
-    if (o) {
-      for (int st = MOE_STAGE_ROUTE; st < MOE_STAGE_GEMM1; ++st) {
-        record(o->stage_begin[st], s);
-        record(o->stage_end[st], s);
-      }
-      record(o->stage_begin[MOE_STAGE_GEMM1], s);
-    }
-    FusedArgs fa = {};
-    fa.T = T;
-    fa.H = H;
-    fa.I = I;
-    fa.E = E;
-    fa.k = topk;
-    fa.renorm = renorm != 0;
-    fa.s1 = pl.s1;
-    fa.kbs1 = pl.kb1;
-    fa.s2 = pl.s2;
-    fa.kbs2 = pl.kb2;
-    fa.xbox = pl.xbox;
-    fa.gather = pl.gather_in_gemm;
-    fa.act_split = pl.act_split;
-    fa.cap = cap;
-    fa.combine_g = combine_lanes(T, H, topk);
-    fa.X = hidden;
-    fa.Wr = router_w;
-    fa.w13 = w13;
-    fa.w2 = w2;
-    fa.logits = logits;
-    fa.topk_w = tw;
-    fa.topk_ids = tid;
-    fa.Xs = xs;
-    fa.aint = aint;
-    fa.p1 = p1;
-    fa.p1_stride = pl.p1_stride;
-    fa.y = reinterpret_cast<float*>(y);
-    fa.y_stride = pl.y_stride;
-    fa.out = out;
-    fa.sync = ws + pl.o_sync;
-    fa.trace = o ? o->trace : nullptr;
-    fa.status = st;
-    fa.num_sms = sms;
-    if (launch_decode_fused(fa, s) != cudaSuccess) return MOE_ERR_CUDA;
-    if (o) {
-      record(o->stage_end[MOE_STAGE_GEMM1], s);
-      for (int st = MOE_STAGE_ACT; st < MOE_NUM_STAGES; ++st) {
-        record(o->stage_begin[st], s);
-        record(o->stage_end[st], s);
-      }
-    }
-    return MOE_OK;
-  }
-
-  if (o && o->inject_timeout) {
-    MOE_TRY(cudaMemsetAsync(flag, 0, sizeof(int), s));
-    MOE_TRY(launch_inject_timeout(flag, st, s));
-    return MOE_OK;
-  }
-
-  // 1-2. router
-  if (o) record(o->stage_begin[MOE_STAGE_ROUTE], s);
-  MOE_TRY(launch_router(hidden, router_w, T, H, E, act_dtype, logits, st, s));
-  MOE_TRY(launch_topk(logits, T, E, topk, renorm != 0, tw, tid, s));
-  if (o) record(o->stage_end[MOE_STAGE_ROUTE], s);
-
-  // 3. permutation
-  if (o) record(o->stage_begin[MOE_STAGE_ALIGN], s);
-  MOE_TRY(launch_align(tid, T, topk, E, pl.B, sorted, eids, meta + META_NPP, nullptr, meta, st, s));
-  if (o) record(o->stage_end[MOE_STAGE_ALIGN], s);
-
-  // 4. activations: the fp32 path gathers rows into expert order here; the
-  // tensor-core paths gather inside GEMM1 (FP8: quantise the input to e4m3 first)
-  if (o) record(o->stage_begin[MOE_STAGE_GATHER], s);
-  if (pl.path == PATH_FP8) {
-    MOE_TRY(cudaMemsetAsync(amax, 0, 2 * sizeof(unsigned), s));
-    MOE_TRY(launch_amax_bf16(hidden, (size_t)T * H, amax, s));
-    if (pl.gather_in_gemm)
-      MOE_TRY(launch_quant_x(hidden, (size_t)T * H, amax, (uint8_t*)xs, s));
-    else
-      MOE_TRY(launch_gather(hidden, T, H, topk, 2, 1, amax, sorted, meta, cap, xs, s));
-  } else if (!pl.gather_in_gemm) {
-    MOE_TRY(launch_gather(hidden, T, H, topk, pl.path == PATH_F32 ? 4 : 2, 0, nullptr, sorted, meta, cap, xs, s));
-  }
-  if (o) record(o->stage_end[MOE_STAGE_GATHER], s);
-
-  if (pl.path == PATH_F32) {
-    if (o) record(o->stage_begin[MOE_STAGE_GEMM1], s);
-    MOE_TRY(launch_gemm1_simt((const float*)xs, (const float*)w13, H, I, pl.B, eids, meta, cap, (float*)aint, s));
-    if (o) record(o->stage_end[MOE_STAGE_GEMM1], s);
-    if (o) record(o->stage_begin[MOE_STAGE_ACT], s);
-    if (o) record(o->stage_end[MOE_STAGE_ACT], s);
-    if (o) record(o->stage_begin[MOE_STAGE_GEMM2], s);
-    MOE_TRY(launch_gemm2_simt((const float*)aint, (const float*)w2, H, I, pl.B, T, topk, sorted, eids, meta, cap,
-                              (float*)y, s));
-    if (o) record(o->stage_end[MOE_STAGE_GEMM2], s);
-  } else {
-    const bool fp8 = pl.path == PATH_FP8;
-    TcGemmArgs g = {};
-    g.swap = pl.swap;
-    g.fp8 = fp8;
-    g.T = T;
-    g.k = topk;
-    g.E = E;
-    g.I = I;
-    g.H = H;
-    g.cap = cap;
-    g.sorted = sorted;
-    g.eids = eids;
-    g.meta = meta;
-    g.status = st;
-    g.num_sms = sms;
-
-    // 5. GEMM1 on w13 (+ SiLU(gate)*up)
-    TcGemmArgs g1 = g;
-    g1.K = H;
-    g1.W = w13;
-    g1.X = (fp8 || !pl.gather_in_gemm) ? (const void*)xs : hidden;
-    g1.gather = pl.gather_in_gemm;
-    g1.w_rows_per_expert = 2 * I;
-    g1.w_pair_off = I;
-    g1.wbox = 128;
-    g1.w_tile_rows = 128;
-    g1.xbox = pl.xbox;
-    g1.n_tiles = I / 128;
-    g1.splits = pl.s1;
-    g1.kb_per_split = pl.kb1;
-    g1.w_scale = w13_scale;
-    g1.a_amax = amax;
-    g1.amax_out = amax + 1;
-    void* aint_lo = pl.act_split ? (void*)((uint16_t*)aint + (size_t)cap * I) : nullptr;
-    if (pl.s1 > 1) {
-      g1.epi = TC_EPI_G1_PART;
-      g1.out = p1;
-      g1.out_split_stride = pl.p1_stride;
-    } else {
-      g1.epi = fp8 ? TC_EPI_G1_F32AMAX : TC_EPI_G1_BF16;
-      g1.out = fp8 ? (void*)af32 : aint;
-      g1.out_lo = aint_lo;
-    }
-    if (o) record(o->stage_begin[MOE_STAGE_GEMM1], s);
-    MOE_TRY(launch_gemm_tc(g1, s));
-    if (o) record(o->stage_end[MOE_STAGE_GEMM1], s);
-
-    // split-K reduction / FP8 quantisation of the intermediate
-    if (o) record(o->stage_begin[MOE_STAGE_ACT], s);
-    if (pl.s1 > 1)
-      MOE_TRY(launch_reduce_act(p1, pl.s1, pl.p1_stride, I, pl.B, n, sorted, eids, meta, cap,
-                                fp8 ? w13_scale : nullptr, amax, fp8 ? 1 : 0, fp8 ? (void*)af32 : aint, aint_lo, amax + 1,
-                                s));
-    if (fp8) MOE_TRY(launch_quant_act(af32, I, meta, cap, amax + 1, (uint8_t*)aint, s));
-    if (o) record(o->stage_end[MOE_STAGE_ACT], s);
-
-    // 6. GEMM2 on w2
-    TcGemmArgs g2 = g;
-    g2.K = I;
-    g2.W = w2;
-    g2.X = aint;
-    g2.x_lo_rows = pl.act_split ? cap : 0;
-    g2.w_rows_per_expert = H;
-    g2.wbox = pl.swap ? 128 : pl.wbox2;
-    g2.w_pair_off = g2.wbox;
-    g2.w_tile_rows = 2 * g2.wbox;
-    g2.xbox = pl.xbox;
-    g2.n_tiles = (H + g2.w_tile_rows - 1) / g2.w_tile_rows;
-    g2.splits = pl.s2;
-    g2.kb_per_split = pl.kb2;
-    g2.w_scale = w2_scale;
-    g2.a_amax = amax + 1;
-    g2.out = y;
-    g2.out_split_stride = pl.y_stride;
-    g2.epi = pl.y_bf16 ? TC_EPI_G2_BF16 : TC_EPI_G2_F32;
-    // GEMM2's predecessor is GEMM1 or a kernel GEMM1 let launch, and GEMM1 lets
-    // its dependents launch only after its own dependency wait: the permutation
-    // metadata is complete by then, so GEMM2 may stream weights early.
-    g2.early = true;
-    if (o) record(o->stage_begin[MOE_STAGE_GEMM2], s);
-    MOE_TRY(launch_gemm_tc(g2, s));
-    if (o) record(o->stage_end[MOE_STAGE_GEMM2], s);
-  }
-
-  // 7. combine
-  if (o) record(o->stage_begin[MOE_STAGE_COMBINE], s);
-  MOE_TRY(launch_combine(y, pl.y_bf16 ? 1 : 0, pl.s2, pl.y_stride, tw, T, topk, H, out, act_dtype == MOE_BF16 ? 1 : 0,
-                         s));
-  if (o) record(o->stage_end[MOE_STAGE_COMBINE], s);
-#undef MOE_TRY
-  return MOE_OK;
+int moe_forward_routed(const void* hidden, const float* topk_w, const int32_t* topk_ids, const void* w13,
+                       const void* w2, int T, int H, int I, int E, int topk, moe_dtype act_dtype, moe_dtype w_dtype,
+                       const float* w13_scale, const float* w2_scale, void* out, void* workspace,
+                       size_t workspace_bytes, const moe_options* opts, moe_stream_t stream) {
+  moe_options o = opts ? *opts : moe_options{};
+  o.single_launch = 2;  // the single launch routes inside its kernel
+  if (opts && opts->single_launch == 1) return MOE_ERR_UNSUPPORTED;
+  if (opts && opts->inject_timeout) return MOE_ERR_ARG;
+  Plan pl;
+  int rc = make_plan(T, H, I, E, topk, act_dtype, w_dtype, &o, &pl);
+  if (rc) return rc;
+  if (T == 0) return MOE_OK;
+  if (!hidden || !topk_w || !topk_ids || !w13 || !w2 || !out || !workspace) return MOE_ERR_ARG;
+  if (pl.path == PATH_FP8 && (!w13_scale || !w2_scale)) return MOE_ERR_ARG;
+  if (misaligned(hidden) || misaligned(topk_w, 4) || misaligned(topk_ids, 4) || misaligned(w13) || misaligned(w2) ||
+      misaligned(out) || misaligned(workspace, 256) || (w13_scale && misaligned(w13_scale, 4)) ||
+      (w2_scale && misaligned(w2_scale, 4)))
+    return MOE_ERR_ALIGNMENT;
+  if (workspace_bytes < pl.total) return MOE_ERR_WORKSPACE;
+  int* st = status_word();
+  const int sms = num_sms();
+  if (!st || sms <= 0) return MOE_ERR_CUDA;
+  return forward_steps(pl, STEPS_EXPERTS, hidden, nullptr, E, nullptr, topk_w, topk_ids, w13, w2, T, H, I, E, topk,
+                       0, act_dtype, w13_scale, w2_scale, out, workspace, opts ? &o : nullptr, st, sms,
+                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 int moe_inv_rope_fp8_quant(const void* x, int T, int heads, int head_dim, int rot_dim, const int32_t* positions,
