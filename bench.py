@@ -41,6 +41,7 @@ WORKLOADS = {
     "fine_decode_M64": ("fine_decode", 64), "fine_decode_M32": ("fine_decode", 32),
     "fine_decode_M8": ("fine_decode", 8), "fine_decode_M1": ("fine_decode", 1),
     "fp8_decode_M64": ("fp8_decode", 64), "fp8_decode_M16": ("fp8_decode", 16), "fp8_decode_M1": ("fp8_decode", 1),
+    "int4_decode_M64": ("int4_decode", 64), "int4_decode_M16": ("int4_decode", 16), "int4_decode_M1": ("int4_decode", 1),
     "prefill_T8192": ("prefill", 8192), "prefill_hot_T8192": ("prefill_hot", 8192),
     "tiny_f32_T64": ("tiny_f32", 64),
 }
@@ -76,12 +77,13 @@ def peaks():
 # algorithmic work of one layer call (from the realised routing)
 # ----------------------------------------------------------------------------
 def work(sp, n_active: int, act_split: bool):
-    wb = 1 if sp.w == "e4m3" else (4 if sp.w == "f32" else 2)
+    # weight bytes per element: e4m3 1, fp32 4, bf16 2, INT4 half a byte plus a 2-byte scale per 128
+    wb = {"e4m3": 1.0, "f32": 4.0, "bf16": 2.0, "int4": 0.5 + 2.0 / 128}[sp.w]
     ab = 4 if sp.act == "f32" else 2
     n = sp.T * sp.k
     I, H = sp.I, sp.H
-    w13 = n_active * 2 * I * H * wb
-    w2 = n_active * H * I * wb
+    w13 = int(n_active * 2 * I * H * wb)
+    w2 = int(n_active * H * I * wb)
     a_bytes = n * I * (1 if sp.w == "e4m3" else ab * (2 if act_split else 1))
     g1_bytes = w13 + n * H * (1 if sp.w == "e4m3" else ab) + a_bytes
     g2_bytes = w2 + a_bytes + n * H * 4
@@ -90,7 +92,7 @@ def work(sp, n_active: int, act_split: bool):
     flops2 = 2.0 * n * H * I
     return {"w13_bytes": w13, "w2_bytes": w2, "gemm1_bytes": g1_bytes, "gemm2_bytes": g2_bytes,
             "layer_bytes": layer_bytes, "gemm1_flops": flops1, "gemm2_flops": flops2,
-            "layer_flops": flops1 + flops2 + 2.0 * sp.T * sp.E * H, "bytes_per_active_expert": 3 * I * H * wb}
+            "layer_flops": flops1 + flops2 + 2.0 * sp.T * sp.E * H, "bytes_per_active_expert": int(3 * I * H * wb)}
 
 
 def _sha(path):
@@ -206,7 +208,8 @@ def run_ours(args, rank, world, dev):
         X, Wr, W13, W2 = L["X"], L["Wr"], L["W13"], L["W2"]
         s13, s2 = L["w13_scale"], L["w2_scale"]
         act = moe.MOE_F32 if sp.act == "f32" else moe.MOE_BF16
-        wdt = {"f32": moe.MOE_F32, "bf16": moe.MOE_BF16, "e4m3": moe.MOE_E4M3}[sp.w]
+        wdt = {"f32": moe.MOE_F32, "bf16": moe.MOE_BF16, "e4m3": moe.MOE_E4M3, "int4": moe.MOE_INT4}[sp.w]
+        wfmt = "int4" if sp.w == "int4" else None
         base_opts = {"single_launch": SINGLE_LAUNCH[args.single_launch]}
         plan = moe.moe_plan_info(T, sp.H, sp.I, sp.E, sp.k, act, wdt, base_opts)
         # the two decode paths (one cooperative kernel / the multi-kernel sequence) where both apply
@@ -229,7 +232,7 @@ def run_ours(args, rank, world, dev):
         def step(options=None):
             o = dict(base_opts)
             o.update(options or {})
-            moe.moe_forward(X, Wr, W13, W2, sp.k, sp.renorm, s13, s2, out=out, workspace=ws, options=o,
+            moe.moe_forward(X, Wr, W13, W2, sp.k, sp.renorm, s13, s2, out=out, workspace=ws, options=o, w_format=wfmt,
                             stream=stream)
 
         is_head = wi == 0
@@ -349,6 +352,7 @@ def run_ours(args, rank, world, dev):
             def e2e_step():
                 Xd.copy_(Xh, non_blocking=True)
                 moe.moe_forward(Xd, Wr, W13, W2, sp.k, sp.renorm, s13, s2, out=out, workspace=ws, options=base_opts,
+                                w_format=wfmt,
                                 stream=stream)
                 outh.copy_(out, non_blocking=True)
 

@@ -52,8 +52,12 @@ typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t */
 typedef struct CUevent_st* moe_event_t;   /* same type as cudaEvent_t */
 
 /* Element types.  BF16 is stored as 16-bit bfloat16, E4M3 as 8-bit OCP E4M3
- * codes (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, max 448). */
-typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2 } moe_dtype;
+ * codes (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, max 448).
+ * INT4 (expert weights only): 4-bit two's complement codes q in [-8, 7], eight
+ * consecutive K elements per little-endian 32-bit word, element e of the word in
+ * nibble (e even ? e/2 : 4 + e/2); one bf16 scale s per (weight row, 128 K
+ * elements); the weight is q * s rounded once to bf16 (nearest even). */
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2, MOE_INT4 = 3 } moe_dtype;
 
 /* Return codes (0 or negative). */
 enum {
@@ -213,7 +217,10 @@ MOE_API int moe_align(const int32_t* topk_ids, int T, int topk, int E, int block
  *   router_w [E][H]      act_dtype
  *   w13      [E][2I][H]  w_dtype; rows [0, I) are the gate, rows [I, 2I) the up projection
  *   w2       [E][H][I]   w_dtype
- *   w13_scale, w2_scale  [E] fp32 per-expert dequantisation scales, required iff w_dtype == MOE_E4M3
+ *   w13_scale, w2_scale  MOE_E4M3 weights: [E] fp32 per-expert dequantisation scales;
+ *                        MOE_INT4 weights: bf16 group scales, group-major per expert,
+ *                        [E][H/128][2I] and [E][I/128][H]; ignored otherwise
+ *   (MOE_INT4: w13 [E][2I][H/2] and w2 [E][H][I/2] bytes of packed codes)
  *   out      [T][H]      act_dtype
  *   workspace            >= moe_workspace_size(...) bytes, 256-byte aligned, contents ignored
  * Supported dtype pairs:
@@ -223,6 +230,10 @@ MOE_API int moe_align(const int32_t* topk_ids, int T, int topk, int E, int block
  *                dynamic scale amax/448, the intermediate likewise; the scales are applied
  *                in the GEMM epilogues (page 1, section "Routage backend pour la
  *                quantisation des tenseurs FP8": scaling fused where the data is used)
+ *   (BF16, INT4) tcgen05 kind::f16 path with the codes expanded to bf16 weights in
+ *                shared memory inside the GEMM main loop ("FusedMoE vs MegaMoE",
+ *                section 6.3: quantised expert weights); SWAP_AB orientation only,
+ *                T <= 128, H % 256 == 0 and I % 256 == 0 (else MOE_ERR_UNSUPPORTED)
  *   tensor-core paths need H % 128 == 0 and I % 128 == 0.
  * The intermediate SiLU(gate)*up is stored in bf16 (as a bf16 hi + lo pair in SWAP_AB
  * mode, see moe_options.act_split; fp32 on the fp32 path; e4m3 on the FP8 path);
@@ -235,8 +246,8 @@ MOE_API int moe_align(const int32_t* topk_ids, int T, int topk, int E, int block
  * MOE_ERR_CUDA if the device cannot hold them (e.g. while another kernel occupies SMs
  * under MPS limits). */
 MOE_API int moe_forward(const void* hidden, const void* router_w, const void* w13, const void* w2, int T, int H, int I, int E,
-                int topk, int renorm, moe_dtype act_dtype, moe_dtype w_dtype, const float* w13_scale,
-                const float* w2_scale, void* out, void* workspace, size_t workspace_bytes, const moe_options* opts,
+                int topk, int renorm, moe_dtype act_dtype, moe_dtype w_dtype, const void* w13_scale,
+                const void* w2_scale, void* out, void* workspace, size_t workspace_bytes, const moe_options* opts,
                 moe_stream_t stream);
 
 /* Inverse rotary position embedding fused with per-head FP8 quantisation
@@ -275,7 +286,7 @@ MOE_API int moe_inv_rope_fp8_quant(const void* x, int T, int heads, int head_dim
  * as moe_forward; the multi-kernel sequence always (single_launch = 1 is refused). */
 MOE_API int moe_forward_routed(const void* hidden, const float* topk_w, const int32_t* topk_ids, const void* w13,
                                const void* w2, int T, int H, int I, int E, int topk, moe_dtype act_dtype,
-                               moe_dtype w_dtype, const float* w13_scale, const float* w2_scale, void* out,
+                               moe_dtype w_dtype, const void* w13_scale, const void* w2_scale, void* out,
                                void* workspace, size_t workspace_bytes, const moe_options* opts, moe_stream_t stream);
 
 /* Expert cache ("FusedMoE vs MegaMoE", section 4: MegaMoE keeps expert weights
@@ -345,7 +356,7 @@ MOE_API int moe_cache_lru_plan(int E, int n_slots, int n_calls, int pairs, const
 #define MOE_NOALLOC_MAX_WORKSPACE (32u << 20)
 MOE_API int moe_forward_noalloc(const void* hidden, const void* router_w, const void* w13, const void* w2, int T, int H,
                                 int I, int E, int topk, int renorm, moe_dtype act_dtype, moe_dtype w_dtype,
-                                const float* w13_scale, const float* w2_scale, void* out, const moe_options* opts,
+                                const void* w13_scale, const void* w2_scale, void* out, const moe_options* opts,
                                 moe_stream_t stream);
 
 /* Synchronises `stream`, then reads and clears this device's status word.

@@ -17,7 +17,7 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmoe_gb300.so")
 
-MOE_F32, MOE_BF16, MOE_E4M3 = 0, 1, 2
+MOE_F32, MOE_BF16, MOE_E4M3, MOE_INT4 = 0, 1, 2, 3
 MOE_OK, MOE_ERR_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE = 0, -1, -2, -3
 MOE_ERR_CUDA, MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_DEVICE_INDEX, MOE_ERR_ALIGNMENT = -4, -5, -6, -7
 ORIENT_AUTO, ORIENT_SWAP_AB, ORIENT_TOKEN_MAJOR = 0, 1, 2
@@ -224,14 +224,19 @@ def moe_align(topk_ids: torch.Tensor, E: int, block: int, stream=None, with_coun
 
 
 def moe_forward(hidden: torch.Tensor, router_w: torch.Tensor, w13: torch.Tensor, w2: torch.Tensor, topk: int,
-                renorm: bool, w13_scale=None, w2_scale=None, out=None, workspace=None, options=None, stream=None):
-    """One fused MoE layer forward; returns out [T,H] in the activation dtype."""
+                renorm: bool, w13_scale=None, w2_scale=None, out=None, workspace=None, options=None, stream=None,
+                w_format=None):
+    """One fused MoE layer forward; returns out [T,H] in the activation dtype.
+
+    w_format="int4": w13 [E,2I,H/2] and w2 [E,H,I/2] are packed INT4 codes (uint8) with bf16 group
+    scales, group-major per expert: w13_scale [E,H/128,2I] and w2_scale [E,I/128,H]."""
     T, H = hidden.shape
     E, twoI, H2 = w13.shape
     I = twoI // 2
-    if H2 != H or w2.shape != (E, H, I) or router_w.shape != (E, H):
+    div = 2 if w_format == "int4" else 1
+    if H2 * div != H or w2.shape != (E, H, I // div) or router_w.shape != (E, H):
         raise ValueError("inconsistent shapes")
-    act, wdt = _dt(hidden), _dt(w13)
+    act, wdt = _dt(hidden), (MOE_INT4 if w_format == "int4" else _dt(w13))
     opts = _opts(options)
     need = moe_workspace_size(T, H, I, E, topk, act, wdt, options)
     if workspace is None:

@@ -56,7 +56,7 @@ constexpr int kFusedSplitMaxTokens = 8;
 // moe_options.single_launch == 0 picks the single-launch kernel for eligible shapes.
 constexpr bool kFusedAuto = false;
 
-enum Path { PATH_F32 = 0, PATH_BF16 = 1, PATH_FP8 = 2 };
+enum Path { PATH_F32 = 0, PATH_BF16 = 1, PATH_FP8 = 2, PATH_W4 = 3 };
 
 struct Plan {
   int path = 0;
@@ -123,8 +123,10 @@ static int make_plan(int T, int H, int I, int E, int topk, moe_dtype act, moe_dt
     p.path = PATH_BF16;
   } else if (act == MOE_BF16 && w == MOE_E4M3) {
     p.path = PATH_FP8;
+  } else if (act == MOE_BF16 && w == MOE_INT4) {
+    p.path = PATH_W4;
   } else {
-    return (act > MOE_E4M3 || w > MOE_E4M3 || act < 0 || w < 0) ? MOE_ERR_ARG : MOE_ERR_UNSUPPORTED;
+    return (act > MOE_INT4 || w > MOE_INT4 || act < 0 || w < 0) ? MOE_ERR_ARG : MOE_ERR_UNSUPPORTED;
   }
   const int orient = opts ? opts->orientation : MOE_ORIENT_AUTO;
   if (orient < 0 || orient > 2) return MOE_ERR_ARG;
@@ -133,8 +135,11 @@ static int make_plan(int T, int H, int I, int E, int topk, moe_dtype act, moe_dt
   const long n = (long)T * topk;
   if (p.path != PATH_F32) {
     if (H % 128 || I % 128) return MOE_ERR_UNSUPPORTED;
-    p.swap = orient == MOE_ORIENT_SWAP_AB || (orient == MOE_ORIENT_AUTO && T <= 64);
+    p.swap = orient == MOE_ORIENT_SWAP_AB ||
+             (orient == MOE_ORIENT_AUTO && (T <= 64 || (p.path == PATH_W4 && T <= 128)));
     if (p.swap && T > 256) return MOE_ERR_UNSUPPORTED;
+    // INT4 weights: swap-AB batches of up to 128 tokens, whole 256-row weight tiles
+    if (p.path == PATH_W4 && (!p.swap || T > 128 || H % 256 || I % 256)) return MOE_ERR_UNSUPPORTED;
     const int eb = p.path == PATH_FP8 ? 1 : 2;
     if (p.swap) {
       p.B = 16;
@@ -142,7 +147,9 @@ static int make_plan(int T, int H, int I, int E, int topk, moe_dtype act, moe_dt
       const long act_upper = std::min<long>(E, n);
       const int forced = opts ? opts->split_k : 0;
       if (forced < 0) return MOE_ERR_ARG;
-      const int kbt1 = H * eb / 128, kbt2 = I * eb / 128;
+      // K blocks: 128 bytes of K for bf16 / e4m3 operands, 128-element raw stages (one scale group) for INT4
+      const int kbt1 = p.path == PATH_W4 ? H / 128 : H * eb / 128;
+      const int kbt2 = p.path == PATH_W4 ? I / 128 : I * eb / 128;
       // swap-AB tiles: 128 gate + 128 up rows (GEMM1), 256 rows of w2 (GEMM2)
       p.s1 = choose_splits(act_upper * (I / 128), kbt1, forced, 8);
       p.kb1 = (kbt1 + p.s1 - 1) / p.s1;
@@ -162,7 +169,7 @@ static int make_plan(int T, int H, int I, int E, int topk, moe_dtype act, moe_dt
     }
     // hi/lo intermediate: by default where it is free (swap-AB decode streams
     // weights from HBM; the second MMA only uses idle tensor-core time)
-    p.act_split = p.path == PATH_BF16 && (act_mode == 2 || (act_mode == 0 && p.swap));
+    p.act_split = (p.path == PATH_BF16 || p.path == PATH_W4) && (act_mode == 2 || (act_mode == 0 && p.swap));
     // GEMM1 gathers token rows itself (one tile::gather4 per 4 rows) when the
     // activation tile is short; for wider tiles the per-stage TMA instruction
     // count outweighs the saved kernel, so rows are gathered beforehand.
@@ -194,7 +201,7 @@ static int make_plan(int T, int H, int I, int E, int topk, moe_dtype act, moe_dt
     o = align_up(o + std::max<size_t>(bytes, 1), A);
     return at;
   };
-  const size_t xb = p.path == PATH_F32 ? 4 : (p.path == PATH_BF16 ? 2 : 1);
+  const size_t xb = p.path == PATH_F32 ? 4 : (p.path == PATH_FP8 ? 1 : 2);  // activation element bytes
   p.o_logits = take((size_t)T * E * 4);
   p.o_tw = take((size_t)n * 4);
   p.o_tid = take((size_t)n * 4);
@@ -275,7 +282,7 @@ enum { STEPS_ROUTE = 1, STEPS_EXPERTS = 2, STEPS_ALL = 3 };
 static int forward_steps(const Plan& pl, int steps, const void* hidden, const void* router_w, int E_router,
                          float* logits_override, const float* tw_in, const int32_t* tid_in, const void* w13,
                          const void* w2, int T, int H, int I, int E, int topk, int renorm, moe_dtype act_dtype,
-                         const float* w13_scale, const float* w2_scale, void* out, void* workspace,
+                         const void* w13_scale, const void* w2_scale, void* out, void* workspace,
                          const moe_options* opts, int* st, int sms, cudaStream_t s) {
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* logits = logits_override ? logits_override : reinterpret_cast<float*>(ws + pl.o_logits);
@@ -403,9 +410,11 @@ static int forward_steps(const Plan& pl, int steps, const void* hidden, const vo
     if (o) record(o->stage_end[MOE_STAGE_GEMM2], s);
   } else {
     const bool fp8 = pl.path == PATH_FP8;
+    const bool w4 = pl.path == PATH_W4;
     TcGemmArgs g = {};
     g.swap = pl.swap;
     g.fp8 = fp8;
+    g.w4 = w4;
     g.T = T;
     g.k = topk;
     g.E = E;
@@ -432,7 +441,8 @@ static int forward_steps(const Plan& pl, int steps, const void* hidden, const vo
     g1.n_tiles = I / 128;
     g1.splits = pl.s1;
     g1.kb_per_split = pl.kb1;
-    g1.w_scale = w13_scale;
+    g1.w_scale = static_cast<const float*>(w13_scale);
+    g1.w4_scale = w4 ? w13_scale : nullptr;
     g1.a_amax = amax;
     g1.amax_out = amax + 1;
     void* aint_lo = pl.act_split ? (void*)((uint16_t*)aint + (size_t)cap * I) : nullptr;
@@ -453,7 +463,8 @@ static int forward_steps(const Plan& pl, int steps, const void* hidden, const vo
     if (o) record(o->stage_begin[MOE_STAGE_ACT], s);
     if (pl.s1 > 1)
       MOE_TRY(launch_reduce_act(p1, pl.s1, pl.p1_stride, I, pl.B, n, sorted, eids, meta, cap,
-                                fp8 ? w13_scale : nullptr, amax, fp8 ? 1 : 0, fp8 ? (void*)af32 : aint, aint_lo, amax + 1,
+                                fp8 ? static_cast<const float*>(w13_scale) : nullptr, amax, fp8 ? 1 : 0,
+                                fp8 ? (void*)af32 : aint, aint_lo, amax + 1,
                                 s));
     if (fp8) MOE_TRY(launch_quant_act(af32, I, meta, cap, amax + 1, (uint8_t*)aint, s));
     if (o) record(o->stage_end[MOE_STAGE_ACT], s);
@@ -472,7 +483,8 @@ static int forward_steps(const Plan& pl, int steps, const void* hidden, const vo
     g2.n_tiles = (H + g2.w_tile_rows - 1) / g2.w_tile_rows;
     g2.splits = pl.s2;
     g2.kb_per_split = pl.kb2;
-    g2.w_scale = w2_scale;
+    g2.w_scale = static_cast<const float*>(w2_scale);
+    g2.w4_scale = w4 ? w2_scale : nullptr;
     g2.a_amax = amax + 1;
     g2.out = y;
     g2.out_split_stride = pl.y_stride;
@@ -606,15 +618,15 @@ int moe_align(const int32_t* topk_ids, int T, int topk, int E, int block, int32_
 }
 
 int moe_forward(const void* hidden, const void* router_w, const void* w13, const void* w2, int T, int H, int I, int E,
-                int topk, int renorm, moe_dtype act_dtype, moe_dtype w_dtype, const float* w13_scale,
-                const float* w2_scale, void* out, void* workspace, size_t workspace_bytes, const moe_options* opts,
+                int topk, int renorm, moe_dtype act_dtype, moe_dtype w_dtype, const void* w13_scale,
+                const void* w2_scale, void* out, void* workspace, size_t workspace_bytes, const moe_options* opts,
                 moe_stream_t stream) {
   Plan pl;
   int rc = make_plan(T, H, I, E, topk, act_dtype, w_dtype, opts, &pl);
   if (rc) return rc;
   if (T == 0) return MOE_OK;
   if (!hidden || !router_w || !w13 || !w2 || !out || !workspace) return MOE_ERR_ARG;
-  if (pl.path == PATH_FP8 && (!w13_scale || !w2_scale)) return MOE_ERR_ARG;
+  if ((pl.path == PATH_FP8 || pl.path == PATH_W4) && (!w13_scale || !w2_scale)) return MOE_ERR_ARG;
   if (misaligned(hidden) || misaligned(router_w) || misaligned(w13) || misaligned(w2) || misaligned(out) ||
       misaligned(workspace, 256) || (w13_scale && misaligned(w13_scale, 4)) || (w2_scale && misaligned(w2_scale, 4)))
     return MOE_ERR_ALIGNMENT;
@@ -630,7 +642,7 @@ int moe_forward(const void* hidden, const void* router_w, const void* w13, const
 
 int moe_forward_routed(const void* hidden, const float* topk_w, const int32_t* topk_ids, const void* w13,
                        const void* w2, int T, int H, int I, int E, int topk, moe_dtype act_dtype, moe_dtype w_dtype,
-                       const float* w13_scale, const float* w2_scale, void* out, void* workspace,
+                       const void* w13_scale, const void* w2_scale, void* out, void* workspace,
                        size_t workspace_bytes, const moe_options* opts, moe_stream_t stream) {
   moe_options o = opts ? *opts : moe_options{};
   o.single_launch = 2;  // the single launch routes inside its kernel
@@ -641,7 +653,7 @@ int moe_forward_routed(const void* hidden, const float* topk_w, const int32_t* t
   if (rc) return rc;
   if (T == 0) return MOE_OK;
   if (!hidden || !topk_w || !topk_ids || !w13 || !w2 || !out || !workspace) return MOE_ERR_ARG;
-  if (pl.path == PATH_FP8 && (!w13_scale || !w2_scale)) return MOE_ERR_ARG;
+  if ((pl.path == PATH_FP8 || pl.path == PATH_W4) && (!w13_scale || !w2_scale)) return MOE_ERR_ARG;
   if (misaligned(hidden) || misaligned(topk_w, 4) || misaligned(topk_ids, 4) || misaligned(w13) || misaligned(w2) ||
       misaligned(out) || misaligned(workspace, 256) || (w13_scale && misaligned(w13_scale, 4)) ||
       (w2_scale && misaligned(w2_scale, 4)))

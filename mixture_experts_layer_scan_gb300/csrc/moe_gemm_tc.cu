@@ -128,6 +128,152 @@ __device__ __forceinline__ Tile tile_at(const TcDev& p, int t) {
 // OR of a flag over the 128 epilogue threads (named barrier 1).
 __device__ __forceinline__ bool epi_any(bool v) { return named_bar_any(1, 128, v); }
 
+// The epilogue of one finished tile: thread lrow (an accumulator row, TMEM
+// lane) reads its accumulator columns from tensor memory at tb and stores them
+// in the tile's output format.
+template <bool SWAP, bool FP8, int EPI>
+__device__ __forceinline__ void epi_tile(const TcDev& p, const Tile& d, uint32_t tb, int lrow, float scale,
+                                         int n_pairs, float& amax) {
+  if constexpr (SWAP && (EPI == TC_EPI_G1_BF16 || EPI == TC_EPI_G1_F32AMAX)) {
+    // lane r of D0 / D1: gate / up of intermediate column i = n*128 + r, one column per token
+    const int i = d.n * 128 + lrow;
+    for (int c0 = 0; c0 < d.npad; c0 += 16) {
+      float g[16], u[16];
+      tmem_ld16(tb + (uint32_t)c0, g);
+      tmem_ld16(tb + (uint32_t)(p.d1_col + c0), u);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int c = c0 + j;
+        if (c < d.ntok) {
+          const float a = silu(g[j] * scale) * (u[j] * scale);
+          const size_t o = (size_t)(d.xrow + c) * p.I + i;
+          if constexpr (EPI == TC_EPI_G1_BF16) {
+            const __nv_bfloat16 hi = __float2bfloat16_rn(a);
+            reinterpret_cast<__nv_bfloat16*>(p.out)[o] = hi;
+            if (p.out_lo)
+              reinterpret_cast<__nv_bfloat16*>(p.out_lo)[o] = __float2bfloat16_rn(a - __bfloat162float(hi));
+          } else {
+            reinterpret_cast<float*>(p.out)[o] = a;
+            amax = fmaxf(amax, fabsf(a));
+          }
+        }
+      }
+    }
+  } else if constexpr (SWAP && EPI == TC_EPI_G1_PART) {
+    // raw fp32 split partials P[s][pair][col]: gate at col i, up at col I + i
+    const int i = d.n * 128 + lrow;
+    float* P = reinterpret_cast<float*>(p.out) + (size_t)d.s * p.out_split_stride;
+    for (int c0 = 0; c0 < d.npad; c0 += 16) {
+      float g[16], u[16];
+      tmem_ld16(tb + (uint32_t)c0, g);
+      tmem_ld16(tb + (uint32_t)(p.d1_col + c0), u);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        if (c0 + j < d.ntok) {
+          float* row = P + (size_t)p.sorted[d.xrow + c0 + j] * (2 * p.I);
+          row[i] = g[j];
+          row[p.I + i] = u[j];
+        }
+      }
+    }
+  } else if constexpr (SWAP && EPI == TC_EPI_G2_F32) {
+    // Y[s][pair][h]: h = n*256 + r (D0) and n*256 + 128 + r (D1), pair = sorted[xrow + c]
+    const int h0 = d.n * 256 + lrow;
+    const bool h1_ok = h0 + 128 < p.H;
+    float* Y = reinterpret_cast<float*>(p.out) + (size_t)d.s * p.out_split_stride;
+    for (int c0 = 0; c0 < d.npad; c0 += 16) {
+      float v0[16], v1[16];
+      tmem_ld16(tb + (uint32_t)c0, v0);
+      tmem_ld16(tb + (uint32_t)(p.d1_col + c0), v1);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int c = c0 + j;
+        if (c < d.ntok) {
+          float* row = Y + (size_t)p.sorted[d.xrow + c] * p.H;
+          row[h0] = v0[j] * scale;
+          if (h1_ok) row[h0 + 128] = v1[j] * scale;
+        }
+      }
+    }
+  } else if constexpr (!SWAP && (EPI == TC_EPI_G1_BF16 || EPI == TC_EPI_G1_F32AMAX)) {
+    // row = xrow + lrow; columns [0, wbox) gate, [wbox, 2 wbox) up of i = n*wbox + c
+    const size_t row = (size_t)(d.xrow + lrow);
+    const bool row_valid = p.sorted[row] < n_pairs;
+    for (int c0 = 0; c0 < p.wbox; c0 += 16) {
+      float g[16], u[16];
+      tmem_ld16(tb + (uint32_t)c0, g);
+      tmem_ld16(tb + (uint32_t)(p.wbox + c0), u);
+      float a[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) a[j] = silu(g[j] * scale) * (u[j] * scale);
+      const size_t o = row * p.I + (size_t)d.n * p.wbox + c0;
+      if constexpr (EPI == TC_EPI_G1_BF16) {
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + o);
+        uint32_t hv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) hv[j] = pack_bf16x2(a[2 * j], a[2 * j + 1]);
+        dst[0] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        dst[1] = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+        if (p.out_lo) {
+          uint32_t lv[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            lv[j] = pack_bf16x2(a[2 * j] - bf16_bits_to_f32(hv[j] & 0xffffu),
+                                a[2 * j + 1] - bf16_bits_to_f32(hv[j] >> 16));
+          uint4* dl = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out_lo) + o);
+          dl[0] = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+          dl[1] = make_uint4(lv[4], lv[5], lv[6], lv[7]);
+        }
+      } else {
+        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + o);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) dst[j] = make_float4(a[4 * j], a[4 * j + 1], a[4 * j + 2], a[4 * j + 3]);
+        if (row_valid) {  // padding rows hold token 0's values: keep them out of the amax
+#pragma unroll
+          for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(a[j]));
+        }
+      }
+    }
+  } else if constexpr (EPI == TC_EPI_LOGITS) {
+    const int row = d.xrow + lrow;
+    const int ncols = 2 * p.wbox;
+    for (int c0 = 0; c0 < ncols; c0 += 16) {
+      float v[16];
+      tmem_ld16(tb + (uint32_t)c0, v);
+      if (row < p.T) {
+        float* dst = reinterpret_cast<float*>(p.out) + (size_t)row * p.n_valid;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (c0 + j < p.n_valid) dst[c0 + j] = v[j];
+      }
+    }
+  } else if constexpr (!SWAP && (EPI == TC_EPI_G2_BF16 || EPI == TC_EPI_G2_F32)) {
+    const int f = p.sorted[d.xrow + lrow];
+    const int ncols = 2 * p.wbox;
+    for (int c0 = 0; c0 < ncols; c0 += 16) {
+      float v[16];
+      tmem_ld16(tb + (uint32_t)c0, v);
+      if (f < n_pairs) {
+        const size_t o = (size_t)f * p.H + (size_t)d.n * ncols + c0;
+        if constexpr (EPI == TC_EPI_G2_BF16) {
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + o);
+          dst[0] = make_uint4(pack_bf16x2(v[0] * scale, v[1] * scale), pack_bf16x2(v[2] * scale, v[3] * scale),
+                              pack_bf16x2(v[4] * scale, v[5] * scale), pack_bf16x2(v[6] * scale, v[7] * scale));
+          dst[1] =
+              make_uint4(pack_bf16x2(v[8] * scale, v[9] * scale), pack_bf16x2(v[10] * scale, v[11] * scale),
+                         pack_bf16x2(v[12] * scale, v[13] * scale), pack_bf16x2(v[14] * scale, v[15] * scale));
+        } else {
+          float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + o);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            dst[j] = make_float4(v[4 * j] * scale, v[4 * j + 1] * scale, v[4 * j + 2] * scale,
+                                 v[4 * j + 3] * scale);
+        }
+      }
+    }
+  }
+}
+
 template <bool SWAP, bool FP8, int EPI>
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const TcDev p) {
@@ -356,144 +502,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.buf_cols);
       const float scale = FP8 ? a_scale * p.w_scale[d.e] : 1.0f;
 
-      if constexpr (SWAP && (EPI == TC_EPI_G1_BF16 || EPI == TC_EPI_G1_F32AMAX)) {
-        // lane r of D0 / D1: gate / up of intermediate column i = n*128 + r, one column per token
-        const int i = d.n * 128 + lrow;
-        for (int c0 = 0; c0 < d.npad; c0 += 16) {
-          float g[16], u[16];
-          tmem_ld16(tb + (uint32_t)c0, g);
-          tmem_ld16(tb + (uint32_t)(p.d1_col + c0), u);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int c = c0 + j;
-            if (c < d.ntok) {
-              const float a = silu(g[j] * scale) * (u[j] * scale);
-              const size_t o = (size_t)(d.xrow + c) * p.I + i;
-              if constexpr (EPI == TC_EPI_G1_BF16) {
-                const __nv_bfloat16 hi = __float2bfloat16_rn(a);
-                reinterpret_cast<__nv_bfloat16*>(p.out)[o] = hi;
-                if (p.out_lo)
-                  reinterpret_cast<__nv_bfloat16*>(p.out_lo)[o] = __float2bfloat16_rn(a - __bfloat162float(hi));
-              } else {
-                reinterpret_cast<float*>(p.out)[o] = a;
-                amax = fmaxf(amax, fabsf(a));
-              }
-            }
-          }
-        }
-      } else if constexpr (SWAP && EPI == TC_EPI_G1_PART) {
-        // raw fp32 split partials P[s][pair][col]: gate at col i, up at col I + i
-        const int i = d.n * 128 + lrow;
-        float* P = reinterpret_cast<float*>(p.out) + (size_t)d.s * p.out_split_stride;
-        for (int c0 = 0; c0 < d.npad; c0 += 16) {
-          float g[16], u[16];
-          tmem_ld16(tb + (uint32_t)c0, g);
-          tmem_ld16(tb + (uint32_t)(p.d1_col + c0), u);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            if (c0 + j < d.ntok) {
-              float* row = P + (size_t)p.sorted[d.xrow + c0 + j] * (2 * p.I);
-              row[i] = g[j];
-              row[p.I + i] = u[j];
-            }
-          }
-        }
-      } else if constexpr (SWAP && EPI == TC_EPI_G2_F32) {
-        // Y[s][pair][h]: h = n*256 + r (D0) and n*256 + 128 + r (D1), pair = sorted[xrow + c]
-        const int h0 = d.n * 256 + lrow;
-        const bool h1_ok = h0 + 128 < p.H;
-        float* Y = reinterpret_cast<float*>(p.out) + (size_t)d.s * p.out_split_stride;
-        for (int c0 = 0; c0 < d.npad; c0 += 16) {
-          float v0[16], v1[16];
-          tmem_ld16(tb + (uint32_t)c0, v0);
-          tmem_ld16(tb + (uint32_t)(p.d1_col + c0), v1);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int c = c0 + j;
-            if (c < d.ntok) {
-              float* row = Y + (size_t)p.sorted[d.xrow + c] * p.H;
-              row[h0] = v0[j] * scale;
-              if (h1_ok) row[h0 + 128] = v1[j] * scale;
-            }
-          }
-        }
-      } else if constexpr (!SWAP && (EPI == TC_EPI_G1_BF16 || EPI == TC_EPI_G1_F32AMAX)) {
-        // row = xrow + lrow; columns [0, wbox) gate, [wbox, 2 wbox) up of i = n*wbox + c
-        const size_t row = (size_t)(d.xrow + lrow);
-        const bool row_valid = p.sorted[row] < n_pairs;
-        for (int c0 = 0; c0 < p.wbox; c0 += 16) {
-          float g[16], u[16];
-          tmem_ld16(tb + (uint32_t)c0, g);
-          tmem_ld16(tb + (uint32_t)(p.wbox + c0), u);
-          float a[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) a[j] = silu(g[j] * scale) * (u[j] * scale);
-          const size_t o = row * p.I + (size_t)d.n * p.wbox + c0;
-          if constexpr (EPI == TC_EPI_G1_BF16) {
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + o);
-            uint32_t hv[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) hv[j] = pack_bf16x2(a[2 * j], a[2 * j + 1]);
-            dst[0] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-            dst[1] = make_uint4(hv[4], hv[5], hv[6], hv[7]);
-            if (p.out_lo) {
-              uint32_t lv[8];
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                lv[j] = pack_bf16x2(a[2 * j] - bf16_bits_to_f32(hv[j] & 0xffffu),
-                                    a[2 * j + 1] - bf16_bits_to_f32(hv[j] >> 16));
-              uint4* dl = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out_lo) + o);
-              dl[0] = make_uint4(lv[0], lv[1], lv[2], lv[3]);
-              dl[1] = make_uint4(lv[4], lv[5], lv[6], lv[7]);
-            }
-          } else {
-            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + o);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) dst[j] = make_float4(a[4 * j], a[4 * j + 1], a[4 * j + 2], a[4 * j + 3]);
-            if (row_valid) {  // padding rows hold token 0's values: keep them out of the amax
-#pragma unroll
-              for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(a[j]));
-            }
-          }
-        }
-      } else if constexpr (EPI == TC_EPI_LOGITS) {
-        const int row = d.xrow + lrow;
-        const int ncols = 2 * p.wbox;
-        for (int c0 = 0; c0 < ncols; c0 += 16) {
-          float v[16];
-          tmem_ld16(tb + (uint32_t)c0, v);
-          if (row < p.T) {
-            float* dst = reinterpret_cast<float*>(p.out) + (size_t)row * p.n_valid;
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (c0 + j < p.n_valid) dst[c0 + j] = v[j];
-          }
-        }
-      } else if constexpr (!SWAP && (EPI == TC_EPI_G2_BF16 || EPI == TC_EPI_G2_F32)) {
-        const int f = p.sorted[d.xrow + lrow];
-        const int ncols = 2 * p.wbox;
-        for (int c0 = 0; c0 < ncols; c0 += 16) {
-          float v[16];
-          tmem_ld16(tb + (uint32_t)c0, v);
-          if (f < n_pairs) {
-            const size_t o = (size_t)f * p.H + (size_t)d.n * ncols + c0;
-            if constexpr (EPI == TC_EPI_G2_BF16) {
-              uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + o);
-              dst[0] = make_uint4(pack_bf16x2(v[0] * scale, v[1] * scale), pack_bf16x2(v[2] * scale, v[3] * scale),
-                                  pack_bf16x2(v[4] * scale, v[5] * scale), pack_bf16x2(v[6] * scale, v[7] * scale));
-              dst[1] =
-                  make_uint4(pack_bf16x2(v[8] * scale, v[9] * scale), pack_bf16x2(v[10] * scale, v[11] * scale),
-                             pack_bf16x2(v[12] * scale, v[13] * scale), pack_bf16x2(v[14] * scale, v[15] * scale));
-            } else {
-              float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + o);
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                dst[j] = make_float4(v[4 * j] * scale, v[4 * j + 1] * scale, v[4 * j + 2] * scale,
-                                     v[4 * j + 3] * scale);
-            }
-          }
-        }
-      }
+      epi_tile<SWAP, FP8, EPI>(p, d, tb, lrow, scale, n_pairs, amax);
       tc_fence_before();
       mbar_arrive(bar_tempty + 8 * acc);
       if (++acc == p.nbuf) {
@@ -512,6 +521,333 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // memory once every warp has.  (A CTA-wide bar.sync here, reached by warps
   // coming out of different roles, was seen to release before all warps had
   // arrived.)
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar_exit);
+  if (warp == 1) {
+    mbar_wait_drain(bar_exit, 0, 2 * kWaitLimitNs);
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// INT4 weight-only grouped GEMM (swap-AB): dequantisation in the main loop
+// ---------------------------------------------------------------------------
+// "FusedMoE vs MegaMoE" (zwxr.cn), section 6.3: quantised expert weights
+// (INT4) cut the bytes the fused kernel streams.  Weights are 4-bit codes q in
+// [-8, 7] with one bf16 scale per (weight row, 128 elements of K); the weight
+// the MMA sees is bf16(q * s).  Packing: each 32-bit word holds 8 consecutive
+// K elements, element e in nibble (e even ? e/2 : 4 + e/2), two's complement.
+// Scales are stored group-major per expert ([E][K/128][rows]), so the 256
+// scales of a tile's group are two contiguous 256-byte runs.
+//
+// With thin token batches every MMA re-reads its 128 x 16 weight operand, so
+// dequantised weights staged in shared memory would cost four times the HBM
+// bytes in shared-memory bandwidth (the limit of a first version of this
+// kernel).  The converters therefore write the bf16 weights to tensor memory
+// and the MMA takes its A operand from there; shared memory only carries the
+// packed codes, the scales and the activation tiles.
+//
+// A raw stage is one 128-element group of K for the tile's 256 weight rows:
+// 16 KB of codes (two TMA boxes of 128 rows x 64 bytes, 64-byte swizzle), the
+// activation tiles of its two 64-element K blocks and the 256 scales of the
+// group, all prefetched by the producer.
+// Roles (448 threads):
+//   warp 0      TMA producer: raw stages into their ring
+//   warps 6-13  converters, one weight row per thread (the warp's tensor-memory
+//               lane quarter): expand each K block's codes to bf16 in a
+//               tensor-memory A buffer (32 columns per 128-row half), signal it
+//   warp 1      MMA issuer (tcgen05 kind::f16, A from tensor memory, B = the
+//               activation tile in shared memory, fp32 accumulators)
+//   warps 2-5   epilogue (shared with k_gemm_tc)
+// Tensor memory: accumulator buffers in columns [0, 256), A buffers of 64
+// columns from column 256.
+// Conversion: a nibble n becomes the bf16 bit pattern of 128 + (n ^ 8)
+// = 128 + q + 8 by one logic operation; subtracting 136 is exact; the product
+// with the scale is the one rounding (bf16x2 multiply, nearest even).
+constexpr int kW4Threads = 448;
+constexpr int kW4ConvWarps = 8;
+constexpr int kW4KPerStage = 128;                   // K elements per raw stage (64 bytes of codes per row)
+constexpr uint32_t kW4CodeBytes = 2u * 128u * 64u;  // codes of one raw stage
+constexpr uint32_t kW4ScaleBytes = 1024u;           // 512 bytes of scales, padded to keep stages 1 KB aligned
+constexpr int kW4ABufs = 4;                         // tensor-memory A buffers (one 64-element K block each)
+constexpr uint32_t kW4ACol = 256;                   // first column of the A buffers
+
+// 8 packed codes (one word, nibble order above) times the bf16 scale pair sc -> 4 bf16x2 (K order)
+__device__ __forceinline__ void w4_dequant8(uint32_t w, uint32_t sc, uint32_t* o) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t t = ((w >> (4 * j)) & 0x000F000Fu) ^ 0x43084308u;  // bf16x2 (128 + q + 8)
+    __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&t);
+    v = __hsub2(v, __floats2bfloat162_rn(136.0f, 136.0f));             // q, exact
+    v = __hmul2(v, *reinterpret_cast<const __nv_bfloat162*>(&sc));    // q * s, rounded once
+    o[j] = *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kW4Threads, 1)
+    k_gemm_w4(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+              const __grid_constant__ CUtensorMap tmS, const TcDev p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar_rfull = sbase + p.bar_off;            // raw stage: codes + activations + scales landed
+  const uint32_t bar_rempty = bar_rfull + 8 * kMaxStages;  // raw stage: converted and read by the MMA
+  const uint32_t bar_afull = bar_rempty + 8 * kMaxStages;  // A buffer: bf16 weights stored
+  const uint32_t bar_aempty = bar_afull + 8 * 4;           // A buffer: consumed by the MMA
+  const uint32_t bar_tfull = bar_aempty + 8 * 4;
+  const uint32_t bar_tempty = bar_tfull + 16;
+  const uint32_t bar_drain = bar_tempty + 16;
+  const uint32_t bar_exit = bar_drain + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + p.bar_off + 8 * (2 * kMaxStages + 8 + 6));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(bar_rfull + 8 * s, 1);
+      mbar_init(bar_rempty + 8 * s, kW4ConvWarps + 1);  // the converter warps + the MMA's commit
+    }
+    for (int b = 0; b < kW4ABufs; ++b) {
+      mbar_init(bar_afull + 8 * b, kW4ConvWarps);
+      mbar_init(bar_aempty + 8 * b, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_tfull + 8 * b, 1);
+      mbar_init(bar_tempty + 8 * b, 128);
+    }
+    mbar_init(bar_drain, 1);
+    mbar_init(bar_exit, kW4Threads / 32);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmS);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  tc_fence_before();
+  cta_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  if (!p.early) pdl_wait();
+  const int ntiles = tile_count<true, EPI>(p);
+  const uint32_t xbytes = (uint32_t)p.xbox * 128u;  // one activation part of one 64-element K block
+  const int parts = p.x_lo_rows ? 2 : 1;
+  const uint32_t scale_off = kW4CodeBytes + 2u * (uint32_t)parts * xbytes;  // scales inside a raw stage
+  const int groups_k = p.kb_total;                                          // scale groups per row
+
+  if (warp == 0) {
+    // ---------------- TMA producer: raw stages (codes + activations + scales) ----------------
+    pdl_wait();
+    const int n_pairs = p.T * p.k;
+    const int npp = p.meta[META_NPP];
+    const int groups = p.xbox / 4;  // gather4 groups per activation tile
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      const Tile d = tile_at<true, EPI>(p, t);
+      int rows[4] = {0, 0, 0, 0};  // token rows of this lane's gather group
+      if (p.gather) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = d.xrow + 4 * lane + i;
+          const int f = (r < npp) ? p.sorted[r] : n_pairs;
+          rows[i] = (f < n_pairs) ? f / p.k : 0;  // padding rows read token 0; never stored
+        }
+      }
+      const int r0 = d.n * p.w_tile_rows;  // first weight row of the tile inside its expert
+      for (int rs = d.kb0; rs < d.kb1; ++rs) {
+        if (!mbar_wait_all(bar_rempty + 8 * stage, phase ^ 1u, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sw = sbase + stage * p.stage_bytes;
+        const uint32_t fb = bar_rfull + 8 * stage;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(fb, scale_off + 512u);
+          tma_load_2d(sw, &tmW, rs * 64, d.wr0, fb);
+          tma_load_2d(sw + kW4CodeBytes / 2, &tmW, rs * 64, d.wr0 + p.w_pair_off, fb);
+          tma_load_2d(sw + scale_off, &tmS, r0, d.e * groups_k + rs, fb);
+          tma_load_2d(sw + scale_off + 256u, &tmS, r0 + p.w_pair_off, d.e * groups_k + rs, fb);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const uint32_t dst = sw + kW4CodeBytes + (uint32_t)(j * parts) * xbytes;
+          const int kel = rs * kW4KPerStage + 64 * j;
+          if (p.gather) {
+            if (lane < groups)
+              tma_gather4(dst + (uint32_t)lane * 512u, &tmX, kel, rows[0], rows[1], rows[2], rows[3], fb);
+          } else if (lane == 0) {
+            tma_load_2d(dst, &tmX, kel, d.xrow, fb);
+            if (p.x_lo_rows) tma_load_2d(dst + xbytes, &tmX, kel, d.xrow + p.x_lo_rows, fb);
+          }
+        }
+        __syncwarp();
+        if (++stage == p.stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (lane == 0) pdl_launch_dependents();
+    __syncwarp();
+  } else if (warp >= 6) {
+    // ---------------- converters ----------------
+    pdl_wait();
+    const int q = warp & 3;                // tensor-memory lane quarter of this warp
+    const int h = (warp - 6) >> 2;         // 128-row half: gate / up (GEMM1), rows 0-127 / 128-255 (GEMM2)
+    const int r = q * 32 + lane;           // row inside the half = tensor-memory lane
+    const uint32_t ta = tmem_base + ((uint32_t)(q * 32) << 16) + kW4ACol + (uint32_t)h * 32u;
+    int stage = 0, b = 0;
+    uint32_t phase = 0, bphase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      const Tile d = tile_at<true, EPI>(p, t);
+      for (int rs = d.kb0; rs < d.kb1 && ok; ++rs) {
+        if (!mbar_wait_all(bar_rfull + 8 * stage, phase, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sw = sbase + stage * p.stage_bytes;
+        uint32_t sc;
+        asm volatile("ld.shared.u16 %0, [%1];" : "=r"(sc) : "r"(sw + scale_off + (uint32_t)(h * 128 + r) * 2u));
+        sc |= sc << 16;  // bf16x2 (s, s)
+        const uint32_t src = sw + (uint32_t)h * (kW4CodeBytes / 2) + (uint32_t)r * 64u;
+        for (int j = 0; j < 2; ++j) {
+          uint32_t wv[8];
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {  // 16-byte chunks 2j, 2j+1 of the 64-byte row, 64-byte swizzle
+            const uint32_t chunk = (uint32_t)(2 * j + c) ^ (uint32_t)((r >> 1) & 3);
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(wv[4 * c]), "=r"(wv[4 * c + 1]), "=r"(wv[4 * c + 2]), "=r"(wv[4 * c + 3])
+                         : "r"(src + chunk * 16u));
+          }
+          uint32_t a[32];  // column m: K elements 2m, 2m+1 of this K block
+#pragma unroll
+          for (int w8 = 0; w8 < 8; ++w8) w4_dequant8(wv[w8], sc, a + 4 * w8);
+          if (!mbar_wait_all(bar_aempty + 8 * b, bphase ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          tmem_st32(ta + (uint32_t)b * 64u, a);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_afull + 8 * b);
+          if (++b == kW4ABufs) {
+            b = 0;
+            bphase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_rempty + 8 * stage);  // codes and scales of this stage read
+        if (++stage == p.stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    pdl_wait();
+    int stage = 0, b = 0, acc = 0;
+    uint32_t phase = 0, bphase = 0, acc_phase = 0;
+    bool ok = true, any = false;
+    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      const Tile d = tile_at<true, EPI>(p, t);
+      const uint32_t idesc = idesc_make(128, d.npad, false);
+      if (!mbar_wait_all(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t dt = tmem_base + (uint32_t)(acc * p.buf_cols);
+      for (int rs = d.kb0; rs < d.kb1 && ok; ++rs) {
+        if (!mbar_wait_all(bar_rfull + 8 * stage, phase, abort_flag, p.status)) {  // activations landed
+          ok = false;
+          break;
+        }
+        const uint32_t sw = sbase + stage * p.stage_bytes;
+        for (int j = 0; j < 2; ++j) {
+          if (!mbar_wait_all(bar_afull + 8 * b, bphase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t ab = tmem_base + kW4ACol + (uint32_t)b * 64u;
+            const uint32_t bx = sw + kW4CodeBytes + (uint32_t)(j * parts) * xbytes;
+            for (int part = 0; part < parts; ++part) {
+              const uint32_t sxp = bx + (uint32_t)part * xbytes;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t acc_in = (part > 0 || rs > d.kb0 || j > 0 || kk > 0) ? 1u : 0u;
+                const uint64_t bdesc = sdesc_k_sw128(sxp + kk * 32);
+                tc_mma_ts(dt, ab + (uint32_t)kk * 8u, bdesc, idesc, acc_in);
+                tc_mma_ts(dt + (uint32_t)p.d1_col, ab + 32u + (uint32_t)kk * 8u, bdesc, idesc, acc_in);
+              }
+            }
+            tc_commit(bar_aempty + 8 * b);
+            if (j == 1) tc_commit(bar_rempty + 8 * stage);  // the stage's activations are read
+          }
+          __syncwarp();
+          any = true;
+          if (++b == kW4ABufs) {
+            b = 0;
+            bphase ^= 1u;
+          }
+        }
+        if (++stage == p.stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) tc_commit(bar_tfull + 8 * acc);
+      __syncwarp();
+      if (++acc == p.nbuf) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (!ok && any) {
+      if (lane == 0) tc_commit(bar_drain);
+      __syncwarp();
+      mbar_wait_drain(bar_drain, 0, 100000000ull);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    pdl_wait();
+    const int q = warp & 3;
+    const int lrow = q * 32 + lane;
+    float amax = 0.0f;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    const int n_pairs = p.T * p.k;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+      const Tile d = tile_at<true, EPI>(p, t);
+      const bool ok = mbar_wait_all(bar_tfull + 8 * acc, acc_phase, abort_flag, p.status);
+      if (epi_any(!ok)) break;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.buf_cols);
+      epi_tile<true, false, EPI>(p, d, tb, lrow, 1.0f, n_pairs, amax);
+      tc_fence_before();
+      mbar_arrive(bar_tempty + 8 * acc);
+      if (++acc == p.nbuf) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
   tc_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive(bar_exit);
@@ -572,20 +908,106 @@ static EncodeTiledFn encode_fn() {
 }
 
 // 2-D K-major tensor [rows][K] of 1- or 2-byte elements, box = 128 bytes of K x box_rows, 128-byte swizzle.
-bool make_tensor_map_2d(CUtensorMap* m, const void* base, int elem_bytes, uint64_t K, uint64_t rows, uint32_t box_rows) {
+bool make_tensor_map_2d(CUtensorMap* m, const void* base, int elem_bytes, uint64_t K, uint64_t rows, uint32_t box_rows,
+                        uint32_t box_bytes) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
+  if (box_bytes != 128 && box_bytes != 64 && box_bytes != 256) return false;
   const cuuint64_t dims[2] = {K, rows};
   const cuuint64_t strides[1] = {K * (uint64_t)elem_bytes};
-  const cuuint32_t box[2] = {(cuuint32_t)(128 / elem_bytes), box_rows};
+  const cuuint32_t box[2] = {(cuuint32_t)(box_bytes / elem_bytes), box_rows};
   const cuuint32_t estr[2] = {1, 1};
   const CUtensorMapDataType dt = elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                             : (box_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE),
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int EPI>
+static cudaError_t launch_w4_inst(const CUtensorMap& mw, const CUtensorMap& mx, const CUtensorMap& ms, const TcDev& p,
+                                  int grid, size_t smem, cudaStream_t s) {
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  auto kern = k_gemm_w4<EPI>;
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  return launch_pdl(kern, dim3(grid), dim3(kW4Threads), smem, s, mw, mx, ms, p);
+}
+
+// INT4 weights: swap-AB only; K splits and tile K ranges in raw stages of 128 elements.
+static cudaError_t launch_gemm_w4(const TcGemmArgs& a, cudaStream_t s) {
+  if (!a.swap || a.fp8 || a.K % kW4KPerStage || a.xbox > 128 || a.xbox % 16 || !a.w4_scale)
+    return cudaErrorInvalidValue;
+  CUtensorMap mw, mx, ms;
+  if (!make_tensor_map_2d(&mw, a.W, 1, (uint64_t)a.K / 2, (uint64_t)a.E * a.w_rows_per_expert, 128u, 64u))
+    return cudaErrorInvalidValue;
+  // scales [E][K/128][rows]: boxes of 128 consecutive rows of one group
+  if (!make_tensor_map_2d(&ms, a.w4_scale, 2, (uint64_t)a.w_rows_per_expert, (uint64_t)a.E * (a.K / 128), 1u, 256u))
+    return cudaErrorInvalidValue;
+  if (a.gather) {
+    if (a.xbox % 4 || a.xbox > 128 || a.x_lo_rows) return cudaErrorInvalidValue;
+    if (!make_tensor_map_2d(&mx, a.X, 2, (uint64_t)a.K, (uint64_t)a.T, 1u)) return cudaErrorInvalidValue;
+  } else if (!make_tensor_map_2d(&mx, a.X, 2, (uint64_t)a.K, (uint64_t)a.cap + (uint64_t)a.x_lo_rows,
+                                 (uint32_t)a.xbox)) {
+    return cudaErrorInvalidValue;
+  }
+  TcDev p = {};
+  p.epi = a.epi;
+  p.T = a.T;
+  p.k = a.k;
+  p.E = a.E;
+  p.I = a.I;
+  p.H = a.H;
+  p.kb_total = a.K / kW4KPerStage;
+  p.kb_per_split = a.kb_per_split;
+  p.splits = a.splits;
+  p.n_tiles = a.n_tiles;
+  p.w_rows_per_expert = a.w_rows_per_expert;
+  p.w_pair_off = a.w_pair_off;
+  p.w_tile_rows = a.w_tile_rows;
+  p.wbox = a.wbox;
+  p.xbox = a.xbox;
+  p.sorted = a.sorted;
+  p.eids = a.eids;
+  p.meta = a.meta;
+  p.out = a.out;
+  p.gather = a.gather ? 1 : 0;
+  p.early = a.early ? 1 : 0;
+  p.out_lo = a.out_lo;
+  p.x_lo_rows = a.x_lo_rows;
+  p.out_split_stride = a.out_split_stride;
+  p.status = a.status;
+  // accumulators: D0 and D1 of xbox columns each; two buffers while they fit below the A buffers
+  p.d1_col = a.xbox;
+  p.buf_cols = 2 * a.xbox;
+  p.nbuf = 2 * p.buf_cols <= (int)kW4ACol ? 2 : 1;
+  const int parts = a.x_lo_rows ? 2 : 1;
+  // codes + two K blocks of activations + scales
+  p.stage_bytes = kW4CodeBytes + 2u * (uint32_t)a.xbox * 128u * parts + kW4ScaleBytes;
+  const uint32_t bar_bytes = 8 * (2 * kMaxStages + 8 + 6) + 16;
+  const uint32_t total = 227 * 1024 - 1024 - bar_bytes;
+  int stages = (int)(total / p.stage_bytes);
+  if (stages > kMaxStages) stages = kMaxStages;
+  if (stages < 2) return cudaErrorInvalidValue;
+  p.stages = stages;
+  p.bar_off = (uint32_t)stages * p.stage_bytes;
+  const size_t smem = 1024 + (size_t)p.bar_off + bar_bytes;
+  const long upper = (long)std::min(a.E, a.T * a.k) * a.n_tiles * a.splits;
+  int grid = (int)std::min<long>(upper, a.num_sms);
+  if (grid < 1) grid = 1;
+  if (a.epi == TC_EPI_G1_BF16) return launch_w4_inst<TC_EPI_G1_BF16>(mw, mx, ms, p, grid, smem, s);
+  if (a.epi == TC_EPI_G1_PART) return launch_w4_inst<TC_EPI_G1_PART>(mw, mx, ms, p, grid, smem, s);
+  if (a.epi == TC_EPI_G2_F32) return launch_w4_inst<TC_EPI_G2_F32>(mw, mx, ms, p, grid, smem, s);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s) {
+  if (a.w4) return launch_gemm_w4(a, s);
   const int eb = a.fp8 ? 1 : 2;
   CUtensorMap mw, mx;
   if (!make_tensor_map_2d(&mw, a.W, eb, (uint64_t)a.K, (uint64_t)a.E * a.w_rows_per_expert, (uint32_t)a.wbox))

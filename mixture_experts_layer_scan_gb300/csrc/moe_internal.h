@@ -109,13 +109,16 @@ struct TcGemmArgs {
   unsigned* amax_out;       // amax bits of the produced intermediate (FP8 GEMM1)
   int* status;
   int num_sms;
+  bool w4;                  // INT4 weight codes (swap-AB), dequantised to bf16 in the main loop
+  const void* w4_scale;     // bf16 group scales [E][K / 128][w_rows_per_expert]
 };
 cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s);
 
-// 2-D K-major tensor map [rows][K] of 1- or 2-byte elements: box of 128 bytes
-// of K x box_rows, 128-byte swizzle.
+// 2-D K-major tensor map [rows][K] of 1- or 2-byte elements: box of box_bytes
+// of K x box_rows; 128 and 64 bytes are swizzled with the same span, 256 bytes
+// are not swizzled.
 bool make_tensor_map_2d(CUtensorMap* m, const void* base, int elem_bytes, uint64_t K, uint64_t rows,
-                        uint32_t box_rows);
+                        uint32_t box_rows, uint32_t box_bytes = 128);
 
 // ---- inverse rotary embedding + per-head FP8 quantisation ----------------------------
 cudaError_t launch_inv_rope_fp8(const void* X, int T, int heads, int D, int R, const int32_t* pos,

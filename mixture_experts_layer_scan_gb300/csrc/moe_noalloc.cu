@@ -45,7 +45,7 @@ void* static_scratch_for_current_device() {
 
 extern "C" int moe_forward_noalloc(const void* hidden, const void* router_w, const void* w13, const void* w2, int T,
                                    int H, int I, int E, int topk, int renorm, moe_dtype act_dtype, moe_dtype w_dtype,
-                                   const float* w13_scale, const float* w2_scale, void* out,
+                                   const void* w13_scale, const void* w2_scale, void* out,
                                    const moe_options* opts, moe_stream_t stream) {
   size_t need = 0;
   const int rc = moe_workspace_size(T, H, I, E, topk, act_dtype, w_dtype, opts, &need);

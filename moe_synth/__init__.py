@@ -55,6 +55,7 @@ def spec(name: str, T: Optional[int] = None, **over) -> LayerSpec:
         "mixtral_decode": dict(T=64, H=4096, E=8, I=14336, k=2, renorm=True, seed=1235),
         "fine_decode": dict(T=64, H=2048, E=128, I=768, k=8, renorm=True, seed=1236, router="zipf"),
         "fp8_decode": dict(T=64, H=4096, E=64, I=8192, k=8, renorm=False, w="e4m3", seed=1237),
+        "int4_decode": dict(T=64, H=4096, E=8, I=14336, k=2, renorm=True, w="int4", seed=1239),
         "prefill": dict(T=8192, H=4096, E=64, I=2048, k=8, renorm=True, seed=1238),
         "prefill_hot": dict(T=8192, H=4096, E=64, I=2048, k=8, renorm=True, seed=1238, router="hot"),
     }[name]
@@ -65,7 +66,8 @@ def spec(name: str, T: Optional[int] = None, **over) -> LayerSpec:
     return LayerSpec(name=name, **base)
 
 
-DECODE_M = {"mixtral_decode": (1, 4, 16, 64), "fine_decode": (1, 8, 32, 64), "fp8_decode": (1, 16, 64)}
+DECODE_M = {"mixtral_decode": (1, 4, 16, 64), "fine_decode": (1, 8, 32, 64), "fp8_decode": (1, 16, 64),
+            "int4_decode": (1, 16, 64)}
 
 
 def _gen(seed: int, device) -> torch.Generator:
@@ -110,6 +112,26 @@ def _structure_columns(sp: LayerSpec, X: torch.Tensor, rows: Optional[torch.Tens
             X[rows, H - 2] = col[rows]
 
 
+# Nibble of element e (0..7) inside a 32-bit word of 8 consecutive K elements (the INT4 storage format).
+INT4_NIBBLE_OF = (0, 4, 1, 5, 2, 6, 3, 7)
+
+
+def _int4_encode_groupwise(w: torch.Tensor):
+    """Stand-in for an offline INT4 weight quantiser (the kind AWQ / GPTQ produce, here without
+    calibration): a bf16 scale per (row, 128 K elements) = max |w| / 7, codes round(w / s) clamped to
+    [-8, 7]; returns (packed codes uint8 [rows, K/2], scales bf16 [rows, K/128])."""
+    rows, K = w.shape
+    wg = w.float().reshape(rows, K // 128, 128)
+    s = (wg.abs().amax(dim=2) / 7.0).clamp_min(1e-8).to(torch.bfloat16)
+    q = torch.round(wg / s.float()[:, :, None]).clamp_(-8, 7).to(torch.int32).reshape(rows, K // 8, 8)
+    nib = torch.tensor(INT4_NIBBLE_OF, dtype=torch.int32, device=w.device)
+    word = torch.zeros(rows, K // 8, dtype=torch.int64, device=w.device)
+    for el in range(8):
+        word |= ((q[:, :, el] & 0xF).to(torch.int64) << (4 * int(nib[el])))
+    b = torch.stack([(word >> (8 * i)) & 0xFF for i in range(4)], dim=2).to(torch.uint8)
+    return b.reshape(rows, K // 2), s
+
+
 def make_layer(sp: LayerSpec, device="cpu", weights: bool = True) -> dict:
     """Draw one synthetic layer + token batch.  Deterministic in (spec, device)."""
     dev = torch.device(device)
@@ -144,7 +166,19 @@ def make_layer(sp: LayerSpec, device="cpu", weights: bool = True) -> dict:
     }
     if not weights:
         return out
-    if sp.w == "e4m3":
+    if sp.w == "int4":
+        W13 = torch.empty(E, 2 * I, H // 2, dtype=torch.uint8, device=dev)
+        W2 = torch.empty(E, H, I // 2, dtype=torch.uint8, device=dev)
+        # scales group-major per expert: [E][K/128][rows]
+        s13 = torch.empty(E, H // 128, 2 * I, dtype=torch.bfloat16, device=dev)
+        s2 = torch.empty(E, I // 128, H, dtype=torch.bfloat16, device=dev)
+        for e in range(E):
+            W13[e], s = _int4_encode_groupwise(torch.randn(2 * I, H, generator=g, device=dev) * sp.w_std)
+            s13[e] = s.t()
+            W2[e], s = _int4_encode_groupwise(torch.randn(H, I, generator=g, device=dev) * sp.w_std)
+            s2[e] = s.t()
+        out.update(W13=W13, W2=W2, w13_scale=s13, w2_scale=s2)
+    elif sp.w == "e4m3":
         W13 = torch.empty(E, 2 * I, H, dtype=torch.float8_e4m3fn, device=dev)
         W2 = torch.empty(E, H, I, dtype=torch.float8_e4m3fn, device=dev)
         s13 = torch.empty(E, dtype=torch.float32, device=dev)

@@ -17,7 +17,7 @@ import threading
 
 import numpy as np
 
-F32, BF16, E4M3 = 0, 1, 2
+F32, BF16, E4M3, INT4 = 0, 1, 2, 3
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "moe_oracle.c")
@@ -190,24 +190,33 @@ def align(ids, E: int, B: int):
     return sorted_ids[:n].copy(), expert_ids[: n // B].copy(), n, counts
 
 
-def moe_forward(X, Wr, W13, W2, topk_k: int, renorm: bool, w13_scale=None, w2_scale=None, tokens=None):
+def moe_forward(X, Wr, W13, W2, topk_k: int, renorm: bool, w13_scale=None, w2_scale=None, tokens=None,
+                w_format=None):
     """Layer output (float64 [n,H]) plus the routing of all T tokens and the FP8 activation scales.
 
     Returns dict(out, ids, w, act_scales).  ``tokens`` selects a subset of output rows.
+    ``w_format="int4"``: W13 [E,2I,H/2] and W2 [E,H,I/2] are packed INT4 codes (uint8) and the scales
+    bf16 group scales, group-major per expert: [E,H/128,2I] and [E,I/128,H].
     """
     x, wr, w13, w2 = _np(X), _np(Wr), _np(W13), _np(W2)
     adt, wdt = _dtype_code(X), _dtype_code(W13)
     T, H = x.shape
     E = wr.shape[0]
     I = w13.shape[1] // 2
+    if w_format == "int4":
+        wdt = INT4
+        s13 = np.ascontiguousarray(_np(w13_scale), dtype=np.uint16)
+        s2 = np.ascontiguousarray(_np(w2_scale), dtype=np.uint16)
+        w13_scale = w2_scale = None
     tok = None if tokens is None else np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
     n = T if tok is None else tok.shape[0]
     out = np.empty((n, H), dtype=np.float64)
     ids = np.empty((T, topk_k), dtype=np.int32)
     w = np.empty((T, topk_k), dtype=np.float64)
     scales = np.zeros(2, dtype=np.float32)
-    s13 = None if w13_scale is None else np.ascontiguousarray(_np(w13_scale), dtype=np.float32)
-    s2 = None if w2_scale is None else np.ascontiguousarray(_np(w2_scale), dtype=np.float32)
+    if w_format != "int4":
+        s13 = None if w13_scale is None else np.ascontiguousarray(_np(w13_scale), dtype=np.float32)
+        s2 = None if w2_scale is None else np.ascontiguousarray(_np(w2_scale), dtype=np.float32)
     rc = _load().oracle_moe_forward(
         _ptr(x), _ptr(wr), _ptr(w13), _ptr(w2), adt, wdt, T, H, I, E, int(topk_k), int(bool(renorm)),
         None if s13 is None else _ptr(s13), None if s2 is None else _ptr(s2),

@@ -44,7 +44,7 @@
 #include <omp.h>
 #endif
 
-enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_E4M3 = 2 };
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_E4M3 = 2, ORC_INT4 = 3 };
 
 /* ------------------------------------------------------------------------ */
 /* Number formats                                                            */
@@ -128,6 +128,39 @@ static double load_elem(const void* p, int dtype, size_t i) {
 }
 
 static float load_f32(const void* p, int dtype, size_t i) { return (float)load_elem(p, dtype, i); }
+
+/*
+ * INT4 weight-only experts ("FusedMoE vs MegaMoE" (zwxr.cn), section 6.3:
+ * quantised expert weights with the fused kernel; the pages give no format).
+ * Reading: a code q in [-8, 7] per weight (two's complement nibble) and one
+ * bf16 scale s per (weight row, 128 consecutive K elements); the weight is
+ * q * s rounded once to bf16 (nearest even).  Packing: each little-endian
+ * 32-bit word holds 8 consecutive K elements, element e of the word in nibble
+ * (e even ? e / 2 : 4 + e / 2).  K is the row length (H for w13, I for w2).
+ * Scales are group-major per expert: [E][K/128][rows of one expert].
+ */
+static double load_w4(const void* codes, const void* scales, int ex, int r, int rows, int K, int k) {
+  const size_t row = (size_t)ex * rows + r;
+  const uint8_t* c = (const uint8_t*)codes + (row * (size_t)(K / 8) + (size_t)(k / 8)) * 4;
+  const uint32_t word = (uint32_t)c[0] | ((uint32_t)c[1] << 8) | ((uint32_t)c[2] << 16) | ((uint32_t)c[3] << 24);
+  const int e = k % 8;
+  const int nib = (e % 2 == 0) ? e / 2 : 4 + e / 2;
+  int q = (int)((word >> (4 * nib)) & 0xFu);
+  if (q >= 8) q -= 16;
+  const size_t si = ((size_t)ex * (K / 128) + (size_t)(k / 128)) * rows + r;
+  const double s = oracle_bf16_to_f64(((const uint16_t*)scales)[si]);
+  return oracle_bf16_to_f64(oracle_f32_to_bf16((float)(q * s)));  /* q * s is exact in fp32 */
+}
+
+/* weight w13[e][r][h] / w2[e][h][i] of the stored format */
+static double w13_at(const void* W13, int w_dtype, const void* s13, int e, int r, int I, int H, int h) {
+  const size_t row = (size_t)e * 2 * I + r;
+  return w_dtype == ORC_INT4 ? load_w4(W13, s13, e, r, 2 * I, H, h) : load_elem(W13, w_dtype, row * H + h);
+}
+static double w2_at(const void* W2, int w_dtype, const void* s2, int e, int h, int H, int I, int i) {
+  const size_t row = (size_t)e * H + h;
+  return w_dtype == ORC_INT4 ? load_w4(W2, s2, e, h, H, I, i) : load_elem(W2, w_dtype, row * I + i);
+}
 
 double oracle_silu(double z) { return z / (1.0 + exp(-z)); }
 
@@ -239,11 +272,15 @@ uint8_t oracle_e4m3_quant(float v, float scale) { return oracle_f32_to_e4m3_satf
 /* Returns 0, or a negative value on bad arguments.                          */
 /* ------------------------------------------------------------------------ */
 int oracle_moe_forward(const void* X, const void* Wr, const void* W13, const void* W2, int act_dtype, int w_dtype,
-                       int T, int H, int I, int E, int k, int renorm, const float* w13_scale, const float* w2_scale,
+                       int T, int H, int I, int E, int k, int renorm, const void* w13_scale_in, const void* w2_scale_in,
                        const int32_t* tokens, int n_tokens, double* out, int32_t* ids_out, double* w_out,
                        float* act_scales_out) {
   if (T < 0 || H < 1 || I < 1 || E < 1 || k < 1 || k > E) return -1;
   if (act_dtype != ORC_F32 && act_dtype != ORC_BF16) return -1;
+  /* scales: [E] fp32 for e4m3 weights; bf16 [E][H/128][2I] and [E][I/128][H] for INT4 */
+  const float* w13_scale = (const float*)w13_scale_in;
+  const float* w2_scale = (const float*)w2_scale_in;
+  if (w_dtype == ORC_INT4 && (!w13_scale_in || !w2_scale_in || H % 128 || I % 128 || H % 8 || I % 8)) return -1;
   const int fp8 = (w_dtype == ORC_E4M3);
   if (fp8 && (!w13_scale || !w2_scale || act_dtype != ORC_BF16)) return -1;
   if (!tokens) n_tokens = T;
@@ -272,20 +309,18 @@ int oracle_moe_forward(const void* X, const void* Wr, const void* W13, const voi
         for (int h = 0; h < H; ++h) { x[h] = load_elem(X, act_dtype, (size_t)t * H + h); o[h] = 0.0; }
         for (int j = 0; j < k; ++j) {
           const int e = ids[(size_t)t * k + j];
-          const size_t w13_base = (size_t)e * 2 * I * H;
           for (int i = 0; i < I; ++i) {
             double g = 0.0, u = 0.0;
             for (int h = 0; h < H; ++h) {
-              g += load_elem(W13, w_dtype, w13_base + (size_t)i * H + h) * x[h];
-              u += load_elem(W13, w_dtype, w13_base + (size_t)(I + i) * H + h) * x[h];
+              g += w13_at(W13, w_dtype, w13_scale_in, e, i, I, H, h) * x[h];
+              u += w13_at(W13, w_dtype, w13_scale_in, e, I + i, I, H, h) * x[h];
             }
             a[i] = oracle_silu(g) * u;
           }
-          const size_t w2_base = (size_t)e * H * I;
           const double wj = w[(size_t)t * k + j];
           for (int h = 0; h < H; ++h) {
             double y = 0.0;
-            for (int i = 0; i < I; ++i) y += load_elem(W2, w_dtype, w2_base + (size_t)h * I + i) * a[i];
+            for (int i = 0; i < I; ++i) y += w2_at(W2, w_dtype, w2_scale_in, e, h, H, I, i) * a[i];
             o[h] += wj * y;
           }
         }
