@@ -252,9 +252,33 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
       : "memory");
 }
 
+// The 8 MMAs of one 64-element K block of a 256-row swap-AB tile, A from
+// tensor memory, issued as one block: D0 (+)= A[a .. a+31] x B and
+// D1 (+)= A[a+32 .. a+63] x B, four K steps of 16 (8 columns of A, 32 bytes of
+// the 128-byte-swizzled B rows each).  accumulate = 0 starts both accumulators.
+__device__ __forceinline__ void tc_mma_ts_kblock(uint32_t d0, uint32_t d1, uint32_t a, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t.reg .b32 a1, a2, a3, a4, a5, a6, a7;\n\t.reg .b64 b1, b2, b3;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\tsetp.ne.b32 t, %4, 0;\n\t"
+      "add.u32 a1, %2, 32;\n\tadd.u32 a2, %2, 8;\n\tadd.u32 a3, %2, 40;\n\tadd.u32 a4, %2, 16;\n\t"
+      "add.u32 a5, %2, 48;\n\tadd.u32 a6, %2, 24;\n\tadd.u32 a7, %2, 56;\n\t"
+      "add.u64 b1, %3, 2;\n\tadd.u64 b2, %3, 4;\n\tadd.u64 b3, %3, 6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %3, %4, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], [a1], %3, %4, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b1, %4, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], [a3], b1, %4, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a4], b2, %4, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], [a5], b2, %4, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a6], b3, %4, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], [a7], b3, %4, t;\n\t}" ::"r"(d0),
+      "r"(d1), "r"(a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // 32 registers per thread -> 32 lanes x 32 consecutive 32-bit columns of tensor
-// memory, complete (visible to the tensor core) on return.
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+// memory; complete (visible to the tensor core) after tmem_wait_st().
+__device__ __forceinline__ void tmem_st32_nowait(uint32_t taddr, const uint32_t* r) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
       "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
@@ -263,8 +287,8 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
       "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Arrive once on an mbarrier when every tcgen05 op issued so far by this thread completes.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {

@@ -557,13 +557,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // Roles (448 threads):
 //   warp 0      TMA producer: raw stages into their ring
 //   warps 6-13  converters, one weight row per thread (the warp's tensor-memory
-//               lane quarter): expand each K block's codes to bf16 in a
-//               tensor-memory A buffer (32 columns per 128-row half), signal it
+//               lane quarter): expand a raw stage's codes to bf16 in a
+//               tensor-memory A buffer (per K block j and 128-row half h, the 32
+//               columns from 64 j + 32 h), signal it
 //   warp 1      MMA issuer (tcgen05 kind::f16, A from tensor memory, B = the
 //               activation tile in shared memory, fp32 accumulators)
 //   warps 2-5   epilogue (shared with k_gemm_tc)
-// Tensor memory: accumulator buffers in columns [0, 256), A buffers of 64
-// columns from column 256.
+// Tensor memory: accumulator buffers in columns [0, 256), A buffers of 128
+// columns from column 256.  The MMA issuer synchronises once per raw stage
+// (16 MMAs, 32 with the hi/lo activation split): with thin token tiles the
+// issuing thread, which shares its scheduler with converter warps, is the
+// critical path, so it runs as few instructions per MMA as possible.
 // Conversion: a nibble n becomes the bf16 bit pattern of 128 + (n ^ 8)
 // = 128 + q + 8 by one logic operation; subtracting 136 is exact; the product
 // with the scale is the one rounding (bf16x2 multiply, nearest even).
@@ -572,7 +576,7 @@ constexpr int kW4ConvWarps = 8;
 constexpr int kW4KPerStage = 128;                   // K elements per raw stage (64 bytes of codes per row)
 constexpr uint32_t kW4CodeBytes = 2u * 128u * 64u;  // codes of one raw stage
 constexpr uint32_t kW4ScaleBytes = 1024u;           // 512 bytes of scales, padded to keep stages 1 KB aligned
-constexpr int kW4ABufs = 4;                         // tensor-memory A buffers (one 64-element K block each)
+constexpr int kW4ABufs = 2;                         // tensor-memory A buffers (one raw stage, 128 columns, each)
 constexpr uint32_t kW4ACol = 256;                   // first column of the A buffers
 
 // 8 packed codes (one word, nibble order above) times the bf16 scale pair sc -> 4 bf16x2 (K order)
@@ -718,34 +722,35 @@ __global__ void __launch_bounds__(kW4Threads, 1)
         asm volatile("ld.shared.u16 %0, [%1];" : "=r"(sc) : "r"(sw + scale_off + (uint32_t)(h * 128 + r) * 2u));
         sc |= sc << 16;  // bf16x2 (s, s)
         const uint32_t src = sw + (uint32_t)h * (kW4CodeBytes / 2) + (uint32_t)r * 64u;
-        for (int j = 0; j < 2; ++j) {
-          uint32_t wv[8];
+        uint32_t wv[16];  // the row's 128 codes: 16-byte chunk c of the 64-byte row sits at chunk c ^ ((r >> 1) & 3)
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {  // 16-byte chunks 2j, 2j+1 of the 64-byte row, 64-byte swizzle
-            const uint32_t chunk = (uint32_t)(2 * j + c) ^ (uint32_t)((r >> 1) & 3);
-            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(wv[4 * c]), "=r"(wv[4 * c + 1]), "=r"(wv[4 * c + 2]), "=r"(wv[4 * c + 3])
-                         : "r"(src + chunk * 16u));
-          }
-          uint32_t a[32];  // column m: K elements 2m, 2m+1 of this K block
-#pragma unroll
-          for (int w8 = 0; w8 < 8; ++w8) w4_dequant8(wv[w8], sc, a + 4 * w8);
-          if (!mbar_wait_all(bar_aempty + 8 * b, bphase ^ 1u, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          tmem_st32(ta + (uint32_t)b * 64u, a);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_afull + 8 * b);
-          if (++b == kW4ABufs) {
-            b = 0;
-            bphase ^= 1u;
-          }
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t chunk = (uint32_t)c ^ (uint32_t)((r >> 1) & 3);
+          asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(wv[4 * c]), "=r"(wv[4 * c + 1]), "=r"(wv[4 * c + 2]), "=r"(wv[4 * c + 3])
+                       : "r"(src + chunk * 16u));
         }
-        if (!ok) break;
+        uint32_t a0[32], a1[32];  // K blocks 0 and 1; column m: K elements 2m, 2m+1 of the block
+#pragma unroll
+        for (int w8 = 0; w8 < 8; ++w8) {
+          w4_dequant8(wv[w8], sc, a0 + 4 * w8);
+          w4_dequant8(wv[8 + w8], sc, a1 + 4 * w8);
+        }
+        if (!mbar_wait_all(bar_aempty + 8 * b, bphase ^ 1u, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        tmem_st32_nowait(ta + (uint32_t)b * 128u, a0);
+        tmem_st32_nowait(ta + (uint32_t)b * 128u + 64u, a1);
+        tmem_wait_st();
+        tc_fence_before();
         __syncwarp();
+        if (lane == 0) mbar_arrive(bar_afull + 8 * b);
+        if (++b == kW4ABufs) {
+          b = 0;
+          bphase ^= 1u;
+        }
         if (lane == 0) mbar_arrive(bar_rempty + 8 * stage);  // codes and scales of this stage read
         if (++stage == p.stages) {
           stage = 0;
@@ -774,35 +779,28 @@ __global__ void __launch_bounds__(kW4Threads, 1)
           ok = false;
           break;
         }
-        const uint32_t sw = sbase + stage * p.stage_bytes;
-        for (int j = 0; j < 2; ++j) {
-          if (!mbar_wait_all(bar_afull + 8 * b, bphase, abort_flag, p.status)) {
-            ok = false;
-            break;
+        if (!mbar_wait_all(bar_afull + 8 * b, bphase, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t sw = sbase + stage * p.stage_bytes;
+          const uint32_t ab = tmem_base + kW4ACol + (uint32_t)b * 128u;
+          const uint32_t d1 = dt + (uint32_t)p.d1_col;
+          for (int j = 0; j < 2; ++j) {
+            const uint64_t bd = sdesc_k_sw128(sw + kW4CodeBytes + (uint32_t)(j * parts) * xbytes);
+            tc_mma_ts_kblock(dt, d1, ab + (uint32_t)j * 64u, bd, idesc, (rs > d.kb0 || j > 0) ? 1u : 0u);
+            if (parts > 1) tc_mma_ts_kblock(dt, d1, ab + (uint32_t)j * 64u, bd + (xbytes >> 4), idesc, 1u);
           }
-          tc_fence_after();
-          if (lane == 0) {
-            const uint32_t ab = tmem_base + kW4ACol + (uint32_t)b * 64u;
-            const uint32_t bx = sw + kW4CodeBytes + (uint32_t)(j * parts) * xbytes;
-            for (int part = 0; part < parts; ++part) {
-              const uint32_t sxp = bx + (uint32_t)part * xbytes;
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint32_t acc_in = (part > 0 || rs > d.kb0 || j > 0 || kk > 0) ? 1u : 0u;
-                const uint64_t bdesc = sdesc_k_sw128(sxp + kk * 32);
-                tc_mma_ts(dt, ab + (uint32_t)kk * 8u, bdesc, idesc, acc_in);
-                tc_mma_ts(dt + (uint32_t)p.d1_col, ab + 32u + (uint32_t)kk * 8u, bdesc, idesc, acc_in);
-              }
-            }
-            tc_commit(bar_aempty + 8 * b);
-            if (j == 1) tc_commit(bar_rempty + 8 * stage);  // the stage's activations are read
-          }
-          __syncwarp();
-          any = true;
-          if (++b == kW4ABufs) {
-            b = 0;
-            bphase ^= 1u;
-          }
+          tc_commit(bar_aempty + 8 * b);
+          tc_commit(bar_rempty + 8 * stage);  // the stage's activations are read
+        }
+        __syncwarp();
+        any = true;
+        if (++b == kW4ABufs) {
+          b = 0;
+          bphase ^= 1u;
         }
         if (++stage == p.stages) {
           stage = 0;
