@@ -277,7 +277,8 @@ __device__ __forceinline__ void epi_tile(const TcDev& p, const Tile& d, uint32_t
 
 template <bool SWAP, bool FP8, int EPI>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const TcDev p) {
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+              const __grid_constant__ CUtensorMap tmX16, const TcDev p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -306,6 +307,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     fence_barrier_init();
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
+    if (SWAP) tma_prefetch_desc(&tmX16);
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
   tc_fence_before();
@@ -337,6 +339,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // first stages of weight tiles before waiting for it (programmatic
     // dependent launch), so this kernel's HBM stream starts while the previous
     // one drains.
+    //
+    // Swap-AB tiles load only the token rows the MMA reads (N = npad): gathered
+    // tiles npad rows, pre-gathered ones a 16-row box when npad is 16, else the
+    // full activation box.
+    const int parts = p.x_lo_rows ? 2 : 1;
+    auto x_rows = [&](const Tile& d) -> int {
+      if constexpr (SWAP) return p.gather ? d.npad : (d.npad <= 16 ? 16 : p.xbox);
+      return p.xbox;
+    };
+    auto stage_tx = [&](const Tile& d) -> uint32_t {
+      return p.w_bytes + (uint32_t)(x_rows(d) * 128 * parts);
+    };
     int pre = 0;
     if (p.early && lane == 0 && (int)blockIdx.x < ntiles) {
       const Tile d = tile_at<SWAP, EPI>(p, blockIdx.x);
@@ -344,7 +358,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int i = 0; i < pre; ++i) {
         const uint32_t sw = sbase + i * p.stage_bytes;
         const uint32_t fb = bar_full + 8 * i;
-        mbar_arrive_expect_tx(fb, p.stage_bytes);
+        mbar_arrive_expect_tx(fb, stage_tx(d));
         tma_load_2d(sw, &tmW, (d.kb0 + i) * KBLK, d.wr0, fb);
         tma_load_2d(sw + p.wbox * 128, &tmW, (d.kb0 + i) * KBLK, d.wr0 + p.w_pair_off, fb);
       }
@@ -353,7 +367,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     pdl_wait();
     const int n_pairs = p.T * p.k;
     const int npp = (EPI == TC_EPI_LOGITS) ? 0 : p.meta[META_NPP];
-    const int groups = p.xbox / 4;  // gather4 groups per activation tile (<= 64)
     int stage = 0;
     uint32_t phase = 0, issued = 0;
     bool ok = true;
@@ -379,19 +392,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             break;
           }
           if (lane == 0) {
-            mbar_arrive_expect_tx(fb, p.stage_bytes);
+            mbar_arrive_expect_tx(fb, stage_tx(d));
             tma_load_2d(sw, &tmW, kb * KBLK, d.wr0, fb);
             tma_load_2d(sw + p.wbox * 128, &tmW, kb * KBLK, d.wr0 + p.w_pair_off, fb);
           }
           __syncwarp();
         }
         if (p.gather) {
+          const int groups_d = x_rows(d) / 4;
 #pragma unroll
           for (int gi = 0; gi < 2; ++gi) {
             const int g = lane + 32 * gi;
-            if (g < groups)
+            if (g < groups_d)
               tma_gather4(sw + p.w_bytes + (uint32_t)g * 512u, &tmX, kb * KBLK, rows[gi][0], rows[gi][1],
                           rows[gi][2], rows[gi][3], fb);
+          }
+        } else if (SWAP && x_rows(d) == 16 && p.xbox > 16) {
+          if (lane == 0) {
+            tma_load_2d(sw + p.w_bytes, &tmX16, kb * KBLK, d.xrow, fb);
+            if (p.x_lo_rows)
+              tma_load_2d(sw + p.w_bytes + p.xbox * 128, &tmX16, kb * KBLK, d.xrow + p.x_lo_rows, fb);
           }
         } else if (p.cluster > 1) {
           // the pair shares the activation tile: each CTA loads its half for both
@@ -878,8 +898,8 @@ __global__ void __launch_bounds__(kW4Threads, 1)
 // host side
 // ---------------------------------------------------------------------------
 template <bool SWAP, bool FP8, int EPI>
-cudaError_t launch_inst(const CUtensorMap& mw, const CUtensorMap& mx, const TcDev& p, int grid, size_t smem,
-                        cudaStream_t s, int max_grid) {
+cudaError_t launch_inst(const CUtensorMap& mw, const CUtensorMap& mx, const CUtensorMap& mx16, const TcDev& p,
+                        int grid, size_t smem, cudaStream_t s, int max_grid) {
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -920,7 +940,7 @@ cudaError_t launch_inst(const CUtensorMap& mw, const CUtensorMap& mx, const TcDe
     if (grid < p.cluster) return cudaErrorInvalidConfiguration;
     cfg.gridDim = dim3(grid);
   }
-  return cudaLaunchKernelEx(&cfg, kern, mw, mx, p);
+  return cudaLaunchKernelEx(&cfg, kern, mw, mx, mx16, p);
 }
 
 }  // namespace
@@ -1064,6 +1084,12 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s) {
     return cudaErrorInvalidValue;
   }
 
+  // swap-AB: a 16-row box for the tiles of experts with at most 16 tokens
+  CUtensorMap mx16 = mx;
+  if (a.swap && !a.gather && a.xbox > 16 &&
+      !make_tensor_map_2d(&mx16, a.X, eb, (uint64_t)a.K, (uint64_t)a.cap + (uint64_t)a.x_lo_rows, 16u))
+    return cudaErrorInvalidValue;
+
   TcDev p = {};
   p.cluster = cluster;
   p.epi = a.epi;
@@ -1130,7 +1156,7 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s) {
 
 #define MOE_TC_CASE(SW, F8, EP)                      \
   if (a.swap == SW && a.fp8 == F8 && a.epi == EP) \
-    return launch_inst<SW, F8, EP>(mw, mx, p, grid, smem, s, a.num_sms);
+    return launch_inst<SW, F8, EP>(mw, mx, mx16, p, grid, smem, s, a.num_sms);
   MOE_TC_CASE(true, false, TC_EPI_G1_BF16)
   MOE_TC_CASE(true, false, TC_EPI_G1_PART)
   MOE_TC_CASE(true, false, TC_EPI_G2_F32)
