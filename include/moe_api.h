@@ -123,9 +123,10 @@ typedef struct {
                          nothing sets, with a ~1 ms bound; the call then reports
                          MOE_ERR_DEVICE_TIMEOUT through moe_get_status and writes
                          nothing else.  0 in normal use. */
-  int act_split;      /* bf16 path: 0 = automatic (hi/lo in SWAP_AB, single in TOKEN_MAJOR),
-                         1 = intermediate stored as one bf16, 2 = as bf16 hi + bf16 lo
-                         (a - bf16(a)), GEMM2 then runs both parts into one fp32 accumulator */
+  int act_split;      /* bf16 and INT4 weights: 0 = automatic (bf16: hi/lo in SWAP_AB, single in
+                         TOKEN_MAJOR; INT4: single), 1 = intermediate stored as one bf16,
+                         2 = as bf16 hi + bf16 lo (a - bf16(a)), GEMM2 then runs both parts into
+                         one fp32 accumulator */
   void* trace;        /* nullable device buffer of MOE_TRACE_WORDS uint64 per SM: when the call
                          runs as a single launch, CTA c writes %globaltimer stamps (ns) of its
                          phases to trace[c * MOE_TRACE_WORDS + moe_trace_event]; events a CTA

@@ -167,9 +167,12 @@ static int make_plan(int T, int H, int I, int E, int topk, moe_dtype act, moe_dt
       p.wbox2 = (H % 256 == 0) ? 128 : 64;
       p.y_bf16 = false;
     }
-    // hi/lo intermediate: by default where it is free (swap-AB decode streams
-    // weights from HBM; the second MMA only uses idle tensor-core time)
-    p.act_split = (p.path == PATH_BF16 || p.path == PATH_W4) && (act_mode == 2 || (act_mode == 0 && p.swap));
+    // hi/lo intermediate: by default where it is free (bf16 swap-AB decode
+    // streams weights from HBM; the second MMA only uses idle tensor-core time).
+    // The INT4 GEMMs are bound by the MMA instruction rate, where GEMM2's second
+    // MMA costs about 10 %: there it is on request only (act_split = 2).
+    p.act_split = (p.path == PATH_BF16 && (act_mode == 2 || (act_mode == 0 && p.swap))) ||
+                  (p.path == PATH_W4 && act_mode == 2);
     // GEMM1 gathers token rows itself (one tile::gather4 per 4 rows) when the
     // activation tile is short; for wider tiles the per-stage TMA instruction
     // count outweighs the saved kernel, so rows are gathered beforehand.

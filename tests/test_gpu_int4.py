@@ -59,11 +59,13 @@ def test_int4_layer_matches_oracle(moe, T, H, I, E, k):
     assert rel_err(out.float().cpu().numpy(), ref, f"int4 T={T}") <= TOL["bf16"]
 
 
-@pytest.mark.parametrize("T,splits", [(3, 1), (3, 2), (20, 1), (48, 1)])
-def test_int4_layer_equals_bf16_layer_on_decoded_weights(moe, T, splits):
+@pytest.mark.parametrize("T,splits,act_split", [(3, 1, 2), (3, 2, 2), (20, 1, 2), (48, 1, 2), (20, 1, 1), (3, 2, 1)])
+def test_int4_layer_equals_bf16_layer_on_decoded_weights(moe, T, splits, act_split):
+    """Same plan on both: K splits and the intermediate's form (hi + lo, or one bf16; the INT4 default
+    is one bf16, the bf16 path's default hi + lo)."""
     L = _layer(T, 512, 512, 16, 4)
     sp = L["spec"]
-    opts = {"split_k": splits}
+    opts = {"split_k": splits, "act_split": act_split}
     a = _run(moe, L, opts)
     W13 = _decoded(L["W13"], L["w13_scale"]).cuda()
     W2 = _decoded(L["W2"], L["w2_scale"]).cuda()
