@@ -114,3 +114,26 @@ def test_forward_argument_errors_before_launch(moe):
     assert lib.moe_route(fake, fake, 4, 256, 8, 0, 1, 1, fake, fake, fake, None) == moe.MOE_ERR_ARG
     assert lib.moe_align(fake, 4, 2, 8, 0, fake, fake, fake, None, None) == moe.MOE_ERR_ARG
     assert lib.moe_topk_from_logits(fake, 4, 8, 9, 1, fake, fake, None) == moe.MOE_ERR_ARG
+
+
+def test_int4_plans_and_argument_errors(moe):
+    """INT4 weights (host logic only): swap-AB up to 128 tokens with H and I multiples of 256, one bf16
+    intermediate by default, the hi/lo pair on request; scales are required."""
+    p = moe.moe_plan_info(64, 4096, 14336, 8, 2, moe.MOE_BF16, moe.MOE_INT4)
+    assert p["orientation"] == moe.ORIENT_SWAP_AB and p["act_split"] == 0
+    assert moe.moe_plan_info(64, 4096, 14336, 8, 2, moe.MOE_BF16, moe.MOE_INT4, {"act_split": 2})["act_split"] == 1
+    assert moe.moe_plan_info(100, 512, 512, 8, 2, moe.MOE_BF16, moe.MOE_INT4)["orientation"] == moe.ORIENT_SWAP_AB
+    for T, H, I, opts in [(129, 512, 512, None), (8, 384, 512, None), (8, 512, 640, None),
+                          (64, 512, 512, {"orientation": 2})]:
+        with pytest.raises(moe.MoeError) as e:
+            moe.moe_plan_info(T, H, I, 8, 2, moe.MOE_BF16, moe.MOE_INT4, opts)
+        assert e.value.code == moe.MOE_ERR_UNSUPPORTED, (T, H, I, opts)
+    with pytest.raises(moe.MoeError):  # fp32 activations with INT4 weights
+        moe.moe_plan_info(8, 512, 512, 8, 2, moe.MOE_F32, moe.MOE_INT4)
+    lib = moe.lib()
+    fake, ws = ctypes.c_void_p(0x1000), ctypes.c_void_p(0x100000)
+    # INT4 without group scales: rejected before anything is launched
+    assert lib.moe_forward(fake, fake, fake, fake, 4, 512, 512, 8, 2, 1, 1, moe.MOE_INT4, None, None, fake, ws,
+                           1 << 30, None, None) == moe.MOE_ERR_ARG
+    # the INT4 workspace is sized from the same plan
+    assert moe.moe_workspace_size(64, 4096, 14336, 8, 2, moe.MOE_BF16, moe.MOE_INT4) == p["workspace_bytes"]
