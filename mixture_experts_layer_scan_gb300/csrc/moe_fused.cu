@@ -680,14 +680,16 @@ __global__ void __launch_bounds__(kFThreads, 1)
     bool okm = true, any = false;
     for (int t = blockIdx.x; t < ntiles && okm; t += gridDim.x) {
       const FTile d = ftile_at(p, t, n_g1, act, cnt, off, poff);
-      const uint32_t idesc = idesc_make(128, d.npad, false);
+      // GEMM2 with a hi/lo intermediate: one MMA over the xbox hi rows then the lo rows
+      const bool stacked = d.g2 && p.act_split;
+      const uint32_t idesc = idesc_make(128, stacked ? p.xbox + d.npad : d.npad, false);
       if (!mbar_wait_all(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag, p.status)) {
         okm = false;
         break;
       }
       tc_fence_after();
       const uint32_t dt = tmem_base + (uint32_t)(acc * 256);
-      const int parts = (d.g2 && p.act_split) ? 2 : 1;
+      const int parts = 1;
       for (int kb = d.kb0; kb < d.kb1; ++kb) {
         if (!mbar_wait_all(bar_full + 8 * stage, phase, abort_flag, p.status)) {
           okm = false;
@@ -697,7 +699,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
         if (lane == 0) {
           const uint32_t sws = sbase + stage * p.stage_bytes;
           const uint32_t sx = sws + kWBytes;
-          // D0 += W[rows 0..127] X^T, D1 += W[rows 128..255] X^T (hi, then lo part of the intermediate)
+          // D0 += W[rows 0..127] X^T, D1 += W[rows 128..255] X^T (GEMM2 with a hi/lo intermediate: X^T
+          // is the hi rows then the lo rows, whose products the epilogue adds)
           for (int part = 0; part < parts; ++part) {
             const uint32_t sxp = sx + (uint32_t)part * x1_bytes;
 #pragma unroll
@@ -783,6 +786,16 @@ __global__ void __launch_bounds__(kFThreads, 1)
           float v0[16], v1[16];
           tmem_ld16(tb + (uint32_t)c0, v0);
           tmem_ld16(tb + 128u + (uint32_t)c0, v1);
+          if (p.act_split) {  // + the low part's products, xbox columns further on
+            float l0[16], l1[16];
+            tmem_ld16(tb + (uint32_t)(p.xbox + c0), l0);
+            tmem_ld16(tb + 128u + (uint32_t)(p.xbox + c0), l1);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              v0[j] += l0[j];
+              v1[j] += l1[j];
+            }
+          }
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int c = c0 + j;

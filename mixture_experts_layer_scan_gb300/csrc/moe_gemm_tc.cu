@@ -57,6 +57,8 @@ struct TcDev {
   int n_valid;      // router: valid output columns
   int x_lo_rows;    // >0: the activation operand also has a bf16 low part at row offset x_lo_rows
   int cluster;      // 2: token-major CTA pairs sharing each activation tile (multicast), else 1
+  int stack_lo;     // swap-AB GEMM2 with a hi/lo activation: one MMA over the hi rows then the lo rows
+                    // (N = xbox + npad), the two column groups summed in the epilogue
   uint32_t stage_bytes, w_bytes, bar_off;
   const int32_t* sorted;
   const int32_t* eids;
@@ -186,6 +188,16 @@ __device__ __forceinline__ void epi_tile(const TcDev& p, const Tile& d, uint32_t
       float v0[16], v1[16];
       tmem_ld16(tb + (uint32_t)c0, v0);
       tmem_ld16(tb + (uint32_t)(p.d1_col + c0), v1);
+      if (p.stack_lo) {  // + the low part's products, xbox columns further on
+        float l0[16], l1[16];
+        tmem_ld16(tb + (uint32_t)(p.xbox + c0), l0);
+        tmem_ld16(tb + (uint32_t)(p.d1_col + p.xbox + c0), l1);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          v0[j] += l0[j];
+          v1[j] += l1[j];
+        }
+      }
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const int c = c0 + j;
@@ -452,7 +464,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     bool ok = true, any = false;
     for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
       const Tile d = tile_at<SWAP, EPI>(p, t);
-      const int N = SWAP ? d.npad : 2 * p.wbox;
+      // (stacked hi/lo: the B rows are the xbox hi rows, then the lo rows, all in one MMA)
+      const int N = SWAP ? (p.stack_lo ? p.xbox + d.npad : d.npad) : 2 * p.wbox;
       const uint32_t idesc = idesc_make(128, N, FP8);
       if (!mbar_wait_all(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag, p.status)) {
         ok = false;
@@ -471,7 +484,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const uint32_t sx = sw + p.w_bytes;
           // the optional low bf16 part of the activations goes into the same fp32
           // accumulator: W (x_hi + x_lo) carries ~16 significant bits of the intermediate
-          const int parts = p.x_lo_rows ? 2 : 1;
+          const int parts = (p.x_lo_rows && !p.stack_lo) ? 2 : 1;
           for (int part = 0; part < parts; ++part) {
             const uint32_t sxp = sx + (uint32_t)(part * p.xbox * 128);
             if constexpr (SWAP) {
@@ -1092,6 +1105,7 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s) {
 
   TcDev p = {};
   p.cluster = cluster;
+  p.stack_lo = (a.swap && a.x_lo_rows && !a.fp8 && a.xbox <= 64) ? 1 : 0;
   p.epi = a.epi;
   p.T = a.T;
   p.k = a.k;
