@@ -817,7 +817,8 @@ __global__ void __launch_bounds__(kW4Threads, 1)
     bool ok = true, any = false;
     for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
       const Tile d = tile_at<true, EPI>(p, t);
-      const uint32_t idesc = idesc_make(128, d.npad, false);
+      // (stacked hi/lo activation: one MMA over the xbox hi rows then the lo rows)
+      const uint32_t idesc = idesc_make(128, p.stack_lo ? p.xbox + d.npad : d.npad, false);
       if (!mbar_wait_all(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag, p.status)) {
         ok = false;
         break;
@@ -841,7 +842,8 @@ __global__ void __launch_bounds__(kW4Threads, 1)
           for (int j = 0; j < 2; ++j) {
             const uint64_t bd = sdesc_k_sw128(sw + kW4CodeBytes + (uint32_t)(j * parts) * xbytes);
             tc_mma_ts_kblock(dt, d1, ab + (uint32_t)j * 64u, bd, idesc, (rs > d.kb0 || j > 0) ? 1u : 0u);
-            if (parts > 1) tc_mma_ts_kblock(dt, d1, ab + (uint32_t)j * 64u, bd + (xbytes >> 4), idesc, 1u);
+            if (parts > 1 && !p.stack_lo)
+              tc_mma_ts_kblock(dt, d1, ab + (uint32_t)j * 64u, bd + (xbytes >> 4), idesc, 1u);
           }
           tc_commit(bar_aempty + 8 * b);
           tc_commit(bar_rempty + 8 * stage);  // the stage's activations are read
@@ -1052,9 +1054,12 @@ static cudaError_t launch_gemm_w4(const TcGemmArgs& a, cudaStream_t s) {
   p.out_split_stride = a.out_split_stride;
   p.status = a.status;
   // accumulators: D0 and D1 of xbox columns each; two buffers while they fit below the A buffers
-  p.d1_col = a.xbox;
-  p.buf_cols = 2 * a.xbox;
+  // (a stacked hi/lo activation needs xbox + npad columns per accumulator)
+  p.stack_lo = (a.x_lo_rows && a.xbox <= 64) ? 1 : 0;
+  p.d1_col = p.stack_lo ? 2 * a.xbox : a.xbox;
+  p.buf_cols = 2 * p.d1_col;
   p.nbuf = 2 * p.buf_cols <= (int)kW4ACol ? 2 : 1;
+  if (a.x_lo_rows && !p.stack_lo && p.buf_cols > (int)kW4ACol) return cudaErrorInvalidValue;
   const int parts = a.x_lo_rows ? 2 : 1;
   // codes + two K blocks of activations + scales
   p.stage_bytes = kW4CodeBytes + 2u * (uint32_t)a.xbox * 128u * parts + kW4ScaleBytes;
