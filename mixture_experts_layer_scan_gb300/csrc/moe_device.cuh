@@ -161,18 +161,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t smem_dst, const void* tmap,
       : "memory");
 }
 
-// The same load delivered to every CTA of the cluster named in cta_mask, at
-// the same shared-memory offset; each destination CTA's mbarrier at offset
-// `bar` receives the bytes that landed in that CTA.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t smem_dst, const void* tmap, int c_inner, int c_row,
-                                               uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
-      "[%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c_inner), "r"(c_row), "h"(cta_mask)
-      : "memory");
-}
-
 // Rank of this CTA in its cluster, and a barrier over every thread of the cluster.
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
@@ -315,13 +303,6 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 // Arrive once on an mbarrier when every tcgen05 op issued so far by this thread completes.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
-}
-
-// As tc_commit, arriving on the mbarrier at offset `bar` of every CTA in cta_mask.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t cta_mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-               "h"(cta_mask)
                : "memory");
 }
 

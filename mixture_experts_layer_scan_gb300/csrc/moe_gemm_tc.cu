@@ -56,7 +56,6 @@ struct TcDev {
   int d1_col;       // swap-AB: column of accumulator D1 (weight rows 128..255) inside a buffer
   int n_valid;      // router: valid output columns
   int x_lo_rows;    // >0: the activation operand also has a bf16 low part at row offset x_lo_rows
-  int cluster;      // 2: token-major CTA pairs sharing each activation tile (multicast), else 1
   int stack_lo;     // swap-AB GEMM2 with a hi/lo activation: one MMA over the hi rows then the lo rows
                     // (N = xbox + npad), the two column groups summed in the epilogue
   uint32_t stage_bytes, w_bytes, bar_off;
@@ -307,7 +306,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, p.cluster);  // a stage is free once every CTA that reads it is done
+      mbar_init(bar_empty + 8 * s, 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_tfull + 8 * b, 1);
@@ -326,9 +325,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   cta_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // CTA pairs: the peer's barriers are initialised before any multicast reaches them
-  const uint32_t crank = p.cluster > 1 ? cluster_ctarank() : 0u;
-  if (p.cluster > 1) cluster_sync_all();
 
   // Programmatic dependent launch: kernels of this library let their
   // dependents launch early, so nothing written by an earlier kernel may be
@@ -425,13 +421,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (p.x_lo_rows)
               tma_load_2d(sw + p.w_bytes + p.xbox * 128, &tmX16, kb * KBLK, d.xrow + p.x_lo_rows, fb);
           }
-        } else if (p.cluster > 1) {
-          // the pair shares the activation tile: each CTA loads its half for both
-          if (lane == 0) {
-            const int half = p.xbox / 2;
-            tma_load_2d_mc(sw + p.w_bytes + crank * (uint32_t)(half * 128), &tmX, kb * KBLK,
-                           d.xrow + (int)crank * half, fb, (uint16_t)0x3);
-          }
         } else if (lane == 0) {
           tma_load_2d(sw + p.w_bytes, &tmX, kb * KBLK, d.xrow, fb);
           if (p.x_lo_rows) tma_load_2d(sw + p.w_bytes + p.xbox * 128, &tmX, kb * KBLK, d.xrow + p.x_lo_rows, fb);
@@ -504,10 +493,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             (part > 0 || kb > d.kb0 || kk > 0) ? 1u : 0u);
             }
           }
-          if (p.cluster > 1)
-            tc_commit_mc(bar_empty + 8 * stage, (uint16_t)0x3);  // both CTAs' copies of the stage
-          else
-            tc_commit(bar_empty + 8 * stage);
+          tc_commit(bar_empty + 8 * stage);
         }
         __syncwarp();
         any = true;
@@ -577,9 +563,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
-  // no CTA of a pair leaves while its peer may still write into its shared memory or barriers
-  __syncwarp();
-  if (p.cluster > 1) cluster_sync_all();
 }
 
 // ---------------------------------------------------------------------------
@@ -929,32 +912,12 @@ cudaError_t launch_inst(const CUtensorMap& mw, const CUtensorMap& mx, const CUte
   cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (p.cluster > 1) {
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = (unsigned)p.cluster;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
-    cfg.numAttrs = 2;
-    // a persistent grid: only as many pairs as can be resident at once (an SM left
-    // over in a GPC cannot take half a pair)
-    static int max_clusters[64] = {};
-    if (dev < 64 && max_clusters[dev] == 0) {
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) n = -1;
-      max_clusters[dev] = n;
-    }
-    const int mc = dev < 64 ? max_clusters[dev] : -1;
-    if (mc < 1) return cudaErrorInvalidConfiguration;
-    grid = std::min(grid, std::min(max_grid, mc * p.cluster));
-    grid -= grid % p.cluster;
-    if (grid < p.cluster) return cudaErrorInvalidConfiguration;
-    cfg.gridDim = dim3(grid);
-  }
+  (void)max_grid;
   return cudaLaunchKernelEx(&cfg, kern, mw, mx, mx16, p);
 }
 
@@ -1091,14 +1054,8 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s) {
     if (a.xbox % 4 || a.xbox > 256 || a.x_lo_rows) return cudaErrorInvalidValue;
     if (!make_tensor_map_2d(&mx, a.X, eb, (uint64_t)a.K, (uint64_t)a.T, 1u)) return cudaErrorInvalidValue;
   }
-  // token-major GEMM1/GEMM2: CTA pairs on neighbouring weight tiles of one token block share
-  // its activation tile, each loading half of it for both (cuts the L2 -> SM bytes per flop)
-  const int cluster = (!a.swap && !a.gather && a.epi != TC_EPI_LOGITS && a.n_tiles % 2 == 0 && a.xbox == 128 &&
-                       !a.x_lo_rows && !a.no_cluster)
-                          ? 2
-                          : 1;
   if (!a.gather && !make_tensor_map_2d(&mx, a.X, eb, (uint64_t)a.K, (uint64_t)a.cap + (uint64_t)a.x_lo_rows,
-                                       (uint32_t)(a.xbox / cluster))) {
+                                       (uint32_t)a.xbox)) {
     return cudaErrorInvalidValue;
   }
 
@@ -1109,7 +1066,6 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s) {
     return cudaErrorInvalidValue;
 
   TcDev p = {};
-  p.cluster = cluster;
   p.stack_lo = (a.swap && a.x_lo_rows && !a.fp8 && a.xbox <= 64) ? 1 : 0;
   p.epi = a.epi;
   p.T = a.T;

@@ -109,7 +109,6 @@ struct TcGemmArgs {
   unsigned* amax_out;       // amax bits of the produced intermediate (FP8 GEMM1)
   int* status;
   int num_sms;
-  bool no_cluster;          // token-major: launch single CTAs instead of activation-sharing pairs
   bool w4;                  // INT4 weight codes (swap-AB), dequantised to bf16 in the main loop
   const void* w4_scale;     // bf16 group scales [E][K / 128][w_rows_per_expert]
 };
