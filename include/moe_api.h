@@ -15,7 +15,9 @@
  *    *workspace* and the FP8 scales are DEVICE pointers of the current CUDA
  *    device.  The caller owns all of them; the library never allocates,
  *    frees or retains device memory across calls (it keeps one status word
- *    per device, see moe_get_status).
+ *    per device, see moe_get_status).  The library caches per-device state
+ *    (that word's address, kernel attributes); cudaDeviceReset() invalidates
+ *    it, so the library must not be used on a device after a reset.
  *  - All arrays are dense row-major with no padding between rows.  Device
  *    pointers must be 16-byte aligned (MOE_ERR_ALIGNMENT otherwise).
  *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
@@ -232,8 +234,9 @@ MOE_API int moe_align(const int32_t* topk_ids, int T, int topk, int E, int block
  *                in the GEMM epilogues (page 1, section "Routage backend pour la
  *                quantisation des tenseurs FP8": scaling fused where the data is used)
  *   (BF16, INT4) tcgen05 kind::f16 path with the codes expanded to bf16 weights in
- *                shared memory inside the GEMM main loop ("FusedMoE vs MegaMoE",
- *                section 6.3: quantised expert weights); SWAP_AB orientation only,
+ *                tensor memory inside the GEMM main loop (the MMA takes its weight operand
+ *                from there; "FusedMoE vs MegaMoE", section 6.3: quantised expert
+ *                weights); SWAP_AB orientation only,
  *                T <= 128, H % 256 == 0 and I % 256 == 0 (else MOE_ERR_UNSUPPORTED)
  *   tensor-core paths need H % 128 == 0 and I % 128 == 0.
  * The intermediate SiLU(gate)*up is stored in bf16 (as a bf16 hi + lo pair in SWAP_AB
@@ -344,14 +347,22 @@ MOE_API int moe_cache_lru_plan(int E, int n_slots, int n_calls, int pairs, const
  * MOE_NOALLOC_MAX_WORKSPACE bytes in this library's device memory, which every
  * GPU that loads the library keeps until the process exits.
  *  - Shapes whose moe_workspace_size() exceeds MOE_NOALLOC_MAX_WORKSPACE are
- *    rejected with MOE_ERR_WORKSPACE before anything is enqueued (decode
- *    batches of the usual sizes fit; prefill batches do not -- use moe_forward).
+ *    rejected with MOE_ERR_WORKSPACE before anything is enqueued.  For
+ *    example, bf16 decode batches of up to 64 tokens of a Mixtral-shaped
+ *    layer (hidden 4096, 8 experts, FFN 14336: 29.5 MiB) or of a fine-grained
+ *    one (hidden 2048, 128 experts, FFN 768, top-8: 26.7 MiB) fit; an FP8
+ *    layer with hidden 4096, 64 experts, FFN 8192, top-8 at 64 tokens needs
+ *    71 MiB and prefill batches need far more -- use moe_forward for those.
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress) and caches it; make that first call before any
- *    stream capture on that device.
+ *    stream capture on that device.  cudaDeviceReset() invalidates the cached
+ *    address (and the library's other per-device state): do not call the
+ *    library on a device after resetting it in the same process.
  *  - Every call on a device uses the same array and finds the previous call's
- *    contents in it; the layer initialises what it reads, so nothing needs
- *    clearing.  Calls whose GPU work overlaps (different streams, or several
+ *    contents in it; the layer initialises every word it reads (the FP8 amax
+ *    words, the timeout test flag and the single-launch kernel's launch tag
+ *    are cleared on the stream first), so nothing needs clearing by the
+ *    caller.  Calls whose GPU work overlaps (different streams, or several
  *    host threads) race on the array: issue them on one stream.
  *  - Allocates nothing, frees nothing, and calls no allocating library routine. */
 #define MOE_NOALLOC_MAX_WORKSPACE (32u << 20)

@@ -249,20 +249,24 @@ def moe_forward(hidden: torch.Tensor, router_w: torch.Tensor, w13: torch.Tensor,
 
 
 def moe_forward_noalloc(hidden: torch.Tensor, router_w: torch.Tensor, w13: torch.Tensor, w2: torch.Tensor, topk: int,
-                        renorm: bool, w13_scale=None, w2_scale=None, out=None, options=None, stream=None):
+                        renorm: bool, w13_scale=None, w2_scale=None, out=None, options=None, stream=None,
+                        w_format=None):
     """moe_forward without a workspace argument, for callers that cannot allocate device memory.
 
     The library keeps the workspace in its own fixed device array (NOALLOC_MAX_WORKSPACE bytes per
     device); larger shapes raise MoeError(MOE_ERR_WORKSPACE).  Pass `out` to allocate nothing here either.
+    w_format="int4" takes packed INT4 weights as moe_forward does.
     """
     T, H = hidden.shape
     E, twoI, H2 = w13.shape
     I = twoI // 2
-    if H2 != H or w2.shape != (E, H, I) or router_w.shape != (E, H):
+    div = 2 if w_format == "int4" else 1
+    if H2 * div != H or w2.shape != (E, H, I // div) or router_w.shape != (E, H):
         raise ValueError("inconsistent shapes")
+    wdt = MOE_INT4 if w_format == "int4" else _dt(w13)
     out = torch.empty_like(hidden) if out is None else out
     _check(_lib.moe_forward_noalloc(_p(hidden), _p(router_w), _p(w13), _p(w2), T, H, I, E, topk, int(bool(renorm)),
-                                    _dt(hidden), _dt(w13), _p(w13_scale), _p(w2_scale), _p(out), _opts(options),
+                                    _dt(hidden), wdt, _p(w13_scale), _p(w2_scale), _p(out), _opts(options),
                                     _stream(stream)), "moe_forward_noalloc")
     return out
 

@@ -355,6 +355,9 @@ static int forward_steps(const Plan& pl, int steps, const void* hidden, const vo
     fa.trace = o ? o->trace : nullptr;
     fa.status = st;
     fa.num_sms = sms;
+    // The launch tag starts at zero: the workspace may hold anything (a previous call of
+    // another shape), and other CTAs start once the tag equals this launch's grid id.
+    if (cudaMemsetAsync(fa.sync, 0, sizeof(unsigned long long), s) != cudaSuccess) return MOE_ERR_CUDA;
     if (launch_decode_fused(fa, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (o) {
       record(o->stage_end[MOE_STAGE_GEMM1], s);

@@ -48,6 +48,8 @@
 // dependency counters live in the workspace: CTA 0 zeroes them at the start of
 // each launch and then publishes the launch's grid id (%gridid, unique per
 // launch in a context); no CTA touches a counter before it has seen that id.
+// The host clears the tag word on the stream before each launch, so stale
+// workspace contents can never pass for the tag.
 #include <algorithm>
 
 #include "moe_device.cuh"

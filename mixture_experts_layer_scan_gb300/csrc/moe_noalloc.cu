@@ -12,7 +12,8 @@
 // library holds it (MOE_NOALLOC_MAX_WORKSPACE bytes) until the process exits.
 // Host code cannot use the array's name as a device address; its address on
 // the current device is looked up once per device with cudaGetSymbolAddress
-// (first call on that device) and cached.
+// (first call on that device) and cached.  cudaDeviceReset() makes the cached
+// address stale; the library is not to be used on a device after a reset.
 #include <mutex>
 
 #include <cuda_runtime.h>
@@ -55,8 +56,9 @@ extern "C" int moe_forward_noalloc(const void* hidden, const void* router_w, con
   void* ws = static_scratch_for_current_device();
   if (!ws) return MOE_ERR_CUDA;
   // moe_forward initialises every workspace word it reads before reading it
-  // (the FP8 amax words and the test flag are cleared on the stream), so the
-  // previous call's contents need no clearing here.
+  // (the FP8 amax words, the test flag and the single-launch kernel's launch
+  // tag are cleared on the stream), so the previous call's contents need no
+  // clearing here.
   return moe_forward(hidden, router_w, w13, w2, T, H, I, E, topk, renorm, act_dtype, w_dtype, w13_scale, w2_scale,
                      out, ws, kStaticScratchBytes, opts, stream);
 }

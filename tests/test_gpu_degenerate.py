@@ -13,7 +13,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import TOL, make_tie_free, rel_err
+from helpers import TOL, assert_parity, make_tie_free, rel_err
 from moe_synth import make_layer, spec
 
 pytestmark = pytest.mark.gpu
@@ -53,15 +53,15 @@ def _dense_ffn(x, w13, w2):
 @pytest.mark.parametrize("orient", [1, 2])
 def test_every_expert_chosen(moe, renorm, orient):
     L = make_layer(spec("mixtral_decode", T=9, H=256, I=256, E=4, k=4, renorm=renorm))
-    assert rel_err(_run(moe, L, {"orientation": orient}), _ref(L), f"k=E renorm={renorm}") <= TOL["bf16"]
+    assert_parity(_run(moe, L, {"orientation": orient}), _ref(L), "bf16", f"k=E renorm={renorm}")
 
 
 @pytest.mark.parametrize("orient", [1, 2])
 def test_single_expert_is_the_dense_ffn(moe, orient):
     L = make_layer(spec("mixtral_decode", T=20, H=256, I=384, E=1, k=1))
     out = _run(moe, L, {"orientation": orient})
-    assert rel_err(out, _ref(L), "E=k=1") <= TOL["bf16"]
-    assert rel_err(out, _dense_ffn(L["X"], L["W13"][0], L["W2"][0]), "E=k=1 vs dense") <= TOL["bf16"]
+    assert_parity(out, _ref(L), "bf16", "E=k=1")
+    assert_parity(out, _dense_ffn(L["X"], L["W13"][0], L["W2"][0]), "bf16", "E=k=1 vs dense")
 
 
 def test_identical_experts_are_the_dense_ffn(moe):
@@ -69,18 +69,17 @@ def test_identical_experts_are_the_dense_ffn(moe):
     L["W13"] = L["W13"][:1].expand_as(L["W13"]).contiguous()
     L["W2"] = L["W2"][:1].expand_as(L["W2"]).contiguous()
     out = _run(moe, L)
-    assert rel_err(out, _dense_ffn(L["X"], L["W13"][0], L["W2"][0]), "identical experts") <= TOL["bf16"]
+    assert_parity(out, _dense_ffn(L["X"], L["W13"][0], L["W2"][0]), "bf16", "identical experts")
 
 
-@pytest.mark.parametrize("T,E,orient", [(6, 512, 1), (200, 512, 2), (40, 1024, 1)])
+@pytest.mark.parametrize("T,E,orient", [(6, 512, 1), (200, 512, 2), (256, 512, 2), (300, 512, 2), (40, 1024, 1)])
 def test_many_experts(moe, T, E, orient):
-    """Up to the 1024 experts the permutation supports.  (The token-major case keeps one bf16
-    intermediate: with exact arithmetic that and the bf16 output already put this draw at 1.73e-2 of
-    the 2e-2 bar; T = 256 or 300 draws of this generator sit at 2.1-2.2e-2, above it, from rounding
-    alone.)"""
+    """Up to the 1024 experts the permutation supports.  The fine-grained generator's constant input
+    feature puts outputs at 6-8 RMS, where the bf16 output rounding alone costs up to 1.9e-2 of RMS:
+    the parity check then bounds the error beyond that rounding."""
     L = make_layer(spec("fine_decode", T=T, H=256, I=128, E=E, k=8))
     make_tie_free(L)
-    assert rel_err(_run(moe, L, {"orientation": orient}), _ref(L), f"E={E} T={T}") <= TOL["bf16"]
+    assert_parity(_run(moe, L, {"orientation": orient}), _ref(L), "bf16", f"E={E} T={T}")
 
 
 def test_all_tokens_route_to_the_same_experts(moe):
@@ -96,4 +95,4 @@ def test_all_tokens_route_to_the_same_experts(moe):
     ids = oracle.moe_forward(L["X"], L["Wr"], L["W13"], L["W2"], sp.k, sp.renorm)["ids"]
     assert set(np.unique(ids).tolist()) == {1, 4, 6}
     for orient in (1, 2):
-        assert rel_err(_run(moe, L, {"orientation": orient}), _ref(L), f"hot orient={orient}") <= TOL["bf16"]
+        assert_parity(_run(moe, L, {"orientation": orient}), _ref(L), "bf16", f"hot orient={orient}")

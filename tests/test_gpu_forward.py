@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import TOL, make_tie_free, rel_err
+from helpers import TOL, assert_parity, make_tie_free, rel_err
 from moe_synth import make_layer, spec
 
 pytestmark = pytest.mark.gpu
@@ -50,7 +50,7 @@ def test_fp32_path(moe, T, H, I, E, k):
     L = _layer("tiny_f32", T=T, H=H, I=I, E=E, k=k)
     out = _run(moe, L)
     assert out.dtype == torch.float32
-    assert rel_err(out.cpu().numpy(), _ref(L)) <= TOL["f32"]
+    assert_parity(out.cpu().numpy(), _ref(L), "f32", "")
 
 
 # swap-AB (decode) shapes: several 64-row weight tiles, K blocks and token counts not multiple of 16
@@ -59,7 +59,7 @@ def test_fp32_path(moe, T, H, I, E, k):
 def test_bf16_swap_ab(moe, T, H, I, E, k):
     L = _layer("mixtral_decode", T=T, H=H, I=I, E=E, k=k)
     out = _run(moe, L, {"orientation": 1})
-    assert rel_err(out.float().cpu().numpy(), _ref(L)) <= TOL["bf16"]
+    assert_parity(out.float().cpu().numpy(), _ref(L), "bf16", "")
 
 
 @pytest.mark.parametrize("T", [200, 256])
@@ -70,7 +70,7 @@ def test_bf16_swap_ab_wide_token_tiles(moe, T):
     plan = moe.moe_plan_info(T, 512, 512, 64, 8, moe.MOE_BF16, moe.MOE_BF16, {"orientation": 1})
     assert plan["orientation"] == moe.ORIENT_SWAP_AB
     out = _run(moe, L, {"orientation": 1})
-    assert rel_err(out.float().cpu().numpy(), _ref(L), f"swap-AB T={T}") <= TOL["bf16"]
+    assert_parity(out.float().cpu().numpy(), _ref(L), "bf16", f"swap-AB T={T}")
 
 
 @pytest.mark.parametrize("T,H,I,E,k", [(65, 256, 256, 8, 2), (200, 384, 256, 8, 2), (513, 256, 384, 16, 4),
@@ -78,21 +78,21 @@ def test_bf16_swap_ab_wide_token_tiles(moe, T):
 def test_bf16_token_major(moe, T, H, I, E, k):
     L = _layer("prefill", T=T, H=H, I=I, E=E, k=k)
     out = _run(moe, L, {"orientation": 2})
-    assert rel_err(out.float().cpu().numpy(), _ref(L)) <= TOL["bf16"]
+    assert_parity(out.float().cpu().numpy(), _ref(L), "bf16", "")
 
 
 @pytest.mark.parametrize("splits", [2, 3, 4])
 def test_bf16_split_k(moe, splits):
     L = _layer("fine_decode", T=5, H=512, I=384, E=16, k=4)
     out = _run(moe, L, {"orientation": 1, "split_k": splits})
-    assert rel_err(out.float().cpu().numpy(), _ref(L)) <= TOL["bf16"]
+    assert_parity(out.float().cpu().numpy(), _ref(L), "bf16", "")
 
 
 @pytest.mark.parametrize("orient,act_split", [(1, 1), (2, 2), (1, 2)])
 def test_bf16_intermediate_single_or_hi_lo(moe, orient, act_split):
     L = _layer("mixtral_decode", T=40, H=384, I=256, E=8, k=2)
     out = _run(moe, L, {"orientation": orient, "act_split": act_split})
-    assert rel_err(out.float().cpu().numpy(), _ref(L), f"orient={orient} act_split={act_split}") <= TOL["bf16"]
+    assert_parity(out.float().cpu().numpy(), _ref(L), "bf16", f"orient={orient} act_split={act_split}")
 
 
 def test_swap_ab_identity_both_orientations(moe):
@@ -101,21 +101,22 @@ def test_swap_ab_identity_both_orientations(moe):
     a = _run(moe, L, {"orientation": 1}).float().cpu().numpy()
     b = _run(moe, L, {"orientation": 2}).float().cpu().numpy()
     ref = _ref(L)
-    assert rel_err(a, ref) <= TOL["bf16"] and rel_err(b, ref) <= TOL["bf16"]
-    assert rel_err(a, b) <= TOL["bf16"]
+    assert_parity(a, ref, "bf16", "swap-AB orientation")
+    assert_parity(b, ref, "bf16", "token-major orientation")
+    assert rel_err(a, b, "swap-AB vs token-major") <= TOL["bf16"]
 
 
 @pytest.mark.parametrize("T,orient", [(1, 1), (16, 1), (64, 1), (130, 2), (7, 2)])
 def test_fp8_path(moe, T, orient):
     L = _layer("fp8_decode", T=T, H=256, I=256, E=8, k=4)
     out = _run(moe, L, {"orientation": orient})
-    assert rel_err(out.float().cpu().numpy(), _ref(L)) <= TOL["e4m3"]
+    assert_parity(out.float().cpu().numpy(), _ref(L), "e4m3", "")
 
 
 def test_fp8_split_k(moe):
     L = _layer("fp8_decode", T=3, H=512, I=256, E=8, k=4)
     out = _run(moe, L, {"orientation": 1, "split_k": 2})
-    assert rel_err(out.float().cpu().numpy(), _ref(L)) <= TOL["e4m3"]
+    assert_parity(out.float().cpu().numpy(), _ref(L), "e4m3", "")
 
 
 def test_deterministic(moe):
@@ -141,4 +142,4 @@ def test_injected_timeout_is_reported(moe):
     moe.moe_forward(d["X"], d["Wr"], d["W13"], d["W2"], 2, True, options={"inject_timeout": 1})
     assert moe.moe_get_status() == moe.MOE_ERR_DEVICE_TIMEOUT
     out = _run(moe, L)  # the context stays usable
-    assert rel_err(out.float().cpu().numpy(), _ref(L)) <= TOL["bf16"]
+    assert_parity(out.float().cpu().numpy(), _ref(L), "bf16", "")

@@ -8,17 +8,17 @@ finishes the last split) and unsplit GEMM1, a hidden size with a half last GEMM2
 tile, full-softmax weights (no renorm), 256 experts, the 512-pair limit, repeated
 launches on one workspace, and CUDA-graph replay.
 
-The error measure includes the final bf16 rounding of out, up to 2^-9 max|out|:
-the shapes here keep max|out|/RMS(out) below about 6, so that rounding alone
-stays under 1.4e-2 of the 2e-2 bar (a draw with an output at 9 RMS would exceed
-the bar with exact arithmetic before the rounding).
+Parity against the oracle uses the bf16 reading of the tolerance: the error
+beyond the final rounding of out to bf16 within 2e-2 of RMS(out), and the plain
+max|err|/RMS within 2e-2 wherever that rounding can cost at most half of it.
+Several shapes (fine-grained routing with small H) put outputs at 6-9 RMS.
 """
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from helpers import TOL, make_tie_free, rel_err
+from helpers import TOL, assert_parity, make_tie_free, rel_err
 from moe_synth import make_layer, spec
 
 pytestmark = pytest.mark.gpu
@@ -66,6 +66,9 @@ SHAPES = [  # name, T, H, I, E, k
     ("fine_decode", 5, 512, 384, 128, 8),
     ("fine_decode", 16, 640, 256, 64, 8),
     ("fine_decode", 3, 256, 256, 256, 8),
+    ("fine_decode", 64, 256, 256, 128, 8),
+    ("fine_decode", 40, 256, 128, 64, 8),
+    ("fine_decode", 24, 256, 256, 32, 4),
 ]
 
 
@@ -79,7 +82,7 @@ def test_single_launch_matches_oracle_and_multi_kernel(moe, name, T, H, I, E, k,
     assert plan["single_launch"] == 1 and plan["kernel_launches"] == 1
     fused = _run(moe, d, FUSED)
     multi = _run(moe, d, MULTI)
-    assert rel_err(fused.float().cpu().numpy(), _ref(L), f"single launch {name} T={T} E={E}") <= TOL["bf16"]
+    assert_parity(fused.float().cpu().numpy(), _ref(L), "bf16", f"single launch {name} T={T} E={E}")
     assert torch.equal(fused, multi)
 
 
@@ -90,7 +93,7 @@ def test_single_launch_k_splits(moe, split_k):
     d = _dev(L)
     f = _run(moe, d, {"single_launch": 1, "split_k": split_k})
     m = _run(moe, d, {"single_launch": 2, "split_k": split_k})
-    assert rel_err(f.float().cpu().numpy(), _ref(L), f"split_k={split_k}") <= TOL["bf16"]
+    assert_parity(f.float().cpu().numpy(), _ref(L), "bf16", f"split_k={split_k}")
     assert torch.equal(f, m)
 
 
@@ -100,7 +103,7 @@ def test_single_launch_intermediate_single_or_hi_lo(moe, act_split):
     d = _dev(L)
     f = _run(moe, d, {"single_launch": 1, "act_split": act_split})
     m = _run(moe, d, {"single_launch": 2, "act_split": act_split})
-    assert rel_err(f.float().cpu().numpy(), _ref(L), f"act_split={act_split}") <= TOL["bf16"]
+    assert_parity(f.float().cpu().numpy(), _ref(L), "bf16", f"act_split={act_split}")
     assert torch.equal(f, m)
 
 
@@ -185,7 +188,7 @@ def test_single_launch_full_size(moe, name, M):
         assert torch.equal(f, m)
     cpu = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in L.items()}
     ref = oracle.moe_forward(cpu["X"], cpu["Wr"], cpu["W13"], cpu["W2"], sp.k, sp.renorm)["out"]
-    assert rel_err(f.float().cpu().numpy(), ref, f"single launch {name} M={M}") <= TOL["bf16"]
+    assert_parity(f.float().cpu().numpy(), ref, "bf16", f"single launch {name} M={M}")
 
 
 @pytest.mark.parametrize("M", [16, 64])

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import TOL, make_tie_free, rel_err
+from helpers import TOL, assert_parity, make_tie_free, rel_err
 from moe_synth import INT4_NIBBLE_OF, make_layer, spec
 
 pytestmark = pytest.mark.gpu
@@ -56,7 +56,7 @@ def test_int4_layer_matches_oracle(moe, T, H, I, E, k):
     sp = L["spec"]
     ref = oracle.moe_forward(L["X"], L["Wr"], L["W13"], L["W2"], sp.k, sp.renorm, L["w13_scale"], L["w2_scale"],
                              w_format="int4")["out"]
-    assert rel_err(out.float().cpu().numpy(), ref, f"int4 T={T}") <= TOL["bf16"]
+    assert_parity(out.float().cpu().numpy(), ref, "bf16", f"int4 T={T}")
 
 
 @pytest.mark.parametrize("T,splits,act_split", [(3, 1, 2), (3, 2, 2), (20, 1, 2), (48, 1, 2), (20, 1, 1), (3, 2, 1)])
@@ -142,4 +142,4 @@ def test_int4_decode_full_size(moe, M):
     cpu = {kk: (v.cpu() if isinstance(v, torch.Tensor) else v) for kk, v in L.items()}
     ref = oracle.moe_forward(cpu["X"], cpu["Wr"], cpu["W13"], cpu["W2"], sp.k, sp.renorm, cpu["w13_scale"],
                              cpu["w2_scale"], tokens=tokens.astype(np.int32), w_format="int4")["out"]
-    assert rel_err(out.float().cpu().numpy()[tokens], ref, f"int4 full M={M}") <= TOL["bf16"]
+    assert_parity(out.float().cpu().numpy()[tokens], ref, "bf16", f"int4 full M={M}")
