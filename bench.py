@@ -410,66 +410,106 @@ def run_rope(dev, pk, steps=200):
     return out
 
 
-def run_offload(dev, steps=48, warm=8, slots=48, M=8):
+def run_offload(dev, steps=48, warm=8, slots=48, M=8, M_big=64, steps_big=12):
     """The expert cache on the fine-grained decode layer (128 experts of 9.4 MB, all in pinned host
     memory; `slots` of them in HBM): a sequence of Zipf-routed batches, each call timed end to end
-    (routing, the host read-back and slot plan, the copies of missing experts, the expert steps),
-    against the same batches with every expert resident."""
-    import time
-
+    (routing, the host read-back and slot plan, the copies of missing experts, the expert steps), in
+    each copy mode, against the same batches with every expert resident; then M_big-token batches,
+    which need more experts than slots (passes).  Also the host -> device copy bandwidth of one
+    expert's weights by the copy engine (pinned cudaMemcpyAsync) and by the cache's copy kernel."""
     import mixture_experts_layer_scan_gb300 as moe
 
-    sp = spec("fine_decode", T=M)
+    sp = spec("fine_decode", T=M_big)
     L = make_layer(sp, device="cpu")
     w13h, w2h = L["W13"].pin_memory(), L["W2"].pin_memory()
     W13, W2, Wr = L["W13"].to(dev), L["W2"].to(dev), L["Wr"].to(dev)
-    batches = []
-    for b in range(warm + steps):
-        resample_tokens(L, torch.arange(M), 7000 + b)
-        batches.append(L["X"].to(dev))
-    cache = moe.ExpertCache(w13h, w2h, n_slots=slots, max_tokens=M, topk=sp.k)
-    ws = torch.empty(cache.workspace_size(M), dtype=torch.uint8, device=dev)
-    out = torch.empty_like(batches[0])
-    for X in batches[:warm]:
-        cache.forward(X, Wr, sp.renorm, out=out, workspace=ws)
-    torch.cuda.synchronize()
-    st0 = cache.stats()
-    t0 = time.perf_counter()
-    for X in batches[warm:]:
-        cache.forward(X, Wr, sp.renorm, out=out, workspace=ws)
-    torch.cuda.synchronize()
-    cached_ms = (time.perf_counter() - t0) / steps * 1e3
-    st1 = cache.stats()
-    assert moe.moe_get_status() == 0
-    wsr = torch.empty(moe.moe_workspace_size(M, sp.H, sp.I, sp.E, sp.k, moe.MOE_BF16, moe.MOE_BF16), dtype=torch.uint8,
-                      device=dev)
-    for X in batches[:warm]:
-        moe.moe_forward(X, Wr, W13, W2, sp.k, sp.renorm, out=out, workspace=wsr)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for X in batches[warm:]:
-        moe.moe_forward(X, Wr, W13, W2, sp.k, sp.renorm, out=out, workspace=wsr)
-    torch.cuda.synchronize()
-    resident_ms = (time.perf_counter() - t0) / steps * 1e3
-    # host -> device copy bandwidth of one expert's weights (pinned source)
-    dst = torch.empty(W13[0].numel() + W2[0].numel(), dtype=torch.bfloat16, device=dev)
+
+    def batches(T, n, seed0):
+        out = []
+        for b in range(n):
+            resample_tokens(L, torch.arange(M_big), seed0 + b)
+            out.append(L["X"][:T].contiguous().to(dev))
+        return out
+
+    small = batches(M, warm + steps, 7000)
+    big = batches(M_big, 2 + steps_big, 9000)
+    res = {"workload": f"fine_decode_M{M}", "experts": sp.E, "expert_mb": round((3 * sp.H * sp.I * 2) / 2 ** 20, 2),
+           "slots": slots, "steps": steps,
+           "timing": "host wall clock per call, eager (the cached call synchronises on its routing)"}
+
+    def run_cached(mode, xs, n_warm, T):
+        cache = moe.ExpertCache(w13h, w2h, n_slots=slots, max_tokens=M_big, topk=sp.k)
+        cache.set_copy_mode(mode)
+        ws = torch.empty(cache.workspace_size(T), dtype=torch.uint8, device=dev)
+        out = torch.empty(T, sp.H, dtype=torch.bfloat16, device=dev)
+        for X in xs[:n_warm]:
+            cache.forward(X, Wr, sp.renorm, out=out, workspace=ws)
+        torch.cuda.synchronize()
+        st0 = cache.stats()
+        t0 = time.perf_counter()
+        for X in xs[n_warm:]:
+            cache.forward(X, Wr, sp.renorm, out=out, workspace=ws)
+        torch.cuda.synchronize()
+        ms = (time.perf_counter() - t0) / (len(xs) - n_warm) * 1e3
+        st1 = cache.stats()
+        assert moe.moe_get_status() == 0
+        cache.close()
+        d = {k: st1[k] - st0[k] for k in st1}
+        return ms, d
+
+    def run_resident(xs, n_warm, T):
+        wsr = torch.empty(moe.moe_workspace_size(T, sp.H, sp.I, sp.E, sp.k, moe.MOE_BF16, moe.MOE_BF16),
+                          dtype=torch.uint8, device=dev)
+        out = torch.empty(T, sp.H, dtype=torch.bfloat16, device=dev)
+        for X in xs[:n_warm]:
+            moe.moe_forward(X, Wr, W13, W2, sp.k, sp.renorm, out=out, workspace=wsr)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for X in xs[n_warm:]:
+            moe.moe_forward(X, Wr, W13, W2, sp.k, sp.renorm, out=out, workspace=wsr)
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t0) / (len(xs) - n_warm) * 1e3
+
+    modes = {"overlap": moe.CACHE_COPY_OVERLAP, "serial": moe.CACHE_COPY_SERIAL, "copy_kernel": moe.CACHE_COPY_KERNEL}
+    res["resident_ms_per_call"] = run_resident(small, warm, M)
+    res["resident_tokens_per_s"] = M / (res["resident_ms_per_call"] * 1e-3)
+    for name, mode in modes.items():
+        try:
+            ms, d = run_cached(mode, small, warm, M)
+        except moe.MoeError as e:
+            res[f"cached_{name}"] = {"unavailable": str(e)}
+            continue
+        distinct = d["hits"] + d["misses"]
+        res[f"cached_{name}"] = {"ms_per_call": ms, "tokens_per_s": M / (ms * 1e-3),
+                                 "hit_rate": d["hits"] / max(1, distinct), "misses_per_call": d["misses"] / steps,
+                                 "h2d_bytes_per_call": d["bytes_h2d"] / steps}
+    ms, d = run_cached(moe.CACHE_COPY_OVERLAP, big, 2, M_big)
+    rb = run_resident(big, 2, M_big)
+    res[f"fine_decode_M{M_big}"] = {"cached_ms_per_call": ms, "resident_ms_per_call": rb,
+                                    "cached_tokens_per_s": M_big / (ms * 1e-3), "passes_per_call": d["passes"] / steps_big,
+                                    "misses_per_call": d["misses"] / steps_big,
+                                    "h2d_bytes_per_call": d["bytes_h2d"] / steps_big, "copy_mode": "overlap"}
+    # host -> device copy bandwidth of one expert's weights, both methods
     src = torch.cat([w13h[0].flatten(), w2h[0].flatten()]).pin_memory()
+    dst = torch.empty_like(src, device=dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(3):
+        dst.copy_(src, non_blocking=True)
     e0.record()
     for _ in range(20):
         dst.copy_(src, non_blocking=True)
     e1.record()
     torch.cuda.synchronize()
-    h2d_gbs = 20 * src.numel() * 2 / (e0.elapsed_time(e1) * 1e-3) / 1e9
-    d = {k: st1[k] - st0[k] for k in st1}
-    cache.close()
-    distinct = d["hits"] + d["misses"]
-    return {"workload": f"fine_decode_M{M}", "experts": sp.E, "expert_mb": round((3 * sp.H * sp.I * 2) / 2 ** 20, 2),
-            "slots": slots, "steps": steps, "cached_ms_per_call": cached_ms, "resident_ms_per_call": resident_ms,
-            "cached_tokens_per_s": M / (cached_ms * 1e-3), "resident_tokens_per_s": M / (resident_ms * 1e-3),
-            "hit_rate": d["hits"] / max(1, distinct), "misses_per_call": d["misses"] / steps,
-            "h2d_bytes_per_call": d["bytes_h2d"] / steps, "h2d_gbs_pinned_copy": h2d_gbs,
-            "timing": "host wall clock per call, eager, both paths (the cached call synchronises on its routing)"}
+    res["h2d_gbs_copy_engine"] = 20 * src.numel() * 2 / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    for _ in range(3):
+        moe.moe_copy_from_host(src, dst)
+    e0.record()
+    for _ in range(20):
+        moe.moe_copy_from_host(src, dst)
+    e1.record()
+    torch.cuda.synchronize()
+    res["h2d_gbs_copy_kernel"] = 20 * src.numel() * 2 / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    return res
 
 
 def cpu_baseline(L, sp, budget_s=20.0):

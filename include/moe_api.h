@@ -294,30 +294,50 @@ MOE_API int moe_forward_routed(const void* hidden, const float* topk_w, const in
                                void* workspace, size_t workspace_bytes, const moe_options* opts, moe_stream_t stream);
 
 /* Expert cache ("FusedMoE vs MegaMoE", section 4: MegaMoE keeps expert weights
- * in host memory and stages the experts a batch needs into GPU memory, loading
- * synchronously on a miss).  The cache owns a pool of n_slots expert slots in
- * device memory; the full weights stay in host memory (on a GB300 the Grace
- * CPU's, over NVLink-C2C).  Each moe_forward_cached call routes the batch on
- * the GPU, reads the expert ids back (one host synchronisation per call), keeps
- * the experts already resident, copies the missing ones into free slots or the
- * slots of the least recently used experts this call does not need (one
- * cudaMemcpyAsync per weight matrix on the cache's copy stream), and runs the
- * expert part of the layer over the slots (moe_forward_routed).  Results equal
- * moe_forward's on the same weights.  Prediction of future experts is not built. */
+ * in host memory, stages the experts a batch needs into GPU memory with an LRU
+ * policy and overlaps the copies with computation on separate CUDA streams
+ * synchronised by events; sections 4.1 and 4.2).  The cache owns a pool of
+ * n_slots expert slots in device memory; the full weights stay in host memory
+ * (on a GB300 the Grace CPU's, over NVLink-C2C).  Each moe_forward_cached call
+ * routes the batch on the GPU, reads the expert ids back (one host
+ * synchronisation per call), keeps the experts already resident, copies the
+ * missing ones into free slots or the slots of the least recently used experts
+ * the call does not need, and runs the expert part of the layer over the slots.
+ * By default (MOE_CACHE_COPY_OVERLAP) the copies run on the cache's copy stream
+ * while the expert kernels already compute the resident experts: a per-slot
+ * readiness word, written on the copy stream after each weight matrix lands,
+ * gates the GEMMs' weight streaming per expert (a bounded wait).  A call needing
+ * more distinct experts than slots runs in passes of at most n_slots experts
+ * (resident ones first) with one combine at the end.  Results equal
+ * moe_forward's on the same weights given the same plan (the expert count of the
+ * plan is n_slots).  Prediction of future experts is not built. */
 typedef struct moe_expert_cache moe_expert_cache;
 typedef struct {
   unsigned long long calls, hits, misses, evictions, bytes_h2d;
+  unsigned long long passes; /* expert passes run (one per call unless a call needs more experts than slots) */
 } moe_cache_stats_t;
+
+/* How a cache brings missing experts in (moe_cache_set_copy_mode). */
+enum {
+  MOE_CACHE_COPY_OVERLAP = 0, /* copy engine on the copy stream, overlapped with the expert kernels (default) */
+  MOE_CACHE_COPY_SERIAL = 1,  /* copy engine; the expert kernels start after every copy of the pass */
+  MOE_CACHE_COPY_KERNEL = 2   /* a copy kernel on the caller's stream reads the host weights directly
+                                 (needs host memory the device can address), then the expert kernels */
+};
 
 /* host_w13 [E][2I][H], host_w2 [E][H][I] in host memory (registered as page-locked
  * by the cache unless already pinned, unregistered at destroy); w_dtype MOE_BF16 or
  * MOE_E4M3 (then host_w13_scale / host_w2_scale [E] fp32, read at each miss).
- * topk <= n_slots <= E device slots; calls take T <= max_tokens tokens and need at most
- * n_slots distinct experts (else MOE_ERR_UNSUPPORTED).  H % 128 == 0, I % 128 == 0.
+ * topk <= n_slots <= E device slots; calls take T <= max_tokens tokens.  FP8 calls
+ * must fit in one pass (at most n_slots distinct experts, else MOE_ERR_UNSUPPORTED):
+ * their intermediate scale spans every pair of the call.  H % 128 == 0, I % 128 == 0.
  * The cache allocates its device and pinned buffers here (cudaMalloc), none per call. */
 MOE_API int moe_cache_create(const void* host_w13, const void* host_w2, const float* host_w13_scale,
                              const float* host_w2_scale, int E, int H, int I, moe_dtype w_dtype, int n_slots,
                              int max_tokens, int topk, moe_expert_cache** cache);
+/* MOE_CACHE_COPY_*; MOE_ERR_UNSUPPORTED for MOE_CACHE_COPY_KERNEL when the device cannot
+ * address the host weights. */
+MOE_API int moe_cache_set_copy_mode(moe_expert_cache* cache, int mode);
 MOE_API int moe_cache_destroy(moe_expert_cache* cache);
 /* Workspace bytes of a moe_forward_cached call with T tokens. */
 MOE_API int moe_cache_workspace_size(const moe_expert_cache* cache, int T, moe_dtype act_dtype,
@@ -328,11 +348,17 @@ MOE_API int moe_forward_cached(moe_expert_cache* cache, const void* hidden, cons
                                moe_dtype act_dtype, void* out, void* workspace, size_t workspace_bytes,
                                const moe_options* opts, moe_stream_t stream);
 MOE_API int moe_cache_stats(const moe_expert_cache* cache, moe_cache_stats_t* stats);
+/* The cache's copy kernel on its own: copies `bytes` (a multiple of 16) from src_host,
+ * page-locked host memory the device can address (reads cross NVLink-C2C on a GB300),
+ * to the device buffer dst, on `stream`; both 16-byte aligned.  MOE_ERR_UNSUPPORTED if the
+ * device cannot address src_host. */
+MOE_API int moe_copy_from_host(const void* src_host, void* dst, size_t bytes, moe_stream_t stream);
+
 /* The cache's slot policy alone, host only (no device work): over n_calls calls of
- * `pairs` expert ids each (ids [n_calls][pairs]), writes the slot of every id
- * (slot_ids [n_calls][pairs]) and, per call, the expert copied into each slot or -1
- * (loaded_expert [n_calls][n_slots]); totals of hits and misses (distinct experts
- * per call found / not found in a slot). */
+ * `pairs` expert ids each (ids [n_calls][pairs]), writes the slot of every id during
+ * its pass (slot_ids [n_calls][pairs]) and, per call, the expert last copied into each
+ * slot or -1 (loaded_expert [n_calls][n_slots]); totals of hits and misses (distinct
+ * experts per pass found / not found in a slot). */
 MOE_API int moe_cache_lru_plan(int E, int n_slots, int n_calls, int pairs, const int32_t* ids, int32_t* slot_ids,
                                int32_t* loaded_expert, unsigned long long* hits, unsigned long long* misses);
 

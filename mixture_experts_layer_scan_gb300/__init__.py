@@ -32,7 +32,8 @@ TRACE_WORDS = len(TRACE_EVENTS)
 EXPORTS = ("moe_strerror", "moe_workspace_size", "moe_plan_info", "moe_align_capacity", "moe_route",
            "moe_topk_from_logits", "moe_align", "moe_forward", "moe_forward_noalloc", "moe_get_status",
            "moe_version", "moe_inv_rope_fp8_quant", "moe_forward_routed", "moe_cache_create", "moe_cache_destroy",
-           "moe_cache_workspace_size", "moe_forward_cached", "moe_cache_stats", "moe_cache_lru_plan")
+           "moe_cache_workspace_size", "moe_forward_cached", "moe_cache_stats", "moe_cache_lru_plan",
+           "moe_cache_set_copy_mode", "moe_copy_from_host")
 NOALLOC_MAX_WORKSPACE = 32 << 20
 
 
@@ -56,7 +57,10 @@ class moe_plan(ctypes.Structure):
 
 
 class moe_cache_stats_t(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_ulonglong) for n in ("calls", "hits", "misses", "evictions", "bytes_h2d")]
+    _fields_ = [(n, ctypes.c_ulonglong) for n in ("calls", "hits", "misses", "evictions", "bytes_h2d", "passes")]
+
+
+CACHE_COPY_OVERLAP, CACHE_COPY_SERIAL, CACHE_COPY_KERNEL = 0, 1, 2
 
 
 def _load():
@@ -92,6 +96,10 @@ def _load():
     lib.moe_cache_create.argtypes = [P, P, P, P, i, i, i, i, i, i, i, ctypes.POINTER(P)]
     lib.moe_cache_destroy.restype = i
     lib.moe_cache_destroy.argtypes = [P]
+    lib.moe_cache_set_copy_mode.restype = i
+    lib.moe_cache_set_copy_mode.argtypes = [P, i]
+    lib.moe_copy_from_host.restype = i
+    lib.moe_copy_from_host.argtypes = [P, P, sz, P]
     lib.moe_cache_workspace_size.restype = i
     lib.moe_cache_workspace_size.argtypes = [P, i, i, P, ctypes.POINTER(sz)]
     lib.moe_forward_cached.restype = i
@@ -332,6 +340,10 @@ class ExpertCache:
                                      self.I, _dt(w13), n_slots, max_tokens, topk, ctypes.byref(h)), "moe_cache_create")
         self._h = h
 
+    def set_copy_mode(self, mode: int) -> None:
+        """CACHE_COPY_OVERLAP (default), CACHE_COPY_SERIAL or CACHE_COPY_KERNEL."""
+        _check(_lib.moe_cache_set_copy_mode(self._h, int(mode)), "moe_cache_set_copy_mode")
+
     def close(self):
         if self._h is not None and self._h.value:
             _lib.moe_cache_destroy(self._h)
@@ -365,6 +377,15 @@ class ExpertCache:
         st = moe_cache_stats_t()
         _check(_lib.moe_cache_stats(self._h, ctypes.byref(st)), "moe_cache_stats")
         return {n: int(getattr(st, n)) for n, _ in moe_cache_stats_t._fields_}
+
+
+def moe_copy_from_host(src: torch.Tensor, dst: torch.Tensor, stream=None) -> torch.Tensor:
+    """The expert cache's copy kernel: src (pinned host tensor) -> dst (device tensor, same bytes)."""
+    n = src.numel() * src.element_size()
+    if src.is_cuda or not dst.is_cuda or dst.numel() * dst.element_size() != n:
+        raise ValueError("src must be a host tensor and dst a device tensor of the same size")
+    _check(_lib.moe_copy_from_host(_p(src), _p(dst), n, _stream(stream)), "moe_copy_from_host")
+    return dst
 
 
 def moe_cache_lru_plan(E: int, n_slots: int, ids):

@@ -275,18 +275,21 @@ static cudaError_t launch_router(const void* X, const void* Wr, int T, int H, in
   return launch_router_logits(X, Wr, T, H, E, act == MOE_BF16, logits, s);
 }
 
-enum { STEPS_ROUTE = 1, STEPS_EXPERTS = 2, STEPS_ALL = 3 };
+enum { STEPS_ROUTE = 1, STEPS_EXPERTS = 2, STEPS_COMBINE = 4, STEPS_ALL = 7 };
 
 // The launch sequence of one layer call on a planned, validated workspace.
-// steps selects routing (S1-S2) and/or the expert part (S3-S7, which reads
-// the routing from the workspace).  E_router is the router's expert count
-// and logits_override an optional logits buffer (both differ from the plan's
-// when the experts are cache slots).
+// steps selects routing (S1-S2), the expert part (S3-S6, which reads the
+// routing from the workspace or tw_in / tid_in) and the combine (S7).
+// E_router is the router's expert count and logits_override an optional
+// logits buffer (both differ from the plan's when the experts are cache
+// slots).  gate (nullable) makes the GEMMs wait for per-slot readiness words;
+// skip_minus_one drops pairs whose id is -1 from the permutation.
 static int forward_steps(const Plan& pl, int steps, const void* hidden, const void* router_w, int E_router,
                          float* logits_override, const float* tw_in, const int32_t* tid_in, const void* w13,
                          const void* w2, int T, int H, int I, int E, int topk, int renorm, moe_dtype act_dtype,
                          const void* w13_scale, const void* w2_scale, void* out, void* workspace,
-                         const moe_options* opts, int* st, int sms, cudaStream_t s) {
+                         const moe_options* opts, int* st, int sms, cudaStream_t s, const SlotGate* gate = nullptr,
+                         bool skip_minus_one = false) {
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* logits = logits_override ? logits_override : reinterpret_cast<float*>(ws + pl.o_logits);
   // the routing: written here by steps 1-2, or given by the caller for the expert steps alone
@@ -382,11 +385,12 @@ static int forward_steps(const Plan& pl, int steps, const void* hidden, const vo
     MOE_TRY(launch_topk(logits, T, E_router, topk, renorm != 0, tw, tid, s));
     if (o) record(o->stage_end[MOE_STAGE_ROUTE], s);
   }
-  if (!(steps & STEPS_EXPERTS)) return MOE_OK;
+  if (!(steps & (STEPS_EXPERTS | STEPS_COMBINE))) return MOE_OK;
+  if (!(steps & STEPS_EXPERTS)) goto combine_step;
 
   // 3. permutation
   if (o) record(o->stage_begin[MOE_STAGE_ALIGN], s);
-  MOE_TRY(launch_align(tid, T, topk, E, pl.B, sorted, eids, meta + META_NPP, nullptr, meta, st, s));
+  MOE_TRY(launch_align(tid, T, topk, E, pl.B, sorted, eids, meta + META_NPP, nullptr, meta, st, s, skip_minus_one));
   if (o) record(o->stage_end[MOE_STAGE_ALIGN], s);
 
   // 4. activations: the fp32 path gathers rows into expert order here; the
@@ -432,6 +436,7 @@ static int forward_steps(const Plan& pl, int steps, const void* hidden, const vo
     g.meta = meta;
     g.status = st;
     g.num_sms = sms;
+    g.want = gate ? gate->want : nullptr;
 
     // 5. GEMM1 on w13 (+ SiLU(gate)*up)
     TcGemmArgs g1 = g;
@@ -451,6 +456,7 @@ static int forward_steps(const Plan& pl, int steps, const void* hidden, const vo
     g1.w4_scale = w4 ? w13_scale : nullptr;
     g1.a_amax = amax;
     g1.amax_out = amax + 1;
+    g1.ready = gate ? gate->ready13 : nullptr;
     void* aint_lo = pl.act_split ? (void*)((uint16_t*)aint + (size_t)cap * I) : nullptr;
     if (pl.s1 > 1) {
       g1.epi = TC_EPI_G1_PART;
@@ -495,6 +501,7 @@ static int forward_steps(const Plan& pl, int steps, const void* hidden, const vo
     g2.out = y;
     g2.out_split_stride = pl.y_stride;
     g2.epi = pl.y_bf16 ? TC_EPI_G2_BF16 : TC_EPI_G2_F32;
+    g2.ready = gate ? gate->ready2 : nullptr;
     // GEMM2's predecessor is GEMM1 or a kernel GEMM1 let launch, and GEMM1 lets
     // its dependents launch only after its own dependency wait: the permutation
     // metadata is complete by then, so GEMM2 may stream weights early.
@@ -504,6 +511,9 @@ static int forward_steps(const Plan& pl, int steps, const void* hidden, const vo
     if (o) record(o->stage_end[MOE_STAGE_GEMM2], s);
   }
 
+  if (!(steps & STEPS_COMBINE)) return MOE_OK;
+
+combine_step:
   // 7. combine
   if (o) record(o->stage_begin[MOE_STAGE_COMBINE], s);
   MOE_TRY(launch_combine(y, pl.y_bf16 ? 1 : 0, pl.s2, pl.y_stride, tw, T, topk, H, out, act_dtype == MOE_BF16 ? 1 : 0,
@@ -668,8 +678,8 @@ int moe_forward_routed(const void* hidden, const float* topk_w, const int32_t* t
   int* st = status_word();
   const int sms = num_sms();
   if (!st || sms <= 0) return MOE_ERR_CUDA;
-  return forward_steps(pl, STEPS_EXPERTS, hidden, nullptr, E, nullptr, topk_w, topk_ids, w13, w2, T, H, I, E, topk,
-                       0, act_dtype, w13_scale, w2_scale, out, workspace, opts ? &o : nullptr, st, sms,
+  return forward_steps(pl, STEPS_EXPERTS | STEPS_COMBINE, hidden, nullptr, E, nullptr, topk_w, topk_ids, w13, w2, T,
+                       H, I, E, topk, 0, act_dtype, w13_scale, w2_scale, out, workspace, opts ? &o : nullptr, st, sms,
                        reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -705,3 +715,29 @@ int moe_get_status(moe_stream_t stream) {
 }
 
 }  // extern "C"
+
+namespace moe {
+
+int forward_routed_pass(const void* hidden, const float* topk_w, const int32_t* ids, const void* w13, const void* w2,
+                        int T, int H, int I, int E, int topk, moe_dtype act_dtype, moe_dtype w_dtype,
+                        const void* w13_scale, const void* w2_scale, void* out, void* workspace,
+                        size_t workspace_bytes, const moe_options* opts, cudaStream_t stream, bool experts,
+                        bool combine, const SlotGate* gate) {
+  moe_options o = opts ? *opts : moe_options{};
+  o.single_launch = 2;
+  if (o.inject_timeout) return MOE_ERR_ARG;
+  Plan pl;
+  int rc = make_plan(T, H, I, E, topk, act_dtype, w_dtype, &o, &pl);
+  if (rc) return rc;
+  if (T == 0 || (!experts && !combine)) return MOE_OK;
+  if (!hidden || !topk_w || !ids || !out || !workspace || (experts && (!w13 || !w2))) return MOE_ERR_ARG;
+  if (workspace_bytes < pl.total) return MOE_ERR_WORKSPACE;
+  int* st = status_word();
+  const int sms = num_sms();
+  if (!st || sms <= 0) return MOE_ERR_CUDA;
+  const int steps = (experts ? STEPS_EXPERTS : 0) | (combine ? STEPS_COMBINE : 0);
+  return forward_steps(pl, steps, hidden, nullptr, E, nullptr, topk_w, ids, w13, w2, T, H, I, E, topk, 0, act_dtype,
+                       w13_scale, w2_scale, out, workspace, &o, st, sms, stream, gate, true);
+}
+
+}  // namespace moe

@@ -141,6 +141,34 @@ __device__ __forceinline__ bool mbar_wait_all(uint32_t bar, uint32_t parity, vol
   }
 }
 
+// Warp-wide bounded wait until the global word *word equals want (acquire).
+// Used for words written by another engine (a copy stream's in-order writes
+// after the data they announce); the data is then read through TMA, so the
+// async proxy is ordered after the observation.
+__device__ __forceinline__ bool wait_word_all(const unsigned* word, unsigned want, volatile int* abort, int* status) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(word) : "memory");
+    if (__all_sync(0xffffffffu, v == want)) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      return true;
+    }
+    if (it == 0) t0 = globaltimer_ns();
+    if ((it & 15u) == 15u) {
+      const bool give_up = *abort || (globaltimer_ns() - t0 > kWaitLimitNs);
+      if (__any_sync(0xffffffffu, give_up)) {
+        if ((threadIdx.x & 31) == 0 && !*abort) {
+          *abort = 1;
+          report(status, MOE_ERR_DEVICE_TIMEOUT);
+        }
+        return false;
+      }
+    }
+    __nanosleep(256);
+  }
+}
+
 // Drain wait used on the abort path only: ignores the abort flag, own limit.
 __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();

@@ -59,6 +59,8 @@ struct TcDev {
   int stack_lo;     // swap-AB GEMM2 with a hi/lo activation: one MMA over the hi rows then the lo rows
                     // (N = xbox + npad), the two column groups summed in the epilogue
   uint32_t stage_bytes, w_bytes, bar_off;
+  const unsigned* ready;  // nullable: expert e's weights are streamed once ready[e] == want[e]
+  const unsigned* want;
   const int32_t* sorted;
   const int32_t* eids;
   const int32_t* meta;
@@ -360,7 +362,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       return p.w_bytes + (uint32_t)(x_rows(d) * 128 * parts);
     };
     int pre = 0;
-    if (p.early && lane == 0 && (int)blockIdx.x < ntiles) {
+    if (p.early && !p.ready && lane == 0 && (int)blockIdx.x < ntiles) {
       const Tile d = tile_at<SWAP, EPI>(p, blockIdx.x);
       pre = min(p.stages, d.kb1 - d.kb0);
       for (int i = 0; i < pre; ++i) {
@@ -380,6 +382,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     bool ok = true;
     for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
       const Tile d = tile_at<SWAP, EPI>(p, t);
+      // expert cache: this expert's weights may still be on their way into its slot
+      if (p.ready && !wait_word_all(p.ready + d.e, p.want[d.e], abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
       int rows[2][4];  // token rows of this lane's gather groups g = lane and lane + 32
       if (p.gather) {
 #pragma unroll
@@ -1044,7 +1051,7 @@ static cudaError_t launch_gemm_w4(const TcGemmArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s) {
-  if (a.w4) return launch_gemm_w4(a, s);
+  if (a.w4) return a.ready ? cudaErrorInvalidValue : launch_gemm_w4(a, s);
   const int eb = a.fp8 ? 1 : 2;
   CUtensorMap mw, mx;
   if (!make_tensor_map_2d(&mw, a.W, eb, (uint64_t)a.K, (uint64_t)a.E * a.w_rows_per_expert, (uint32_t)a.wbox))
@@ -1096,6 +1103,8 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s) {
   p.a_amax = a.a_amax;
   p.amax_out = a.amax_out;
   p.status = a.status;
+  p.ready = a.ready;
+  p.want = a.ready ? a.want : nullptr;
 
   p.w_bytes = (uint32_t)(2 * a.wbox * 128);
   p.stage_bytes = p.w_bytes + (uint32_t)(a.xbox * 128) * (a.x_lo_rows ? 2u : 1u);

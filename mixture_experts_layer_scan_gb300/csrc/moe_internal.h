@@ -29,8 +29,11 @@ cudaError_t launch_topk(const float* logits, int T, int E, int k, int renorm, fl
 cudaError_t launch_inject_timeout(const int* flag, int* status, cudaStream_t s);
 
 // ---- permutation / data movement ----------------------------------------------
+// skip_minus_one: ids equal to -1 are pairs handled elsewhere (dropped silently); other ids
+// outside [0, E) are dropped and flagged MOE_ERR_DEVICE_INDEX
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int B, int32_t* sorted, int32_t* eids,
-                         int32_t* npp, int32_t* counts, int32_t* meta, int* status, cudaStream_t s);
+                         int32_t* npp, int32_t* counts, int32_t* meta, int* status, cudaStream_t s,
+                         bool skip_minus_one = false);
 // amax over n bf16 values -> *amax_bits (float bits, must be zeroed before)
 cudaError_t launch_amax_bf16(const void* X, size_t n, unsigned* amax_bits, cudaStream_t s);
 // Xs[r] = X[sorted[r]/k] (zero rows for the sentinel) for r < num_post_pad;
@@ -111,6 +114,10 @@ struct TcGemmArgs {
   int num_sms;
   bool w4;                  // INT4 weight codes (swap-AB), dequantised to bf16 in the main loop
   const void* w4_scale;     // bf16 group scales [E][K / 128][w_rows_per_expert]
+  // expert cache: before streaming expert e's weights the producer waits (bounded) until
+  // ready[e] == want[e] (words written by the cache's copy stream after each copy); nullable
+  const unsigned* ready;
+  const unsigned* want;
 };
 cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s);
 
@@ -161,5 +168,25 @@ cudaError_t launch_decode_fused(const FusedArgs& a, cudaStream_t s);
 
 // status word of the current device
 int* status_word();
+
+// ---- expert cache passes (moe_cache.cu) -----------------------------------------------
+// Per-slot readiness words: GEMM1 streams slot e's w13 once ready13[e] == want[e], GEMM2
+// its w2 once ready2[e] == want[e].  Null members: no waiting.
+struct SlotGate {
+  const unsigned* ready13;
+  const unsigned* ready2;
+  const unsigned* want;
+};
+// Steps of the layer on a given routing (as moe_forward_routed), for the expert cache:
+//   experts: permutation + GEMMs of the pairs whose id is not -1 (ids -1 are skipped
+//            silently: another pass computes them); Y rows of those pairs are written
+//   combine: the weighted sum of every pair's Y rows into out
+// The plan depends only on (T, H, I, E, topk, dtypes, options), so passes over disjoint
+// pair sets with the same arguments share the workspace's Y buffers and one combine.
+int forward_routed_pass(const void* hidden, const float* topk_w, const int32_t* ids, const void* w13, const void* w2,
+                        int T, int H, int I, int E, int topk, moe_dtype act_dtype, moe_dtype w_dtype,
+                        const void* w13_scale, const void* w2_scale, void* out, void* workspace,
+                        size_t workspace_bytes, const moe_options* opts, cudaStream_t stream, bool experts,
+                        bool combine, const SlotGate* gate);
 
 }  // namespace moe

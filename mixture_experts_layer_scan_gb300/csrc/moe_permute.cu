@@ -64,7 +64,7 @@ __device__ int block_exclusive_scan(int v, int* scratch /* >= 33 ints */, int* t
 __global__ void __launch_bounds__(kAlignThreads, 1)
     k_align(const int32_t* __restrict__ ids, int T, int k, int E, int B, int32_t* __restrict__ sorted,
             int32_t* __restrict__ eids, int32_t* __restrict__ npp_out, int32_t* __restrict__ counts_out,
-            int32_t* __restrict__ meta, int* status) {
+            int32_t* __restrict__ meta, int* status, int skip_minus_one) {
   pdl_enter();
   cg::cluster_group cluster = cg::this_cluster();
   const int csize = (int)cluster.num_blocks();
@@ -93,7 +93,8 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
     int e = -1;
     if (f < end) {
       e = ids[f];
-      if (e < 0 || e >= E) { bad = true; e = -1; }
+      // -1 marks a pair another pass handles (skip_minus_one): dropped without a flag
+      if (e < 0 || e >= E) { bad = bad || !(skip_minus_one && e == -1); e = -1; }
     }
     const unsigned grp = __match_any_sync(0xffffffffu, e);
     if (e >= 0 && lane == __ffs(grp) - 1) wc[warp * E + e] += __popc(grp);
@@ -474,7 +475,8 @@ int grid_for(size_t work, int threads, int cap_blocks = 152 * 16) {
 }  // namespace
 
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int B, int32_t* sorted, int32_t* eids,
-                         int32_t* npp, int32_t* counts, int32_t* meta, int* status, cudaStream_t s) {
+                         int32_t* npp, int32_t* counts, int32_t* meta, int* status, cudaStream_t s,
+                         bool skip_minus_one) {
   const size_t smem = (size_t)(kAlignWarps * E + 4 * E + 1 + 33) * sizeof(int);
   static bool configured[64] = {};
   int dev = 0;
@@ -499,7 +501,8 @@ cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int B, int32_t
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_align, ids, T, k, E, B, sorted, eids, npp, counts, meta, status);
+  return cudaLaunchKernelEx(&cfg, k_align, ids, T, k, E, B, sorted, eids, npp, counts, meta, status,
+                            skip_minus_one ? 1 : 0);
 }
 
 cudaError_t launch_amax_bf16(const void* X, size_t n, unsigned* amax_bits, cudaStream_t s) {
