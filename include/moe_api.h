@@ -142,11 +142,17 @@ typedef struct {
    * kernels of each stage (the caller creates and owns them). */
   moe_event_t stage_begin[MOE_NUM_STAGES];
   moe_event_t stage_end[MOE_NUM_STAGES];
+  int cta_pair;       /* TOKEN_MAJOR tensor-core GEMMs: 0 = automatic (CTA pairs when H % 256 == 0),
+                         1 = CTA pairs (MOE_ERR_UNSUPPORTED where they do not apply), 2 = single CTAs.
+                         On CTA pairs (tcgen05 cta_group::2) two SMs compute a 256-token x
+                         256-weight-row tile together, each staging half of both operands, and the
+                         permutation pads experts to 256 rows; on single CTAs, tiles of 128 tokens. */
 } moe_options;
 
 /* What moe_forward will run for a shape (filled by moe_plan_info). */
 typedef struct {
   int orientation;      /* MOE_ORIENT_SWAP_AB or MOE_ORIENT_TOKEN_MAJOR (0 on the fp32 path) */
+  /* (cta_pair below: 1 if the TOKEN_MAJOR GEMMs run on CTA pairs) */
   int block;            /* permutation block size B */
   int splits_gemm1;     /* K splits of GEMM1 / GEMM2 */
   int splits_gemm2;
@@ -154,6 +160,7 @@ typedef struct {
   int kernel_launches;  /* kernels one moe_forward call launches */
   int single_launch;    /* 1 if the whole layer runs as one cooperative kernel */
   size_t workspace_bytes;
+  int cta_pair;         /* 1 if the TOKEN_MAJOR GEMMs run on CTA pairs */
 } moe_plan;
 
 /* Human-readable text of a return code (static storage). */

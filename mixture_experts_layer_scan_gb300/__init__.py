@@ -47,13 +47,13 @@ class moe_options(ctypes.Structure):
     _fields_ = [("orientation", ctypes.c_int), ("split_k", ctypes.c_int), ("inject_timeout", ctypes.c_int),
                 ("act_split", ctypes.c_int), ("trace", ctypes.c_void_p), ("single_launch", ctypes.c_int),
                 ("stage_begin", ctypes.c_void_p * NUM_STAGES),
-                ("stage_end", ctypes.c_void_p * NUM_STAGES)]
+                ("stage_end", ctypes.c_void_p * NUM_STAGES), ("cta_pair", ctypes.c_int)]
 
 
 class moe_plan(ctypes.Structure):
     _fields_ = [("orientation", ctypes.c_int), ("block", ctypes.c_int), ("splits_gemm1", ctypes.c_int),
                 ("splits_gemm2", ctypes.c_int), ("act_split", ctypes.c_int), ("kernel_launches", ctypes.c_int),
-                ("single_launch", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t)]
+                ("single_launch", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t), ("cta_pair", ctypes.c_int)]
 
 
 class moe_cache_stats_t(ctypes.Structure):
@@ -164,6 +164,7 @@ def _opts(options) -> Optional[ctypes.POINTER(moe_options)]:
     o.inject_timeout = int(options.get("inject_timeout", 0))
     o.act_split = int(options.get("act_split", 0))
     o.single_launch = int(options.get("single_launch", 0))
+    o.cta_pair = int(options.get("cta_pair", 0))
     if options.get("trace") is not None:
         o.trace = ctypes.c_void_p(options["trace"].data_ptr())
     for name, ev in (options.get("stage_begin") or {}).items():

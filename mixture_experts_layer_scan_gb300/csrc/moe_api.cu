@@ -70,6 +70,7 @@ struct Plan {
   bool act_split = false;  // bf16 intermediate stored as hi + lo parts (two MMAs in GEMM2)
   bool gather_in_gemm = false;  // GEMM1 gathers its activation rows itself (TMA tile::gather4)
   bool fused = false;           // the whole layer as one cooperative kernel
+  bool pair = false;            // token-major GEMMs on CTA pairs (256-row permutation blocks)
   size_t o_sync = 0;
   size_t o_logits = 0, o_tw = 0, o_tid = 0, o_meta = 0, o_sorted = 0, o_eids = 0, o_xs = 0, o_aint = 0, o_af32 = 0,
          o_p1 = 0, o_y = 0, o_misc = 0, total = 0;
@@ -159,7 +160,11 @@ static int make_plan(int T, int H, int I, int E, int topk, moe_dtype act, moe_dt
       p.s2 = (kbt2 + p.kb2 - 1) / p.kb2;
       p.y_bf16 = false;
     } else {
-      p.B = 128;
+      const int pair_mode = opts ? opts->cta_pair : 0;
+      if (pair_mode < 0 || pair_mode > 2) return MOE_ERR_ARG;
+      p.pair = pair_mode != 2 && H % 256 == 0;
+      if (pair_mode == 1 && !p.pair) return MOE_ERR_UNSUPPORTED;
+      p.B = p.pair ? 256 : 128;
       p.xbox = 128;
       p.s1 = p.s2 = 1;
       p.kb1 = H * eb / 128;
@@ -437,6 +442,7 @@ static int forward_steps(const Plan& pl, int steps, const void* hidden, const vo
     g.status = st;
     g.num_sms = sms;
     g.want = gate ? gate->want : nullptr;
+    g.pair = pl.pair;
 
     // 5. GEMM1 on w13 (+ SiLU(gate)*up)
     TcGemmArgs g1 = g;
@@ -577,6 +583,7 @@ int moe_plan_info(int T, int H, int I, int E, int topk, moe_dtype act_dtype, moe
   info->kernel_launches = T > 0 ? n : 0;
   info->single_launch = p.fused ? 1 : 0;
   info->workspace_bytes = p.total;
+  info->cta_pair = p.pair ? 1 : 0;
   return MOE_OK;
 }
 

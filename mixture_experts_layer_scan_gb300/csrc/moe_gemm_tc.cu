@@ -56,6 +56,7 @@ struct TcDev {
   int d1_col;       // swap-AB: column of accumulator D1 (weight rows 128..255) inside a buffer
   int n_valid;      // router: valid output columns
   int x_lo_rows;    // >0: the activation operand also has a bf16 low part at row offset x_lo_rows
+  int tm_rows;      // token-major: sorted rows per tile (128; 256 on CTA pairs)
   int stack_lo;     // swap-AB GEMM2 with a hi/lo activation: one MMA over the hi rows then the lo rows
                     // (N = xbox + npad), the two column groups summed in the epilogue
   uint32_t stage_bytes, w_bytes, bar_off;
@@ -84,7 +85,7 @@ __device__ __forceinline__ int tile_count(const TcDev& p) {
   else if constexpr (SWAP)
     return p.meta[META_NACT] * p.n_tiles * p.splits;
   else
-    return (p.meta[META_NPP] / 128) * p.n_tiles;
+    return (p.meta[META_NPP] / p.tm_rows) * p.n_tiles;
 }
 
 template <bool SWAP, int EPI>
@@ -119,9 +120,9 @@ __device__ __forceinline__ Tile tile_at(const TcDev& p, int t) {
     d.n = t - m * p.n_tiles;
     d.s = 0;
     d.e = p.eids[m];
-    d.xrow = m * 128;
-    d.ntok = 128;
-    d.npad = 128;
+    d.xrow = m * p.tm_rows;
+    d.ntok = p.tm_rows;
+    d.npad = p.tm_rows;
     d.kb0 = 0;
     d.kb1 = p.kb_total;
   }
@@ -573,6 +574,234 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Token-major grouped GEMM on CTA pairs (tcgen05 cta_group::2)
+// ---------------------------------------------------------------------------
+// A cluster of two CTAs computes a tile of 256 sorted token rows x 256 weight
+// rows (the permutation pads each expert to 256 rows).  CTA r stages token rows
+// [128r, 128r + 128) of the tile and weight box r (GEMM1: the 128 gate rows,
+// then the matching 128 up rows; GEMM2: rows [128r, 128r + 128) of the 256)
+// in its own shared memory.  CTA 0 issues one M = 256, N = 256 MMA per K step;
+// it reads both CTAs' halves and leaves each CTA's 128 token rows x 256
+// columns of the result in that CTA's tensor memory, so the epilogue pairs
+// gate and up exactly as the single-CTA tile does.  Per 64-element K block an
+// SM now writes and reads 32 KB of operands instead of 48 KB: the shared-memory
+// bandwidth that bounds the single-CTA token-major tile ("FusedMoE vs
+// MegaMoE", section 3.2: weight tiles staged in shared memory, every SM busy).
+// Synchronisation: full[s] lives in CTA 0 and counts both CTAs' TMA bytes;
+// empty[s] and tfull[b] live in both CTAs and are signalled by CTA 0's commits;
+// tempty[b] in CTA 0 takes one arrival per epilogue warp of either CTA.
+// Every wait is bounded; both CTAs meet at a cluster barrier before freeing
+// tensor memory and exiting.
+constexpr int kPairEpiArrivals = 8;  // epilogue warps of both CTAs
+
+template <bool FP8, int EPI>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    k_gemm_pair(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const TcDev p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar_full = sbase + p.bar_off;
+  const uint32_t bar_empty = bar_full + 8 * kMaxStages;
+  const uint32_t bar_tfull = bar_empty + 8 * kMaxStages;
+  const uint32_t bar_tempty = bar_tfull + 16;
+  const uint32_t bar_drain = bar_tempty + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + p.bar_off + 8 * (2 * kMaxStages + 6));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_tfull + 8 * b, 1);
+      mbar_init(bar_tempty + 8 * b, kPairEpiArrivals);
+    }
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+  }
+  if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+  tc_fence_before();
+  cta_sync();
+  cluster_sync_all();  // both CTAs' barriers are initialised before any remote signal
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (!p.early) pdl_wait();
+  const int ntiles = tile_count<false, EPI>(p);
+  constexpr int KBLK = FP8 ? 128 : 64;  // elements per 128-byte K block
+  const uint32_t half_bytes = 128u * 128u;  // a 128-row box of 128 bytes
+
+  if (warp == 0) {
+    // ---------------- TMA producer (both CTAs) ----------------
+    // Each CTA loads its weight box and its 128 token rows; completion is counted
+    // on CTA 0's full barrier, which CTA 0 arms for both CTAs' bytes.
+    const uint32_t wrow_off = rank ? (uint32_t)p.w_pair_off : 0u;
+    int pre = 0;
+    if (p.early && lane == 0 && pair < ntiles) {
+      const Tile d = tile_at<false, EPI>(p, pair);
+      pre = min(p.stages, d.kb1 - d.kb0);
+      for (int i = 0; i < pre; ++i) {
+        const uint32_t fb = bar_full + 8 * i;
+        if (leader) mbar_arrive_expect_tx(fb, 4 * half_bytes);
+        tma_load_2d_pair(sbase + i * p.stage_bytes, &tmW, (d.kb0 + i) * KBLK, d.wr0 + (int)wrow_off,
+                         mapa_shared(fb, 0));
+      }
+    }
+    pre = __shfl_sync(0xffffffffu, pre, 0);
+    pdl_wait();
+    int stage = 0;
+    uint32_t phase = 0, issued = 0;
+    bool ok = true;
+    for (int t = pair; t < ntiles && ok; t += npairs) {
+      const Tile d = tile_at<false, EPI>(p, t);
+      for (int kb = d.kb0; kb < d.kb1; ++kb) {
+        const uint32_t sw = sbase + stage * p.stage_bytes;
+        const uint32_t fb = bar_full + 8 * stage;
+        if ((int)issued >= pre) {
+          if (!mbar_wait_all(bar_empty + 8 * stage, phase ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            if (leader) mbar_arrive_expect_tx(fb, 4 * half_bytes);
+            tma_load_2d_pair(sw, &tmW, kb * KBLK, d.wr0 + (int)wrow_off, mapa_shared(fb, 0));
+          }
+          __syncwarp();
+        }
+        if (lane == 0)
+          tma_load_2d_pair(sw + half_bytes, &tmX, kb * KBLK, d.xrow + 128 * (int)rank, mapa_shared(fb, 0));
+        __syncwarp();
+        ++issued;
+        if (++stage == p.stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (lane == 0) {
+      pdl_launch_dependents();
+      if (!ok && leader) {  // let the copies already in flight land before the CTA exits
+        const uint32_t first = issued > (uint32_t)p.stages ? issued - p.stages : 0u;
+        for (uint32_t i = first; i < issued; ++i)
+          mbar_wait_drain(bar_full + 8 * (i % p.stages), (i / p.stages) & 1u, 100000000ull);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (CTA 0) ----------------
+    if (leader) {
+      pdl_wait();
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true, any = false;
+      const uint32_t idesc = idesc_make(256, 256, FP8);
+      for (int t = pair; t < ntiles && ok; t += npairs) {
+        const Tile d = tile_at<false, EPI>(p, t);
+        if (!mbar_wait_all(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t dt = tmem_base + (uint32_t)(acc * p.buf_cols);
+        for (int kb = d.kb0; kb < d.kb1; ++kb) {
+          if (!mbar_wait_all(bar_full + 8 * stage, phase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t sw = sbase + stage * p.stage_bytes;
+            const uint32_t sx = sw + half_bytes;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma_pair<FP8>(dt, sdesc_k_sw128(sx + kk * 32), sdesc_k_sw128(sw + kk * 32), idesc,
+                               (kb > d.kb0 || kk > 0) ? 1u : 0u);
+            tc_commit_pair(bar_empty + 8 * stage);                  // this CTA's copy of the stage
+            tc_commit_pair(mapa_shared(bar_empty + 8 * stage, 1));  // the peer's
+          }
+          __syncwarp();
+          any = true;
+          if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        if (lane == 0) {
+          tc_commit_pair(bar_tfull + 8 * acc);
+          tc_commit_pair(mapa_shared(bar_tfull + 8 * acc, 1));
+        }
+        __syncwarp();
+        if (++acc == p.nbuf) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok && any) {  // the tensor cores must be idle before tensor memory is freed
+        if (lane == 0) tc_commit_pair(bar_drain);
+        __syncwarp();
+        mbar_wait_drain(bar_drain, 0, 100000000ull);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue (warps 2..5 of both CTAs) ----------------
+    pdl_wait();
+    const int q = warp & 3;
+    const int lrow = q * 32 + lane;
+    float a_scale = 1.0f;
+    if constexpr (FP8) a_scale = e4m3_scale_from_amax(__uint_as_float(*p.a_amax));
+    float amax = 0.0f;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    const int n_pairs = p.T * p.k;
+    for (int t = pair; t < ntiles; t += npairs) {
+      Tile d = tile_at<false, EPI>(p, t);
+      const bool ok = mbar_wait_all(bar_tfull + 8 * acc, acc_phase, abort_flag, p.status);
+      if (epi_any(!ok)) break;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.buf_cols);
+      const float scale = FP8 ? a_scale * p.w_scale[d.e] : 1.0f;
+      d.xrow += 128 * (int)rank;  // this CTA's 128 token rows of the tile
+      epi_tile<false, FP8, EPI>(p, d, tb, lrow, scale, n_pairs, amax);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader)
+          mbar_arrive(bar_tempty + 8 * acc);
+        else
+          mbar_arrive_cluster(mapa_shared(bar_tempty + 8 * acc, 0));
+      }
+      if (++acc == p.nbuf) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if constexpr (EPI == TC_EPI_G1_F32AMAX) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+      if (lane == 0 && amax > 0.0f) atomicMax(p.amax_out, __float_as_uint(amax));
+    }
+  }
+
+  // Both CTAs finish every role (and with it every read of the other CTA's
+  // shared memory or tensor memory) before either frees tensor memory or exits.
+  tc_fence_before();
+  __syncwarp();
+  cluster_sync_all();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, kTmemCols);
+}
+
+// ---------------------------------------------------------------------------
 // INT4 weight-only grouped GEMM (swap-AB): dequantisation in the main loop
 // ---------------------------------------------------------------------------
 // "FusedMoE vs MegaMoE" (zwxr.cn), section 6.3: quantised expert weights
@@ -928,6 +1157,50 @@ cudaError_t launch_inst(const CUtensorMap& mw, const CUtensorMap& mx, const CUte
   return cudaLaunchKernelEx(&cfg, kern, mw, mx, mx16, p);
 }
 
+// CTA-pair kernels: clusters of 2, a persistent grid of as many pairs as can be
+// resident at once (an SM left over in a GPC cannot take half a pair).
+template <bool FP8, int EPI>
+cudaError_t launch_pair_inst(const CUtensorMap& mw, const CUtensorMap& mx, const TcDev& p, int tiles, size_t smem,
+                             cudaStream_t s) {
+  static bool attr_set[64] = {};
+  static int max_clusters[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  auto kern = k_gemm_pair<FP8, EPI>;
+  if (!attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cfg.gridDim = dim3(2);
+  if (max_clusters[dev] == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      n = -1;
+    }
+    max_clusters[dev] = n;
+  }
+  if (max_clusters[dev] < 1) return cudaErrorInvalidConfiguration;
+  const int pairs = std::max(1, std::min(tiles, max_clusters[dev]));
+  cfg.gridDim = dim3(2 * pairs);
+  return cudaLaunchKernelEx(&cfg, kern, mw, mx, p);
+}
+
 }  // namespace
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -998,6 +1271,7 @@ static cudaError_t launch_gemm_w4(const TcGemmArgs& a, cudaStream_t s) {
     return cudaErrorInvalidValue;
   }
   TcDev p = {};
+  p.tm_rows = 128;
   p.epi = a.epi;
   p.T = a.T;
   p.k = a.k;
@@ -1050,8 +1324,68 @@ static cudaError_t launch_gemm_w4(const TcGemmArgs& a, cudaStream_t s) {
   return cudaErrorInvalidValue;
 }
 
+// Token-major GEMM1 / GEMM2 on CTA pairs: tiles of 256 sorted rows (the
+// permutation block) x 256 weight rows, each CTA staging half of each operand.
+static cudaError_t launch_gemm_pair(const TcGemmArgs& a, cudaStream_t s) {
+  if (a.swap || a.gather || a.x_lo_rows || a.w4 || a.epi == TC_EPI_LOGITS || a.wbox != 128 || a.xbox != 128)
+    return cudaErrorInvalidValue;
+  const int eb = a.fp8 ? 1 : 2;
+  CUtensorMap mw, mx;
+  if (!make_tensor_map_2d(&mw, a.W, eb, (uint64_t)a.K, (uint64_t)a.E * a.w_rows_per_expert, 128u) ||
+      !make_tensor_map_2d(&mx, a.X, eb, (uint64_t)a.K, (uint64_t)a.cap, 128u))
+    return cudaErrorInvalidValue;
+  TcDev p = {};
+  p.epi = a.epi;
+  p.T = a.T;
+  p.k = a.k;
+  p.E = a.E;
+  p.I = a.I;
+  p.H = a.H;
+  p.kb_total = a.K * eb / 128;
+  p.kb_per_split = p.kb_total;
+  p.splits = 1;
+  p.n_tiles = a.n_tiles;
+  p.w_rows_per_expert = a.w_rows_per_expert;
+  p.w_pair_off = a.w_pair_off;
+  p.w_tile_rows = a.w_tile_rows;
+  p.wbox = 128;
+  p.xbox = 128;
+  p.tm_rows = 256;
+  p.sorted = a.sorted;
+  p.eids = a.eids;
+  p.meta = a.meta;
+  p.out = a.out;
+  p.early = a.early ? 1 : 0;
+  p.out_split_stride = a.out_split_stride;
+  p.w_scale = a.w_scale;
+  p.a_amax = a.a_amax;
+  p.amax_out = a.amax_out;
+  p.status = a.status;
+  p.w_bytes = 128u * 128u;
+  p.stage_bytes = 2u * 128u * 128u;  // this CTA's weight box and token rows
+  const uint32_t bar_bytes = 8 * (2 * kMaxStages + 6) + 16;
+  int stages = (int)((227 * 1024 - 1024 - bar_bytes) / p.stage_bytes);
+  if (stages > kMaxStages) stages = kMaxStages;
+  p.stages = stages;
+  p.bar_off = (uint32_t)stages * p.stage_bytes;
+  p.d1_col = 0;
+  p.buf_cols = 256;
+  p.nbuf = 2;
+  const size_t smem = 1024 + (size_t)p.bar_off + bar_bytes;
+  const int tiles = (int)std::max<long>(1, (long)(a.cap / 256) * a.n_tiles);
+  if (a.fp8) {
+    if (a.epi == TC_EPI_G1_F32AMAX) return launch_pair_inst<true, TC_EPI_G1_F32AMAX>(mw, mx, p, tiles, smem, s);
+    if (a.epi == TC_EPI_G2_F32) return launch_pair_inst<true, TC_EPI_G2_F32>(mw, mx, p, tiles, smem, s);
+  } else {
+    if (a.epi == TC_EPI_G1_BF16) return launch_pair_inst<false, TC_EPI_G1_BF16>(mw, mx, p, tiles, smem, s);
+    if (a.epi == TC_EPI_G2_F32) return launch_pair_inst<false, TC_EPI_G2_F32>(mw, mx, p, tiles, smem, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s) {
   if (a.w4) return a.ready ? cudaErrorInvalidValue : launch_gemm_w4(a, s);
+  if (a.pair) return a.ready ? cudaErrorInvalidValue : launch_gemm_pair(a, s);
   const int eb = a.fp8 ? 1 : 2;
   CUtensorMap mw, mx;
   if (!make_tensor_map_2d(&mw, a.W, eb, (uint64_t)a.K, (uint64_t)a.E * a.w_rows_per_expert, (uint32_t)a.wbox))
@@ -1073,6 +1407,7 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s) {
     return cudaErrorInvalidValue;
 
   TcDev p = {};
+  p.tm_rows = 128;
   p.stack_lo = (a.swap && a.x_lo_rows && !a.fp8 && a.xbox <= 64) ? 1 : 0;
   p.epi = a.epi;
   p.T = a.T;

@@ -112,6 +112,7 @@ struct TcGemmArgs {
   unsigned* amax_out;       // amax bits of the produced intermediate (FP8 GEMM1)
   int* status;
   int num_sms;
+  bool pair;                // token-major on CTA pairs (tcgen05 cta_group::2): 256-row permutation blocks
   bool w4;                  // INT4 weight codes (swap-AB), dequantised to bf16 in the main loop
   const void* w4_scale;     // bf16 group scales [E][K / 128][w_rows_per_expert]
   // expert cache: before streaming expert e's weights the producer waits (bounded) until

@@ -143,3 +143,29 @@ def test_injected_timeout_is_reported(moe):
     assert moe.moe_get_status() == moe.MOE_ERR_DEVICE_TIMEOUT
     out = _run(moe, L)  # the context stays usable
     assert_parity(out.float().cpu().numpy(), _ref(L), "bf16", "")
+
+
+# Token-major GEMMs on CTA pairs (tcgen05 cta_group::2, 256-row tiles split over two SMs):
+# against the oracle at ragged multi-tile sizes, bf16 and FP8, and against single-CTA tiles
+@pytest.mark.parametrize("name,T,H,I,E,k", [("prefill", 300, 512, 384, 8, 2), ("prefill", 700, 256, 256, 16, 4),
+                                            ("prefill", 129, 768, 128, 3, 2), ("fp8_decode", 260, 512, 256, 8, 2)])
+def test_token_major_cta_pairs(moe, name, T, H, I, E, k):
+    L = _layer(name, T=T, H=H, I=I, E=E, k=k)
+    sp = L["spec"]
+    plan = moe.moe_plan_info(T, H, I, E, k, moe.MOE_BF16, moe.MOE_E4M3 if sp.w == "e4m3" else moe.MOE_BF16,
+                             {"orientation": 2})
+    assert plan["cta_pair"] == 1 and plan["block"] == 256
+    kind = "e4m3" if sp.w == "e4m3" else "bf16"
+    ref = _ref(L)
+    pair = _run(moe, L, {"orientation": 2, "cta_pair": 1}).float().cpu().numpy()
+    single = _run(moe, L, {"orientation": 2, "cta_pair": 2}).float().cpu().numpy()
+    assert_parity(pair, ref, kind, f"CTA pairs {name} T={T}")
+    assert_parity(single, ref, kind, f"single CTAs {name} T={T}")
+    print(f"[pairs] {name} T={T}: pair and single-CTA outputs bit-identical: {np.array_equal(pair, single)}")
+
+
+def test_token_major_cta_pairs_deterministic(moe):
+    L = _layer("prefill", T=513, H=512, I=256, E=8, k=2)
+    a = _run(moe, L, {"orientation": 2, "cta_pair": 1})
+    b = _run(moe, L, {"orientation": 2, "cta_pair": 1})
+    assert torch.equal(a, b)
