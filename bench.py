@@ -513,21 +513,32 @@ def run_offload(dev, steps=48, warm=8, slots=48, M=8, M_big=64, steps_big=12):
 
 
 def cpu_baseline(L, sp, budget_s=20.0):
-    """The CPU oracle, as it stands, on a bounded token sample of the workload, on all host cores."""
+    """The CPU oracle, as it stands, on a bounded token sample of the workload: on all host cores, and
+    single-threaded on a smaller sample."""
     import oracle
 
-    oracle.set_threads(len(os.sched_getaffinity(0)))
-    cores = oracle.get_threads()
+    all_cores = len(os.sched_getaffinity(0))
     cpu = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in L.items()}
+
+    def timed(threads, n):
+        oracle.set_threads(threads)
+        t0 = time.perf_counter()
+        oracle.moe_forward(cpu["X"], cpu["Wr"], cpu["W13"], cpu["W2"], sp.k, sp.renorm, cpu["w13_scale"],
+                           cpu["w2_scale"], tokens=list(range(n)))
+        return time.perf_counter() - t0
+
+    oracle.set_threads(all_cores)
+    cores = oracle.get_threads()
     n = min(sp.T, max(1, 2 * cores))
-    tokens = list(range(n))
-    t0 = time.perf_counter()
-    oracle.moe_forward(cpu["X"], cpu["Wr"], cpu["W13"], cpu["W2"], sp.k, sp.renorm, cpu["w13_scale"],
-                       cpu["w2_scale"], tokens=tokens)
-    dt = time.perf_counter() - t0
+    dt = timed(cores, n)
+    n1 = min(sp.T, 2)
+    dt1 = timed(1, n1)
+    oracle.set_threads(all_cores)
     return {"value": n / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"{n} of the {sp.T} tokens of the batch (full layer weights, routing of all {sp.T} tokens), "
-                      f"{dt:.1f} s on {cores} threads"}
+                      f"{dt:.1f} s on {cores} threads",
+            "single_thread": {"value": n1 / dt1, "unit": "tokens/s", "cores": 1,
+                              "sample": f"{n1} of the {sp.T} tokens, {dt1:.1f} s on 1 thread"}}
 
 
 def main():

@@ -184,7 +184,9 @@ MOE_API int moe_align_capacity(int T, int topk, int E, int block, size_t* sorted
 /* Router: steps 1-2 of the layer
  *   ("FusedMoE vs MegaMoE", section 2: the router gives every token a weight
  *    distribution over experts and the k highest experts are chosen).
- *   logits_out[T][E] (fp32, required) = hidden[T][H] . router_w[E][H]^T, fp32 accumulation;
+ *   logits_out[T][E] (fp32, required: the library allocates nothing, and the router writes the
+ *   logits there before ranking them; NULL returns MOE_ERR_ARG)
+ *                      = hidden[T][H] . router_w[E][H]^T, fp32 accumulation;
  *   p = softmax over all E; topk_ids[T][topk] (int32) = the topk largest p in
  *   descending order, equal values ranked by lower expert index (ranking is on
  *   the fp32 logit, which orders like p); topk_w[T][topk] (fp32) = p of those

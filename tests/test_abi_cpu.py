@@ -120,6 +120,8 @@ def test_forward_argument_errors_before_launch(moe):
     assert lib.moe_forward(fake, fake, fake, fake, 4, 256, 256, 2000, 2, 1, 1, 1, None, None, fake, ws, 1 << 30,
                            None, None) == moe.MOE_ERR_ARG
     assert lib.moe_route(fake, fake, 4, 256, 8, 0, 1, 1, fake, fake, fake, None) == moe.MOE_ERR_ARG
+    # logits_out is required: the router writes the logits there before ranking them (no scratch of its own)
+    assert lib.moe_route(fake, fake, 4, 256, 8, 2, 1, 1, None, fake, fake, None) == moe.MOE_ERR_ARG
     assert lib.moe_align(fake, 4, 2, 8, 0, fake, fake, fake, None, None) == moe.MOE_ERR_ARG
     assert lib.moe_topk_from_logits(fake, 4, 8, 9, 1, fake, fake, None) == moe.MOE_ERR_ARG
 
