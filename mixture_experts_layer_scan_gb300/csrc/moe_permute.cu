@@ -209,19 +209,32 @@ __global__ void k_amax_bf16(const uint16_t* __restrict__ X, size_t n, unsigned* 
 
 // Gather of token rows into expert order, 16-byte vectors; one CTA per row
 // (grid-stride).  Rows holding the sentinel are zero-filled.
-__global__ void k_gather_copy(const uint4* __restrict__ X, int vec_per_row, int k, int n_pairs,
-                              const int32_t* __restrict__ sorted, const int32_t* __restrict__ meta,
-                              uint4* __restrict__ Xs) {
+__global__ void __launch_bounds__(256) k_gather_copy(const uint4* __restrict__ X, int vec_per_row, int k,
+                                                     int n_pairs, const int32_t* __restrict__ sorted,
+                                                     const int32_t* __restrict__ meta, uint4* __restrict__ Xs) {
   pdl_enter();
+  // one warp per row; each lane has kGatherUnroll 16-byte loads in flight before its stores
+  constexpr int kGatherUnroll = 8;
   const int npp = meta[META_NPP];
-  for (int r = blockIdx.x; r < npp; r += gridDim.x) {
+  const int lane = threadIdx.x & 31;
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < npp; r += nwarps) {
     const int f = sorted[r];
+    const bool real = f < n_pairs;
+    const uint4* src = X + (size_t)(real ? f / k : 0) * vec_per_row;
     uint4* dst = Xs + (size_t)r * vec_per_row;
-    if (f < n_pairs) {
-      const uint4* src = X + (size_t)(f / k) * vec_per_row;
-      for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) dst[v] = src[v];
-    } else {
-      for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) dst[v] = make_uint4(0, 0, 0, 0);
+    for (int v0 = lane; v0 < vec_per_row; v0 += 32 * kGatherUnroll) {
+      uint4 buf[kGatherUnroll];
+#pragma unroll
+      for (int u = 0; u < kGatherUnroll; ++u) {
+        const int v = v0 + 32 * u;
+        buf[u] = (real && v < vec_per_row) ? src[v] : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < kGatherUnroll; ++u) {
+        const int v = v0 + 32 * u;
+        if (v < vec_per_row) dst[v] = buf[u];
+      }
     }
   }
 }
@@ -515,7 +528,9 @@ cudaError_t launch_gather(const void* X, int T, int H, int k, int elem_bytes, in
   const int grid = cap < 152 * 8 ? (cap > 0 ? cap : 1) : 152 * 8;
   if (mode == 0) {
     const int vpr = H * elem_bytes / 16;
-    MOE_LAUNCH(k_gather_copy, dim3(grid), dim3(128), 0, s, (const uint4*)X, vpr, k, T * k, sorted, meta, (uint4*)Xs);
+    const int rows_grid = std::max(1, std::min((cap + 7) / 8, 152 * 8));  // 8 warps (rows) per CTA
+    MOE_LAUNCH(k_gather_copy, dim3(rows_grid), dim3(256), 0, s, (const uint4*)X, vpr, k, T * k, sorted, meta,
+               (uint4*)Xs);
   } else {
     const int vpr = H / 8;
     MOE_LAUNCH(k_gather_quant, dim3(grid), dim3(128), 0, s, (const uint4*)X, vpr, k, T * k, sorted, meta, amax_bits, (uint2*)Xs);
