@@ -73,7 +73,7 @@ struct Plan {
   bool pair = false;            // token-major GEMMs on CTA pairs (256-row permutation blocks)
   size_t o_sync = 0;
   size_t o_logits = 0, o_tw = 0, o_tid = 0, o_meta = 0, o_sorted = 0, o_eids = 0, o_xs = 0, o_aint = 0, o_af32 = 0,
-         o_p1 = 0, o_y = 0, o_misc = 0, total = 0;
+         o_p1 = 0, o_y = 0, o_misc = 0, o_pblk = 0, total = 0;
   size_t p1_stride = 0, y_stride = 0;
 };
 
@@ -164,7 +164,7 @@ static int make_plan(int T, int H, int I, int E, int topk, moe_dtype act, moe_dt
       if (pair_mode < 0 || pair_mode > 2) return MOE_ERR_ARG;
       p.pair = pair_mode != 2 && H % 256 == 0;
       if (pair_mode == 1 && !p.pair) return MOE_ERR_UNSUPPORTED;
-      p.B = p.pair ? 256 : 128;
+      p.B = 128;
       p.xbox = 128;
       p.s1 = p.s2 = 1;
       p.kb1 = H * eb / 128;
@@ -230,6 +230,7 @@ static int make_plan(int T, int H, int I, int E, int topk, moe_dtype act, moe_dt
   p.y_stride = (size_t)n * H;
   p.o_y = take(p.y_stride * p.s2 * (p.y_bf16 ? 2 : 4));
   p.o_misc = take(256);
+  if (p.pair) p.o_pblk = take((size_t)std::max<long>(p.nblk_cap, 1) * 4);
   if (p.fused) p.o_sync = take(fused_sync_bytes(T, H, I, E));
   p.total = o;
   *pl = p;
@@ -303,6 +304,7 @@ static int forward_steps(const Plan& pl, int steps, const void* hidden, const vo
   int32_t* meta = reinterpret_cast<int32_t*>(ws + pl.o_meta);
   int32_t* sorted = reinterpret_cast<int32_t*>(ws + pl.o_sorted);
   int32_t* eids = reinterpret_cast<int32_t*>(ws + pl.o_eids);
+  int32_t* pblk = pl.pair ? reinterpret_cast<int32_t*>(ws + pl.o_pblk) : nullptr;
   void* xs = ws + pl.o_xs;
   void* aint = ws + pl.o_aint;
   float* af32 = reinterpret_cast<float*>(ws + pl.o_af32);
@@ -395,7 +397,8 @@ static int forward_steps(const Plan& pl, int steps, const void* hidden, const vo
 
   // 3. permutation
   if (o) record(o->stage_begin[MOE_STAGE_ALIGN], s);
-  MOE_TRY(launch_align(tid, T, topk, E, pl.B, sorted, eids, meta + META_NPP, nullptr, meta, st, s, skip_minus_one));
+  MOE_TRY(launch_align(tid, T, topk, E, pl.B, sorted, eids, meta + META_NPP, nullptr, meta, st, s, skip_minus_one,
+                       pblk));
   if (o) record(o->stage_end[MOE_STAGE_ALIGN], s);
 
   // 4. activations: the fp32 path gathers rows into expert order here; the
@@ -443,6 +446,7 @@ static int forward_steps(const Plan& pl, int steps, const void* hidden, const vo
     g.num_sms = sms;
     g.want = gate ? gate->want : nullptr;
     g.pair = pl.pair;
+    g.pblk = pblk;
 
     // 5. GEMM1 on w13 (+ SiLU(gate)*up)
     TcGemmArgs g1 = g;

@@ -60,6 +60,7 @@ struct TcDev {
   int stack_lo;     // swap-AB GEMM2 with a hi/lo activation: one MMA over the hi rows then the lo rows
                     // (N = xbox + npad), the two column groups summed in the epilogue
   uint32_t stage_bytes, w_bytes, bar_off;
+  const int32_t* pblk;    // CTA pairs: tile chunks (first row << 1 | 1 for a 128-row chunk)
   const unsigned* ready;  // nullable: expert e's weights are streamed once ready[e] == want[e]
   const unsigned* want;
   const int32_t* sorted;
@@ -577,13 +578,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // Token-major grouped GEMM on CTA pairs (tcgen05 cta_group::2)
 // ---------------------------------------------------------------------------
 // A cluster of two CTAs computes a tile of 256 sorted token rows x 256 weight
-// rows (the permutation pads each expert to 256 rows).  CTA r stages token rows
-// [128r, 128r + 128) of the tile and weight box r (GEMM1: the 128 gate rows,
-// then the matching 128 up rows; GEMM2: rows [128r, 128r + 128) of the 256)
-// in its own shared memory.  CTA 0 issues one M = 256, N = 256 MMA per K step;
-// it reads both CTAs' halves and leaves each CTA's 128 token rows x 256
-// columns of the result in that CTA's tensor memory, so the epilogue pairs
-// gate and up exactly as the single-CTA tile does.  Per 64-element K block an
+// rows.  CTA r stages token rows [128r, 128r + 128) of the tile and weight box r
+// (GEMM1: the 128 gate rows, then the matching 128 up rows; GEMM2: rows
+// [128r, 128r + 128) of the 256) in its own shared memory.  CTA 0 issues one
+// M = 256, N = 256 MMA per K step; it reads both CTAs' halves and leaves each
+// CTA's 128 token rows x 256 columns of the result in that CTA's tensor memory,
+// so the epilogue pairs gate and up exactly as the single-CTA tile does.
+// The permutation pads experts to 128 rows; an expert with an odd number of
+// 128-row blocks ends in a 128-row tile, run as M = 128 MMAs: CTA r stages token
+// rows [64r, 64r + 64), and the result lands in CTA r's tensor memory as row
+// 64r + (lane mod 64) with columns 0-127 of N in lanes 0-63 and 128-255 in lanes
+// 64-127.  For GEMM1 each CTA's weight half is then 64 gate rows followed by the
+// matching 64 up rows, so gate and up of a column still meet in one thread.  Per 64-element K block an
 // SM now writes and reads 32 KB of operands instead of 48 KB: the shared-memory
 // bandwidth that bounds the single-CTA token-major tile ("FusedMoE vs
 // MegaMoE", section 3.2: weight tiles staged in shared memory, every SM busy).
@@ -594,9 +600,81 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // tensor memory and exiting.
 constexpr int kPairEpiArrivals = 8;  // epilogue warps of both CTAs
 
+// CTA-pair tile t: chunk t / n_tiles of the permutation (256 rows, or 128 for an
+// expert's last odd block: tail), weight tile t % n_tiles.
+__device__ __forceinline__ Tile pair_tile_at(const TcDev& p, int t, bool& tail) {
+  Tile d;
+  const int c = t / p.n_tiles;
+  d.n = t - c * p.n_tiles;
+  d.s = 0;
+  const int v = p.pblk[c];
+  d.xrow = v >> 1;
+  tail = (v & 1) != 0;
+  d.e = p.eids[d.xrow / 128];
+  d.ntok = d.npad = tail ? 128 : 256;
+  d.kb0 = 0;
+  d.kb1 = p.kb_total;
+  d.wr0 = d.e * p.w_rows_per_expert + d.n * p.w_tile_rows;
+  return d;
+}
+
+// Epilogue of a 128-row tail tile on a CTA pair: this thread's tensor-memory lane
+// holds row 64 * rank + (lrow mod 64) of the tile and the half lrow / 64 of N.
+template <bool FP8, int EPI>
+__device__ __forceinline__ void epi_pair_tail(const TcDev& p, const Tile& d, uint32_t tb, int lrow, uint32_t rank,
+                                              float scale, int n_pairs, float& amax) {
+  const int hf = lrow >> 6;
+  const size_t row = (size_t)(d.xrow + 64 * (int)rank + (lrow & 63));
+  if constexpr (EPI == TC_EPI_G1_BF16 || EPI == TC_EPI_G1_F32AMAX) {
+    // columns [0, 64): gate of intermediate column i = n*128 + 64*hf + c; [64, 128): its up
+    const bool row_valid = p.sorted[row] < n_pairs;
+    for (int c0 = 0; c0 < 64; c0 += 16) {
+      float g[16], u[16];
+      tmem_ld16(tb + (uint32_t)c0, g);
+      tmem_ld16(tb + (uint32_t)(64 + c0), u);
+      float a[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) a[j] = silu(g[j] * scale) * (u[j] * scale);
+      const size_t o = row * p.I + (size_t)d.n * 128 + (size_t)(64 * hf + c0);
+      if constexpr (EPI == TC_EPI_G1_BF16) {
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + o);
+        uint32_t hv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) hv[j] = pack_bf16x2(a[2 * j], a[2 * j + 1]);
+        dst[0] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        dst[1] = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+      } else {
+        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + o);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) dst[j] = make_float4(a[4 * j], a[4 * j + 1], a[4 * j + 2], a[4 * j + 3]);
+        if (row_valid) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(a[j]));
+        }
+      }
+    }
+  } else {
+    // fp32 Y row of pair sorted[row], columns h = n*256 + 128*hf + c
+    const int f = p.sorted[row];
+    for (int c0 = 0; c0 < 128; c0 += 16) {
+      float v[16];
+      tmem_ld16(tb + (uint32_t)c0, v);
+      if (f < n_pairs) {
+        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + (size_t)f * p.H +
+                                                (size_t)d.n * 256 + (size_t)(128 * hf + c0));
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          dst[j] = make_float4(v[4 * j] * scale, v[4 * j + 1] * scale, v[4 * j + 2] * scale, v[4 * j + 3] * scale);
+      }
+    }
+  }
+}
+
 template <bool FP8, int EPI>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    k_gemm_pair(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const TcDev p) {
+    k_gemm_pair(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                const __grid_constant__ CUtensorMap tmW64, const __grid_constant__ CUtensorMap tmX64, const TcDev p) {
+  constexpr bool G1 = EPI != TC_EPI_G2_F32;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -626,6 +704,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     fence_barrier_init();
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmW64);
+    tma_prefetch_desc(&tmX64);
   }
   if (warp == 1) tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
   tc_fence_before();
@@ -635,24 +715,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   if (!p.early) pdl_wait();
-  const int ntiles = tile_count<false, EPI>(p);
+  const int ntiles = p.meta[META_NPB] * p.n_tiles;
   constexpr int KBLK = FP8 ? 128 : 64;  // elements per 128-byte K block
   const uint32_t half_bytes = 128u * 128u;  // a 128-row box of 128 bytes
 
   if (warp == 0) {
     // ---------------- TMA producer (both CTAs) ----------------
-    // Each CTA loads its weight box and its 128 token rows; completion is counted
-    // on CTA 0's full barrier, which CTA 0 arms for both CTAs' bytes.
+    // Each CTA loads its weight box and its token rows; completion is counted on
+    // CTA 0's full barrier, which CTA 0 arms for both CTAs' bytes.
     const uint32_t wrow_off = rank ? (uint32_t)p.w_pair_off : 0u;
+    // this CTA's weight half of one K block: GEMM1 tail tiles take 64 gate rows and
+    // the matching 64 up rows, every other tile one 128-row box
+    auto load_w = [&](uint32_t sw, const Tile& d, bool tail, int kb, uint32_t fb0) {
+      if (G1 && tail) {
+        tma_load_2d_pair(sw, &tmW64, kb * KBLK, d.wr0 + 64 * (int)rank, fb0);
+        tma_load_2d_pair(sw + half_bytes / 2, &tmW64, kb * KBLK, d.wr0 + p.w_pair_off + 64 * (int)rank, fb0);
+      } else {
+        tma_load_2d_pair(sw, &tmW, kb * KBLK, d.wr0 + (int)wrow_off, fb0);
+      }
+    };
     int pre = 0;
     if (p.early && lane == 0 && pair < ntiles) {
-      const Tile d = tile_at<false, EPI>(p, pair);
+      bool tail;
+      const Tile d = pair_tile_at(p, pair, tail);
       pre = min(p.stages, d.kb1 - d.kb0);
       for (int i = 0; i < pre; ++i) {
         const uint32_t fb = bar_full + 8 * i;
-        if (leader) mbar_arrive_expect_tx(fb, 4 * half_bytes);
-        tma_load_2d_pair(sbase + i * p.stage_bytes, &tmW, (d.kb0 + i) * KBLK, d.wr0 + (int)wrow_off,
-                         mapa_shared(fb, 0));
+        if (leader) mbar_arrive_expect_tx(fb, (tail ? 3u : 4u) * half_bytes);
+        load_w(sbase + i * p.stage_bytes, d, tail, d.kb0 + i, mapa_shared(fb, 0));
       }
     }
     pre = __shfl_sync(0xffffffffu, pre, 0);
@@ -661,7 +751,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint32_t phase = 0, issued = 0;
     bool ok = true;
     for (int t = pair; t < ntiles && ok; t += npairs) {
-      const Tile d = tile_at<false, EPI>(p, t);
+      bool tail;
+      const Tile d = pair_tile_at(p, t, tail);
       for (int kb = d.kb0; kb < d.kb1; ++kb) {
         const uint32_t sw = sbase + stage * p.stage_bytes;
         const uint32_t fb = bar_full + 8 * stage;
@@ -671,13 +762,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             break;
           }
           if (lane == 0) {
-            if (leader) mbar_arrive_expect_tx(fb, 4 * half_bytes);
-            tma_load_2d_pair(sw, &tmW, kb * KBLK, d.wr0 + (int)wrow_off, mapa_shared(fb, 0));
+            // both CTAs' weight halves, plus token rows of 128 (64 in a tail tile) per CTA
+            if (leader) mbar_arrive_expect_tx(fb, (tail ? 3u : 4u) * half_bytes);
+            load_w(sw, d, tail, kb, mapa_shared(fb, 0));
           }
           __syncwarp();
         }
-        if (lane == 0)
-          tma_load_2d_pair(sw + half_bytes, &tmX, kb * KBLK, d.xrow + 128 * (int)rank, mapa_shared(fb, 0));
+        if (lane == 0) {
+          if (tail)
+            tma_load_2d_pair(sw + half_bytes, &tmX64, kb * KBLK, d.xrow + 64 * (int)rank, mapa_shared(fb, 0));
+          else
+            tma_load_2d_pair(sw + half_bytes, &tmX, kb * KBLK, d.xrow + 128 * (int)rank, mapa_shared(fb, 0));
+        }
         __syncwarp();
         ++issued;
         if (++stage == p.stages) {
@@ -702,9 +798,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true, any = false;
-      const uint32_t idesc = idesc_make(256, 256, FP8);
       for (int t = pair; t < ntiles && ok; t += npairs) {
-        const Tile d = tile_at<false, EPI>(p, t);
+        bool tail;
+        const Tile d = pair_tile_at(p, t, tail);
+        const uint32_t idesc = idesc_make(tail ? 128 : 256, 256, FP8);
         if (!mbar_wait_all(bar_tempty + 8 * acc, acc_phase ^ 1u, abort_flag, p.status)) {
           ok = false;
           break;
@@ -764,14 +861,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint32_t acc_phase = 0;
     const int n_pairs = p.T * p.k;
     for (int t = pair; t < ntiles; t += npairs) {
-      Tile d = tile_at<false, EPI>(p, t);
+      bool tail;
+      Tile d = pair_tile_at(p, t, tail);
       const bool ok = mbar_wait_all(bar_tfull + 8 * acc, acc_phase, abort_flag, p.status);
       if (epi_any(!ok)) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.buf_cols);
       const float scale = FP8 ? a_scale * p.w_scale[d.e] : 1.0f;
-      d.xrow += 128 * (int)rank;  // this CTA's 128 token rows of the tile
-      epi_tile<false, FP8, EPI>(p, d, tb, lrow, scale, n_pairs, amax);
+      if (tail) {
+        epi_pair_tail<FP8, EPI>(p, d, tb, lrow, rank, scale, n_pairs, amax);
+      } else {
+        d.xrow += 128 * (int)rank;  // this CTA's 128 token rows of the tile
+        epi_tile<false, FP8, EPI>(p, d, tb, lrow, scale, n_pairs, amax);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -1160,8 +1262,8 @@ cudaError_t launch_inst(const CUtensorMap& mw, const CUtensorMap& mx, const CUte
 // CTA-pair kernels: clusters of 2, a persistent grid of as many pairs as can be
 // resident at once (an SM left over in a GPC cannot take half a pair).
 template <bool FP8, int EPI>
-cudaError_t launch_pair_inst(const CUtensorMap& mw, const CUtensorMap& mx, const TcDev& p, int tiles, size_t smem,
-                             cudaStream_t s) {
+cudaError_t launch_pair_inst(const CUtensorMap& mw, const CUtensorMap& mx, const CUtensorMap& mw64,
+                             const CUtensorMap& mx64, const TcDev& p, int tiles, size_t smem, cudaStream_t s) {
   static bool attr_set[64] = {};
   static int max_clusters[64] = {};
   int dev = 0;
@@ -1198,7 +1300,7 @@ cudaError_t launch_pair_inst(const CUtensorMap& mw, const CUtensorMap& mx, const
   if (max_clusters[dev] < 1) return cudaErrorInvalidConfiguration;
   const int pairs = std::max(1, std::min(tiles, max_clusters[dev]));
   cfg.gridDim = dim3(2 * pairs);
-  return cudaLaunchKernelEx(&cfg, kern, mw, mx, p);
+  return cudaLaunchKernelEx(&cfg, kern, mw, mx, mw64, mx64, p);
 }
 
 }  // namespace
@@ -1327,12 +1429,15 @@ static cudaError_t launch_gemm_w4(const TcGemmArgs& a, cudaStream_t s) {
 // Token-major GEMM1 / GEMM2 on CTA pairs: tiles of 256 sorted rows (the
 // permutation block) x 256 weight rows, each CTA staging half of each operand.
 static cudaError_t launch_gemm_pair(const TcGemmArgs& a, cudaStream_t s) {
-  if (a.swap || a.gather || a.x_lo_rows || a.w4 || a.epi == TC_EPI_LOGITS || a.wbox != 128 || a.xbox != 128)
+  if (a.swap || a.gather || a.x_lo_rows || a.w4 || a.epi == TC_EPI_LOGITS || a.wbox != 128 || a.xbox != 128 ||
+      !a.pblk)
     return cudaErrorInvalidValue;
   const int eb = a.fp8 ? 1 : 2;
-  CUtensorMap mw, mx;
+  CUtensorMap mw, mx, mw64, mx64;
   if (!make_tensor_map_2d(&mw, a.W, eb, (uint64_t)a.K, (uint64_t)a.E * a.w_rows_per_expert, 128u) ||
-      !make_tensor_map_2d(&mx, a.X, eb, (uint64_t)a.K, (uint64_t)a.cap, 128u))
+      !make_tensor_map_2d(&mx, a.X, eb, (uint64_t)a.K, (uint64_t)a.cap, 128u) ||
+      !make_tensor_map_2d(&mw64, a.W, eb, (uint64_t)a.K, (uint64_t)a.E * a.w_rows_per_expert, 64u) ||
+      !make_tensor_map_2d(&mx64, a.X, eb, (uint64_t)a.K, (uint64_t)a.cap, 64u))
     return cudaErrorInvalidValue;
   TcDev p = {};
   p.epi = a.epi;
@@ -1350,7 +1455,8 @@ static cudaError_t launch_gemm_pair(const TcGemmArgs& a, cudaStream_t s) {
   p.w_tile_rows = a.w_tile_rows;
   p.wbox = 128;
   p.xbox = 128;
-  p.tm_rows = 256;
+  p.tm_rows = 128;
+  p.pblk = a.pblk;
   p.sorted = a.sorted;
   p.eids = a.eids;
   p.meta = a.meta;
@@ -1372,13 +1478,15 @@ static cudaError_t launch_gemm_pair(const TcGemmArgs& a, cudaStream_t s) {
   p.buf_cols = 256;
   p.nbuf = 2;
   const size_t smem = 1024 + (size_t)p.bar_off + bar_bytes;
-  const int tiles = (int)std::max<long>(1, (long)(a.cap / 256) * a.n_tiles);
+  const int tiles = (int)std::max<long>(1, (long)(a.cap / 128) * a.n_tiles);
   if (a.fp8) {
-    if (a.epi == TC_EPI_G1_F32AMAX) return launch_pair_inst<true, TC_EPI_G1_F32AMAX>(mw, mx, p, tiles, smem, s);
-    if (a.epi == TC_EPI_G2_F32) return launch_pair_inst<true, TC_EPI_G2_F32>(mw, mx, p, tiles, smem, s);
+    if (a.epi == TC_EPI_G1_F32AMAX)
+      return launch_pair_inst<true, TC_EPI_G1_F32AMAX>(mw, mx, mw64, mx64, p, tiles, smem, s);
+    if (a.epi == TC_EPI_G2_F32) return launch_pair_inst<true, TC_EPI_G2_F32>(mw, mx, mw64, mx64, p, tiles, smem, s);
   } else {
-    if (a.epi == TC_EPI_G1_BF16) return launch_pair_inst<false, TC_EPI_G1_BF16>(mw, mx, p, tiles, smem, s);
-    if (a.epi == TC_EPI_G2_F32) return launch_pair_inst<false, TC_EPI_G2_F32>(mw, mx, p, tiles, smem, s);
+    if (a.epi == TC_EPI_G1_BF16)
+      return launch_pair_inst<false, TC_EPI_G1_BF16>(mw, mx, mw64, mx64, p, tiles, smem, s);
+    if (a.epi == TC_EPI_G2_F32) return launch_pair_inst<false, TC_EPI_G2_F32>(mw, mx, mw64, mx64, p, tiles, smem, s);
   }
   return cudaErrorInvalidValue;
 }

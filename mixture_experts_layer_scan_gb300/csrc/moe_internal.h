@@ -11,11 +11,12 @@
 namespace moe {
 
 // Per-call routing metadata written by the permutation kernel (int32 words):
-//   [0] num_post_pad  [1] number of blocks  [2] number of active experts  [3] unused
+//   [0] num_post_pad  [1] number of blocks  [2] number of active experts
+//   [3] number of CTA-pair chunks (token-major on CTA pairs; see launch_align)
 //   [4, 4+E)          active experts, ascending
 //   [4+E, 5+2E)       padded start offset of every expert (E+1 entries, last = num_post_pad)
 //   [5+2E, 5+3E)      tokens per expert
-enum { META_NPP = 0, META_NBLK = 1, META_NACT = 2, META_HDR = 4 };
+enum { META_NPP = 0, META_NBLK = 1, META_NACT = 2, META_NPB = 3, META_HDR = 4 };
 inline int meta_words(int E) { return META_HDR + 3 * E + 1; }
 __host__ __device__ inline int meta_active(int E) { (void)E; return META_HDR; }
 __host__ __device__ inline int meta_offsets(int E) { return META_HDR + E; }
@@ -30,10 +31,14 @@ cudaError_t launch_inject_timeout(const int* flag, int* status, cudaStream_t s);
 
 // ---- permutation / data movement ----------------------------------------------
 // skip_minus_one: ids equal to -1 are pairs handled elsewhere (dropped silently); other ids
-// outside [0, E) are dropped and flagged MOE_ERR_DEVICE_INDEX
+// outside [0, E) are dropped and flagged MOE_ERR_DEVICE_INDEX.
+// pblk (nullable, B = 128, capacity sorted_cap / 128): the chunks of the CTA-pair GEMM tiles,
+// every expert's padded run split into 256-row chunks with a 128-row last chunk where the
+// run has an odd number of blocks: pblk[c] = (first row << 1) | (1 for 128 rows); their
+// count goes to meta[META_NPB].
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int B, int32_t* sorted, int32_t* eids,
                          int32_t* npp, int32_t* counts, int32_t* meta, int* status, cudaStream_t s,
-                         bool skip_minus_one = false);
+                         bool skip_minus_one = false, int32_t* pblk = nullptr);
 // amax over n bf16 values -> *amax_bits (float bits, must be zeroed before)
 cudaError_t launch_amax_bf16(const void* X, size_t n, unsigned* amax_bits, cudaStream_t s);
 // Xs[r] = X[sorted[r]/k] (zero rows for the sentinel) for r < num_post_pad;
@@ -112,7 +117,8 @@ struct TcGemmArgs {
   unsigned* amax_out;       // amax bits of the produced intermediate (FP8 GEMM1)
   int* status;
   int num_sms;
-  bool pair;                // token-major on CTA pairs (tcgen05 cta_group::2): 256-row permutation blocks
+  bool pair;                // token-major on CTA pairs (tcgen05 cta_group::2), tiles from pblk
+  const int32_t* pblk;      // CTA-pair chunks (launch_align)
   bool w4;                  // INT4 weight codes (swap-AB), dequantised to bf16 in the main loop
   const void* w4_scale;     // bf16 group scales [E][K / 128][w_rows_per_expert]
   // expert cache: before streaming expert e's weights the producer waits (bounded) until

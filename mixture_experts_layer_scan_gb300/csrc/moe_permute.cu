@@ -64,7 +64,7 @@ __device__ int block_exclusive_scan(int v, int* scratch /* >= 33 ints */, int* t
 __global__ void __launch_bounds__(kAlignThreads, 1)
     k_align(const int32_t* __restrict__ ids, int T, int k, int E, int B, int32_t* __restrict__ sorted,
             int32_t* __restrict__ eids, int32_t* __restrict__ npp_out, int32_t* __restrict__ counts_out,
-            int32_t* __restrict__ meta, int* status, int skip_minus_one) {
+            int32_t* __restrict__ meta, int* status, int skip_minus_one, int32_t* __restrict__ pblk) {
   pdl_enter();
   cg::cluster_group cluster = cg::this_cluster();
   const int csize = (int)cluster.num_blocks();
@@ -159,6 +159,21 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
     }
   }
   __syncthreads();
+
+  // CTA-pair tiles (pblk non-null, B = 128): every expert's padded run in chunks of
+  // 256 rows, the last one 128 rows when the run has an odd number of blocks;
+  // pblk[p] = (first row << 1) | (1 for a 128-row chunk), meta word 3 = chunks
+  if (pblk) {
+    const int e = threadIdx.x;
+    const int padded = (e < E) ? off[e + 1] - off[e] : 0;
+    const int np = (padded + 255) / 256;
+    int total_np = 0;
+    const int ps = block_exclusive_scan(np, scan_tmp, &total_np);
+    if (crank == 0) {
+      for (int j = 0; j < np; ++j) pblk[ps + j] = ((off[e] + 256 * j) << 1) | (padded - 256 * j == 128 ? 1 : 0);
+      if (e == 0 && meta) meta[META_NPB] = total_np;
+    }
+  }
 
   // pass 2: stable scatter
   for (int base = beg; base < end; base += 32) {
@@ -489,7 +504,8 @@ int grid_for(size_t work, int threads, int cap_blocks = 152 * 16) {
 
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int B, int32_t* sorted, int32_t* eids,
                          int32_t* npp, int32_t* counts, int32_t* meta, int* status, cudaStream_t s,
-                         bool skip_minus_one) {
+                         bool skip_minus_one, int32_t* pblk) {
+  if (pblk && B != 128) return cudaErrorInvalidValue;
   const size_t smem = (size_t)(kAlignWarps * E + 4 * E + 1 + 33) * sizeof(int);
   static bool configured[64] = {};
   int dev = 0;
@@ -515,7 +531,7 @@ cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int B, int32_t
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, k_align, ids, T, k, E, B, sorted, eids, npp, counts, meta, status,
-                            skip_minus_one ? 1 : 0);
+                            skip_minus_one ? 1 : 0, pblk);
 }
 
 cudaError_t launch_amax_bf16(const void* X, size_t n, unsigned* amax_bits, cudaStream_t s) {

@@ -75,7 +75,7 @@ def test_plan_info(moe):
     assert d["splits_gemm1"] > 1 and d["kernel_launches"] == 7
     assert d["workspace_bytes"] == moe.moe_workspace_size(1, 2048, 768, 128, 8, moe.MOE_BF16, moe.MOE_BF16)
     p = moe.moe_plan_info(8192, 4096, 2048, 64, 8, moe.MOE_BF16, moe.MOE_BF16)
-    assert p["orientation"] == moe.ORIENT_TOKEN_MAJOR and p["block"] == 256 and p["kernel_launches"] == 7
+    assert p["orientation"] == moe.ORIENT_TOKEN_MAJOR and p["block"] == 128 and p["kernel_launches"] == 7
     assert p["cta_pair"] == 1
     single = moe.moe_plan_info(8192, 4096, 2048, 64, 8, moe.MOE_BF16, moe.MOE_BF16, {"cta_pair": 2})
     assert single["block"] == 128 and single["cta_pair"] == 0

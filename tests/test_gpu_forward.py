@@ -154,7 +154,7 @@ def test_token_major_cta_pairs(moe, name, T, H, I, E, k):
     sp = L["spec"]
     plan = moe.moe_plan_info(T, H, I, E, k, moe.MOE_BF16, moe.MOE_E4M3 if sp.w == "e4m3" else moe.MOE_BF16,
                              {"orientation": 2})
-    assert plan["cta_pair"] == 1 and plan["block"] == 256
+    assert plan["cta_pair"] == 1 and plan["block"] == 128
     kind = "e4m3" if sp.w == "e4m3" else "bf16"
     ref = _ref(L)
     pair = _run(moe, L, {"orientation": 2, "cta_pair": 1}).float().cpu().numpy()
