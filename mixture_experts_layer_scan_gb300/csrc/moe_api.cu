@@ -53,6 +53,8 @@ constexpr int kFusedMaxPairs = 512;
 constexpr int kFusedMaxExperts = 256;
 // Largest batch whose single-launch GEMM1 keeps the K splits of the multi-kernel plan.
 constexpr int kFusedSplitMaxTokens = 8;
+// Largest batch whose split GEMM1 is summed by the last-arriving CTA of each tile.
+constexpr int kFinMaxTokens = 8;
 // moe_options.single_launch == 0 picks the single-launch kernel for eligible shapes.
 constexpr bool kFusedAuto = false;
 
@@ -71,9 +73,10 @@ struct Plan {
   bool gather_in_gemm = false;  // GEMM1 gathers its activation rows itself (TMA tile::gather4)
   bool fused = false;           // the whole layer as one cooperative kernel
   bool pair = false;            // token-major GEMMs on CTA pairs (256-row permutation blocks)
+  bool fin = false;             // bf16 swap-AB GEMM1 splits summed by the last-arriving CTA (no reduction kernel)
   size_t o_sync = 0;
   size_t o_logits = 0, o_tw = 0, o_tid = 0, o_meta = 0, o_sorted = 0, o_eids = 0, o_xs = 0, o_aint = 0, o_af32 = 0,
-         o_p1 = 0, o_y = 0, o_misc = 0, o_pblk = 0, total = 0;
+         o_p1 = 0, o_y = 0, o_misc = 0, o_pblk = 0, o_fin = 0, total = 0;
   size_t p1_stride = 0, y_stride = 0;
 };
 
@@ -231,6 +234,10 @@ static int make_plan(int T, int H, int I, int E, int topk, moe_dtype act, moe_dt
   p.o_y = take(p.y_stride * p.s2 * (p.y_bf16 ? 2 : 4));
   p.o_misc = take(256);
   if (p.pair) p.o_pblk = take((size_t)std::max<long>(p.nblk_cap, 1) * 4);
+  // (the last arriver sums the splits token by token: a chain of L2 round trips that
+  // outgrows the separate reduction kernel past a few tokens)
+  p.fin = p.path == PATH_BF16 && p.swap && p.s1 > 1 && !p.fused && T <= kFinMaxTokens;
+  if (p.fin) p.o_fin = take((size_t)E * (I / 128) * 4);
   if (p.fused) p.o_sync = take(fused_sync_bytes(T, H, I, E));
   p.total = o;
   *pl = p;
@@ -305,6 +312,7 @@ static int forward_steps(const Plan& pl, int steps, const void* hidden, const vo
   int32_t* sorted = reinterpret_cast<int32_t*>(ws + pl.o_sorted);
   int32_t* eids = reinterpret_cast<int32_t*>(ws + pl.o_eids);
   int32_t* pblk = pl.pair ? reinterpret_cast<int32_t*>(ws + pl.o_pblk) : nullptr;
+  unsigned* fin = pl.fin ? reinterpret_cast<unsigned*>(ws + pl.o_fin) : nullptr;
   void* xs = ws + pl.o_xs;
   void* aint = ws + pl.o_aint;
   float* af32 = reinterpret_cast<float*>(ws + pl.o_af32);
@@ -398,7 +406,7 @@ static int forward_steps(const Plan& pl, int steps, const void* hidden, const vo
   // 3. permutation
   if (o) record(o->stage_begin[MOE_STAGE_ALIGN], s);
   MOE_TRY(launch_align(tid, T, topk, E, pl.B, sorted, eids, meta + META_NPP, nullptr, meta, st, s, skip_minus_one,
-                       pblk));
+                       pblk, fin, pl.fin ? E * (I / 128) : 0));
   if (o) record(o->stage_end[MOE_STAGE_ALIGN], s);
 
   // 4. activations: the fp32 path gathers rows into expert order here; the
@@ -472,6 +480,11 @@ static int forward_steps(const Plan& pl, int steps, const void* hidden, const vo
       g1.epi = TC_EPI_G1_PART;
       g1.out = p1;
       g1.out_split_stride = pl.p1_stride;
+      if (pl.fin) {
+        g1.fin = fin;
+        g1.out_fin = aint;
+        g1.out_fin_lo = aint_lo;
+      }
     } else {
       g1.epi = fp8 ? TC_EPI_G1_F32AMAX : TC_EPI_G1_BF16;
       g1.out = fp8 ? (void*)af32 : aint;
@@ -483,7 +496,7 @@ static int forward_steps(const Plan& pl, int steps, const void* hidden, const vo
 
     // split-K reduction / FP8 quantisation of the intermediate
     if (o) record(o->stage_begin[MOE_STAGE_ACT], s);
-    if (pl.s1 > 1)
+    if (pl.s1 > 1 && !pl.fin)
       MOE_TRY(launch_reduce_act(p1, pl.s1, pl.p1_stride, I, pl.B, n, sorted, eids, meta, cap,
                                 fp8 ? static_cast<const float*>(w13_scale) : nullptr, amax, fp8 ? 1 : 0,
                                 fp8 ? (void*)af32 : aint, aint_lo, amax + 1,
@@ -582,7 +595,7 @@ int moe_plan_info(int T, int H, int I, int E, int topk, moe_dtype act_dtype, moe
   int n = 6;
   if (!p.gather_in_gemm) n += 1;            // row gather (FP8: with input quantisation)
   if (p.path == PATH_FP8) n += p.gather_in_gemm ? 3 : 2;  // input amax (+ input quantisation), intermediate quantisation
-  if (p.s1 > 1) n += 1;
+  if (p.s1 > 1 && !p.fin) n += 1;
   if (p.fused) n = 1;
   info->kernel_launches = T > 0 ? n : 0;
   info->single_launch = p.fused ? 1 : 0;

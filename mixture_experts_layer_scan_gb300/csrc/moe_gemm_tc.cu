@@ -61,6 +61,11 @@ struct TcDev {
                     // (N = xbox + npad), the two column groups summed in the epilogue
   uint32_t stage_bytes, w_bytes, bar_off;
   const int32_t* pblk;    // CTA pairs: tile chunks (first row << 1 | 1 for a 128-row chunk)
+  unsigned* fin;          // nullable (bf16 split GEMM1): per-(expert, weight tile) arrival counters,
+                          // zeroed by the permutation kernel; the CTA storing a tile's last split
+                          // sums the splits and writes the intermediate (out_fin, out_fin_lo)
+  void* out_fin;
+  void* out_fin_lo;
   const unsigned* ready;  // nullable: expert e's weights are streamed once ready[e] == want[e]
   const unsigned* want;
   const int32_t* sorted;
@@ -139,7 +144,7 @@ __device__ __forceinline__ bool epi_any(bool v) { return named_bar_any(1, 128, v
 // in the tile's output format.
 template <bool SWAP, bool FP8, int EPI>
 __device__ __forceinline__ void epi_tile(const TcDev& p, const Tile& d, uint32_t tb, int lrow, float scale,
-                                         int n_pairs, float& amax) {
+                                         int n_pairs, float& amax, volatile int* sm_word = nullptr) {
   if constexpr (SWAP && (EPI == TC_EPI_G1_BF16 || EPI == TC_EPI_G1_F32AMAX)) {
     // lane r of D0 / D1: gate / up of intermediate column i = n*128 + r, one column per token
     const int i = d.n * 128 + lrow;
@@ -179,6 +184,39 @@ __device__ __forceinline__ void epi_tile(const TcDev& p, const Tile& d, uint32_t
           float* row = P + (size_t)p.sorted[d.xrow + c0 + j] * (2 * p.I);
           row[i] = g[j];
           row[p.I + i] = u[j];
+        }
+      }
+    }
+    if constexpr (!FP8) {
+      if (p.fin) {
+        // Last arriver: once all 128 columns of this split are stored, count it; the
+        // CTA bringing the tile's last split sums the splits in split order from 0,
+        // then SiLU(gate)*up into the bf16 (hi, lo) intermediate -- the arithmetic of
+        // the split-reduction kernel, so the results are the same bit for bit.
+        // (sm_word: a shared-memory word of the CTA for the decision)
+        named_bar_sync(1, 128);
+        if (lrow == 0) {
+          __threadfence();
+          *sm_word = atomicAdd(p.fin + d.e * p.n_tiles + d.n, 1u) == (unsigned)(p.splits - 1);
+        }
+        named_bar_sync(1, 128);
+        if (*sm_word) {
+          __threadfence();
+          const float* P0 = reinterpret_cast<const float*>(p.out);
+          for (int c = 0; c < d.ntok; ++c) {
+            const float* row = P0 + (size_t)p.sorted[d.xrow + c] * (2 * p.I);
+            float g = 0.0f, u = 0.0f;
+            for (int sp = 0; sp < p.splits; ++sp) {
+              g += __ldcg(row + (size_t)sp * p.out_split_stride + i);
+              u += __ldcg(row + (size_t)sp * p.out_split_stride + p.I + i);
+            }
+            const float a = silu(g) * u;
+            const size_t o = (size_t)(d.xrow + c) * p.I + i;
+            const __nv_bfloat16 hi = __float2bfloat16_rn(a);
+            reinterpret_cast<__nv_bfloat16*>(p.out_fin)[o] = hi;
+            if (p.out_fin_lo)
+              reinterpret_cast<__nv_bfloat16*>(p.out_fin_lo)[o] = __float2bfloat16_rn(a - __bfloat162float(hi));
+          }
         }
       }
     }
@@ -544,7 +582,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.buf_cols);
       const float scale = FP8 ? a_scale * p.w_scale[d.e] : 1.0f;
 
-      epi_tile<SWAP, FP8, EPI>(p, d, tb, lrow, scale, n_pairs, amax);
+      epi_tile<SWAP, FP8, EPI>(p, d, tb, lrow, scale, n_pairs, amax,
+                               reinterpret_cast<volatile int*>(tmem_slot + 2));
       tc_fence_before();
       mbar_arrive(bar_tempty + 8 * acc);
       if (++acc == p.nbuf) {
@@ -1548,6 +1587,10 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s) {
   p.status = a.status;
   p.ready = a.ready;
   p.want = a.ready ? a.want : nullptr;
+  p.fin = a.fin;
+  p.out_fin = a.out_fin;
+  p.out_fin_lo = a.out_fin_lo;
+  if (a.fin && (!a.swap || a.fp8 || a.epi != TC_EPI_G1_PART || !a.out_fin)) return cudaErrorInvalidValue;
 
   p.w_bytes = (uint32_t)(2 * a.wbox * 128);
   p.stage_bytes = p.w_bytes + (uint32_t)(a.xbox * 128) * (a.x_lo_rows ? 2u : 1u);

@@ -38,7 +38,8 @@ cudaError_t launch_inject_timeout(const int* flag, int* status, cudaStream_t s);
 // count goes to meta[META_NPB].
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int B, int32_t* sorted, int32_t* eids,
                          int32_t* npp, int32_t* counts, int32_t* meta, int* status, cudaStream_t s,
-                         bool skip_minus_one = false, int32_t* pblk = nullptr);
+                         bool skip_minus_one = false, int32_t* pblk = nullptr, unsigned* zero_words = nullptr,
+                         int n_zero = 0);
 // amax over n bf16 values -> *amax_bits (float bits, must be zeroed before)
 cudaError_t launch_amax_bf16(const void* X, size_t n, unsigned* amax_bits, cudaStream_t s);
 // Xs[r] = X[sorted[r]/k] (zero rows for the sentinel) for r < num_post_pad;
@@ -121,6 +122,11 @@ struct TcGemmArgs {
   const int32_t* pblk;      // CTA-pair chunks (launch_align)
   bool w4;                  // INT4 weight codes (swap-AB), dequantised to bf16 in the main loop
   const void* w4_scale;     // bf16 group scales [E][K / 128][w_rows_per_expert]
+  // bf16 swap-AB GEMM1 with K splits: arrival counters [E][n_tiles] (zeroed by launch_align) that
+  // let the CTA storing a tile's last split write the finished intermediate (out_fin / out_fin_lo)
+  unsigned* fin;
+  void* out_fin;
+  void* out_fin_lo;
   // expert cache: before streaming expert e's weights the producer waits (bounded) until
   // ready[e] == want[e] (words written by the cache's copy stream after each copy); nullable
   const unsigned* ready;

@@ -64,8 +64,11 @@ __device__ int block_exclusive_scan(int v, int* scratch /* >= 33 ints */, int* t
 __global__ void __launch_bounds__(kAlignThreads, 1)
     k_align(const int32_t* __restrict__ ids, int T, int k, int E, int B, int32_t* __restrict__ sorted,
             int32_t* __restrict__ eids, int32_t* __restrict__ npp_out, int32_t* __restrict__ counts_out,
-            int32_t* __restrict__ meta, int* status, int skip_minus_one, int32_t* __restrict__ pblk) {
+            int32_t* __restrict__ meta, int* status, int skip_minus_one, int32_t* __restrict__ pblk,
+            unsigned* __restrict__ zero_words, int n_zero) {
   pdl_enter();
+  // counters of the next kernels of this call start at zero (e.g. GEMM1's split arrivals)
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_zero; i += gridDim.x * blockDim.x) zero_words[i] = 0u;
   cg::cluster_group cluster = cg::this_cluster();
   const int csize = (int)cluster.num_blocks();
   const int crank = (int)cluster.block_rank();
@@ -504,8 +507,9 @@ int grid_for(size_t work, int threads, int cap_blocks = 152 * 16) {
 
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int B, int32_t* sorted, int32_t* eids,
                          int32_t* npp, int32_t* counts, int32_t* meta, int* status, cudaStream_t s,
-                         bool skip_minus_one, int32_t* pblk) {
+                         bool skip_minus_one, int32_t* pblk, unsigned* zero_words, int n_zero) {
   if (pblk && B != 128) return cudaErrorInvalidValue;
+  if (n_zero > 0 && !zero_words) return cudaErrorInvalidValue;
   const size_t smem = (size_t)(kAlignWarps * E + 4 * E + 1 + 33) * sizeof(int);
   static bool configured[64] = {};
   int dev = 0;
@@ -531,7 +535,7 @@ cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int B, int32_t
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, k_align, ids, T, k, E, B, sorted, eids, npp, counts, meta, status,
-                            skip_minus_one ? 1 : 0, pblk);
+                            skip_minus_one ? 1 : 0, pblk, zero_words, n_zero);
 }
 
 cudaError_t launch_amax_bf16(const void* X, size_t n, unsigned* amax_bits, cudaStream_t s) {
