@@ -749,6 +749,7 @@ int forward_routed_pass(const void* hidden, const float* topk_w, const int32_t* 
                         bool combine, const SlotGate* gate) {
   moe_options o = opts ? *opts : moe_options{};
   o.single_launch = 2;
+  if (gate) o.cta_pair = 2;  // readiness waits live in the single-CTA GEMMs (smaller or equal workspace)
   if (o.inject_timeout) return MOE_ERR_ARG;
   Plan pl;
   int rc = make_plan(T, H, I, E, topk, act_dtype, w_dtype, &o, &pl);
