@@ -475,6 +475,13 @@ static int forward_steps(const Plan& pl, int steps, const void* hidden, const vo
     g1.a_amax = amax;
     g1.amax_out = amax + 1;
     g1.ready = gate ? gate->ready13 : nullptr;
+    // routing leaves HBM idle: when every expert is almost surely active (T*k at least
+    // 8 E pairs), each GEMM1 CTA prefetches its first tile's first weights into L2,
+    // about 64 MB over the grid (a hint: a wrong guess costs only idle bandwidth)
+    if (pl.swap && !gate && (long)T * topk >= 8L * E) {
+      const long kb_bytes = 2L * 128 * 128;  // both 128-row boxes of one K block
+      g1.prefetch_kb = (int)std::max<long>(1, (64L << 20) / (kb_bytes * std::max(1, sms)));
+    }
     void* aint_lo = pl.act_split ? (void*)((uint16_t*)aint + (size_t)cap * I) : nullptr;
     if (pl.s1 > 1) {
       g1.epi = TC_EPI_G1_PART;

@@ -234,6 +234,13 @@ __device__ __forceinline__ void tma_gather4(uint32_t smem_dst, const void* tmap,
       : "memory");
 }
 
+// Prefetch a 2-D tile of a tensor into L2 (a hint: no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_l2(const void* tmap, int c_inner, int c_row) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(tmap)),
+               "r"(c_inner), "r"(c_row)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }

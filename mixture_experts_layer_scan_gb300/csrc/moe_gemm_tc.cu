@@ -57,6 +57,8 @@ struct TcDev {
   int n_valid;      // router: valid output columns
   int x_lo_rows;    // >0: the activation operand also has a bf16 low part at row offset x_lo_rows
   int tm_rows;      // token-major: sorted rows per tile (128; 256 on CTA pairs)
+  int prefetch_kb;  // swap-AB GEMM1: K blocks of this CTA's first tile to prefetch into L2 before the
+                    // dependency wait, guessing that every expert is active (0: none)
   int stack_lo;     // swap-AB GEMM2 with a hi/lo activation: one MMA over the hi rows then the lo rows
                     // (N = xbox + npad), the two column groups summed in the epilogue
   uint32_t stage_bytes, w_bytes, bar_off;
@@ -368,6 +370,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  if constexpr (SWAP && EPI != TC_EPI_LOGITS) {
+    // While routing still runs, HBM is idle: when every expert is almost surely active
+    // (the host sets prefetch_kb only then), the tile list is the identity over experts
+    // and this CTA's first tile is known; its first K blocks go to L2 as a hint.  A wrong
+    // guess only costs idle bandwidth.
+    if (p.prefetch_kb > 0 && !p.early && threadIdx.x == 0) {
+      const int per_e = p.n_tiles * p.splits;
+      const int t = blockIdx.x;
+      const int e = t / per_e;
+      if (e < p.E) {
+        const int rem = t - e * per_e;
+        const int n = rem / p.splits, sp = rem - n * p.splits;
+        const int wr0 = e * p.w_rows_per_expert + n * p.w_tile_rows;
+        const int kb0 = sp * p.kb_per_split, kb1 = min(kb0 + min(p.kb_per_split, p.prefetch_kb), p.kb_total);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          tma_prefetch_l2(&tmW, kb * (FP8 ? 128 : 64), wr0);
+          tma_prefetch_l2(&tmW, kb * (FP8 ? 128 : 64), wr0 + p.w_pair_off);
+        }
+      }
+    }
+  }
   // Programmatic dependent launch: kernels of this library let their
   // dependents launch early, so nothing written by an earlier kernel may be
   // read before pdl_wait() -- except when the host sets `early`: for GEMM2
@@ -1555,6 +1578,7 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s) {
 
   TcDev p = {};
   p.tm_rows = 128;
+  p.prefetch_kb = a.prefetch_kb;
   p.stack_lo = (a.swap && a.x_lo_rows && !a.fp8 && a.xbox <= 64) ? 1 : 0;
   p.epi = a.epi;
   p.T = a.T;

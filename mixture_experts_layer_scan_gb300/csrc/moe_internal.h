@@ -120,6 +120,8 @@ struct TcGemmArgs {
   int num_sms;
   bool pair;                // token-major on CTA pairs (tcgen05 cta_group::2), tiles from pblk
   const int32_t* pblk;      // CTA-pair chunks (launch_align)
+  int prefetch_kb;          // swap-AB GEMM1: L2 prefetch of the first tile's first K blocks before the
+                            // dependency wait, on the guess that all experts are active (0: off)
   bool w4;                  // INT4 weight codes (swap-AB), dequantised to bf16 in the main loop
   const void* w4_scale;     // bf16 group scales [E][K / 128][w_rows_per_expert]
   // bf16 swap-AB GEMM1 with K splits: arrival counters [E][n_tiles] (zeroed by launch_align) that
