@@ -45,6 +45,9 @@ static int num_sms() {
 constexpr int kPlanSms = 152;
 // Router logits go through the tensor-core GEMM from this many tokens on.
 constexpr int kRouterTcMinTokens = 256;
+// From this many tokens on, the row gather goes token by token (each token row read
+// once, stored at its k sorted rows); shorter batches gather row by row over more warps.
+constexpr int kGatherTokenOrderMinTokens = 4096;
 // Largest swap-AB activation tile whose rows GEMM1 gathers itself.
 constexpr int kGatherInGemmMaxRows = 32;
 // Single-launch decode kernel limits (shared-memory tables, one token column per epilogue thread).
@@ -76,7 +79,7 @@ struct Plan {
   bool fin = false;             // bf16 swap-AB GEMM1 splits summed by the last-arriving CTA (no reduction kernel)
   size_t o_sync = 0;
   size_t o_logits = 0, o_tw = 0, o_tid = 0, o_meta = 0, o_sorted = 0, o_eids = 0, o_xs = 0, o_aint = 0, o_af32 = 0,
-         o_p1 = 0, o_y = 0, o_misc = 0, o_pblk = 0, o_fin = 0, total = 0;
+         o_p1 = 0, o_y = 0, o_misc = 0, o_pblk = 0, o_fin = 0, o_inv = 0, total = 0;
   size_t p1_stride = 0, y_stride = 0;
 };
 
@@ -234,6 +237,9 @@ static int make_plan(int T, int H, int I, int E, int topk, moe_dtype act, moe_dt
   p.o_y = take(p.y_stride * p.s2 * (p.y_bf16 ? 2 : 4));
   p.o_misc = take(256);
   if (p.pair) p.o_pblk = take((size_t)std::max<long>(p.nblk_cap, 1) * 4);
+  // pair -> sorted row, for the token-order gather of long batches
+  if (p.gather_in_gemm || p.path == PATH_FP8 || T < kGatherTokenOrderMinTokens) p.o_inv = 0;
+  else p.o_inv = take((size_t)n * 4);
   // (the last arriver sums the splits token by token: a chain of L2 round trips that
   // outgrows the separate reduction kernel past a few tokens)
   p.fin = p.path == PATH_BF16 && p.swap && p.s1 > 1 && !p.fused && T <= kFinMaxTokens;
@@ -312,6 +318,7 @@ static int forward_steps(const Plan& pl, int steps, const void* hidden, const vo
   int32_t* sorted = reinterpret_cast<int32_t*>(ws + pl.o_sorted);
   int32_t* eids = reinterpret_cast<int32_t*>(ws + pl.o_eids);
   int32_t* pblk = pl.pair ? reinterpret_cast<int32_t*>(ws + pl.o_pblk) : nullptr;
+  int32_t* inv = pl.o_inv ? reinterpret_cast<int32_t*>(ws + pl.o_inv) : nullptr;
   unsigned* fin = pl.fin ? reinterpret_cast<unsigned*>(ws + pl.o_fin) : nullptr;
   void* xs = ws + pl.o_xs;
   void* aint = ws + pl.o_aint;
@@ -406,7 +413,7 @@ static int forward_steps(const Plan& pl, int steps, const void* hidden, const vo
   // 3. permutation
   if (o) record(o->stage_begin[MOE_STAGE_ALIGN], s);
   MOE_TRY(launch_align(tid, T, topk, E, pl.B, sorted, eids, meta + META_NPP, nullptr, meta, st, s, skip_minus_one,
-                       pblk, fin, pl.fin ? E * (I / 128) : 0));
+                       pblk, fin, pl.fin ? E * (I / 128) : 0, inv));
   if (o) record(o->stage_end[MOE_STAGE_ALIGN], s);
 
   // 4. activations: the fp32 path gathers rows into expert order here; the
@@ -418,9 +425,10 @@ static int forward_steps(const Plan& pl, int steps, const void* hidden, const vo
     if (pl.gather_in_gemm)
       MOE_TRY(launch_quant_x(hidden, (size_t)T * H, amax, (uint8_t*)xs, s));
     else
-      MOE_TRY(launch_gather(hidden, T, H, topk, 2, 1, amax, sorted, meta, cap, xs, s));
+      MOE_TRY(launch_gather(hidden, T, H, topk, 2, 1, amax, sorted, nullptr, meta, cap, xs, s));
   } else if (!pl.gather_in_gemm) {
-    MOE_TRY(launch_gather(hidden, T, H, topk, pl.path == PATH_F32 ? 4 : 2, 0, nullptr, sorted, meta, cap, xs, s));
+    MOE_TRY(launch_gather(hidden, T, H, topk, pl.path == PATH_F32 ? 4 : 2, 0, nullptr, sorted, inv, meta, cap, xs,
+                          s));
   }
   if (o) record(o->stage_end[MOE_STAGE_GATHER], s);
 

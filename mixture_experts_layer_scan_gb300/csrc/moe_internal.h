@@ -35,17 +35,21 @@ cudaError_t launch_inject_timeout(const int* flag, int* status, cudaStream_t s);
 // pblk (nullable, B = 128, capacity sorted_cap / 128): the chunks of the CTA-pair GEMM tiles,
 // every expert's padded run split into 256-row chunks with a 128-row last chunk where the
 // run has an odd number of blocks: pblk[c] = (first row << 1) | (1 for 128 rows); their
-// count goes to meta[META_NPB].
+// count goes to meta[META_NPB].  inv (nullable, T*k words): the sorted row of each
+// pair, -1 for a pair left out.
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int B, int32_t* sorted, int32_t* eids,
                          int32_t* npp, int32_t* counts, int32_t* meta, int* status, cudaStream_t s,
                          bool skip_minus_one = false, int32_t* pblk = nullptr, unsigned* zero_words = nullptr,
-                         int n_zero = 0);
+                         int n_zero = 0, int32_t* inv = nullptr);
 // amax over n bf16 values -> *amax_bits (float bits, must be zeroed before)
 cudaError_t launch_amax_bf16(const void* X, size_t n, unsigned* amax_bits, cudaStream_t s);
 // Xs[r] = X[sorted[r]/k] (zero rows for the sentinel) for r < num_post_pad;
-// mode 0: copy elements of elem_bytes; mode 1: bf16 -> e4m3 with scale amax/448
+// mode 0: copy elements of elem_bytes, token by token through inv when it is given
+// (launch_align's inverse map; k <= 32: every token row read once), else row by row;
+// mode 1: bf16 -> e4m3 with scale amax/448 (inv unused)
 cudaError_t launch_gather(const void* X, int T, int H, int k, int elem_bytes, int mode, const unsigned* amax_bits,
-                          const int32_t* sorted, const int32_t* meta, int cap, void* Xs, cudaStream_t s);
+                          const int32_t* sorted, const int32_t* inv, const int32_t* meta, int cap, void* Xs,
+                          cudaStream_t s);
 // split-K reduction of the GEMM1 partials P[split][pair][2I] + scale + SiLU(gate)*up
 // into sorted rows (row r holds pair sorted[r]).
 //   out_mode 0: bf16 A_int   1: fp32 A (+ amax into amax_bits)

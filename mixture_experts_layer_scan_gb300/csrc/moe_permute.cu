@@ -20,6 +20,7 @@ namespace {
 
 constexpr int kAlignThreads = 1024;
 constexpr int kAlignWarps = kAlignThreads / 32;
+constexpr int kGatherThreads = 64;  // two warps (tokens) per CTA: short batches spread over SMs
 
 // Exclusive scan over blockDim.x (= 1024) values, one per thread; returns the
 // exclusive prefix of the caller and writes the block total to *total.
@@ -65,7 +66,7 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
     k_align(const int32_t* __restrict__ ids, int T, int k, int E, int B, int32_t* __restrict__ sorted,
             int32_t* __restrict__ eids, int32_t* __restrict__ npp_out, int32_t* __restrict__ counts_out,
             int32_t* __restrict__ meta, int* status, int skip_minus_one, int32_t* __restrict__ pblk,
-            unsigned* __restrict__ zero_words, int n_zero) {
+            unsigned* __restrict__ zero_words, int n_zero, int32_t* __restrict__ inv) {
   pdl_enter();
   // counters of the next kernels of this call start at zero (e.g. GEMM1's split arrivals)
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_zero; i += gridDim.x * blockDim.x) zero_words[i] = 0u;
@@ -194,6 +195,7 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
       sorted[slot] = f;
       if (lane == __ffs(grp) - 1) wc[warp * E + e] += __popc(grp);
     }
+    if (inv && f < end) inv[f] = e >= 0 ? slot : -1;  // pair -> sorted row (-1: left out)
     __syncwarp();
   }
 
@@ -225,8 +227,62 @@ __global__ void k_amax_bf16(const uint16_t* __restrict__ X, size_t n, unsigned* 
   if ((threadIdx.x & 31) == 0) atomicMax(amax_bits, __float_as_uint(m));
 }
 
-// Gather of token rows into expert order, 16-byte vectors; one CTA per row
-// (grid-stride).  Rows holding the sentinel are zero-filled.
+// Gather of token rows into expert order, 16-byte vectors, token by token: a
+// warp reads token t's row once and stores it at the sorted rows of its k pairs
+// (inv[t*k + j]; -1 for a pair left out), so every row is read from memory once
+// however many experts it goes to.  Rows holding the sentinel (expert padding)
+// are then zero-filled.
+__global__ void __launch_bounds__(kGatherThreads) k_gather_scatter(const uint4* __restrict__ X, int vec_per_row,
+                                                                   int T, int k, int n_pairs,
+                                                                   const int32_t* __restrict__ inv,
+                                                                   const int32_t* __restrict__ sorted,
+                                                                   const int32_t* __restrict__ meta,
+                                                                   uint4* __restrict__ Xs) {
+  pdl_enter();
+  constexpr int kUnroll = 8;  // 16-byte loads of one lane in flight before its stores
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  // (every loop bound below is the same in all lanes of a warp, so all 32 lanes reach
+  // each shuffle and ballot; only the loads and stores depend on the lane)
+  for (int t = gw; t < T; t += nwarps) {
+    const int my_row = lane < k ? inv[(size_t)t * k + lane] : -1;  // k <= 32
+    const uint4* src = X + (size_t)t * vec_per_row;
+    for (int v0 = 0; v0 < vec_per_row; v0 += 32 * kUnroll) {
+      uint4 buf[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int v = v0 + 32 * u + lane;
+        if (v < vec_per_row) buf[u] = src[v];
+      }
+      for (int j = 0; j < k; ++j) {
+        const int r = __shfl_sync(0xffffffffu, my_row, j);
+        if (r < 0) continue;
+        uint4* dst = Xs + (size_t)r * vec_per_row;
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int v = v0 + 32 * u + lane;
+          if (v < vec_per_row) dst[v] = buf[u];
+        }
+      }
+    }
+  }
+  const int npp = meta[META_NPP];
+  for (int r0 = gw * 32; r0 < npp; r0 += nwarps * 32) {
+    const int r = r0 + lane;
+    unsigned pad = __ballot_sync(0xffffffffu, r < npp && sorted[r] >= n_pairs);
+    while (pad) {
+      const int b = __ffs(pad) - 1;
+      pad &= pad - 1;
+      uint4* dst = Xs + (size_t)(r0 + b) * vec_per_row;
+      for (int v = lane; v < vec_per_row; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
+    }
+  }
+}
+
+// Gather of token rows into expert order, 16-byte vectors, row by row: one warp
+// per sorted row (grid-stride), rows holding the sentinel zero-filled.  For short
+// batches, whose token rows stay in L2, this spreads the copies over the most warps.
 __global__ void __launch_bounds__(256) k_gather_copy(const uint4* __restrict__ X, int vec_per_row, int k,
                                                      int n_pairs, const int32_t* __restrict__ sorted,
                                                      const int32_t* __restrict__ meta, uint4* __restrict__ Xs) {
@@ -507,7 +563,7 @@ int grid_for(size_t work, int threads, int cap_blocks = 152 * 16) {
 
 cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int B, int32_t* sorted, int32_t* eids,
                          int32_t* npp, int32_t* counts, int32_t* meta, int* status, cudaStream_t s,
-                         bool skip_minus_one, int32_t* pblk, unsigned* zero_words, int n_zero) {
+                         bool skip_minus_one, int32_t* pblk, unsigned* zero_words, int n_zero, int32_t* inv) {
   if (pblk && B != 128) return cudaErrorInvalidValue;
   if (n_zero > 0 && !zero_words) return cudaErrorInvalidValue;
   const size_t smem = (size_t)(kAlignWarps * E + 4 * E + 1 + 33) * sizeof(int);
@@ -535,7 +591,7 @@ cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int B, int32_t
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, k_align, ids, T, k, E, B, sorted, eids, npp, counts, meta, status,
-                            skip_minus_one ? 1 : 0, pblk, zero_words, n_zero);
+                            skip_minus_one ? 1 : 0, pblk, zero_words, n_zero, inv);
 }
 
 cudaError_t launch_amax_bf16(const void* X, size_t n, unsigned* amax_bits, cudaStream_t s) {
@@ -544,13 +600,22 @@ cudaError_t launch_amax_bf16(const void* X, size_t n, unsigned* amax_bits, cudaS
 }
 
 cudaError_t launch_gather(const void* X, int T, int H, int k, int elem_bytes, int mode, const unsigned* amax_bits,
-                          const int32_t* sorted, const int32_t* meta, int cap, void* Xs, cudaStream_t s) {
+                          const int32_t* sorted, const int32_t* inv, const int32_t* meta, int cap, void* Xs,
+                          cudaStream_t s) {
   const int grid = cap < 152 * 8 ? (cap > 0 ? cap : 1) : 152 * 8;
   if (mode == 0) {
     const int vpr = H * elem_bytes / 16;
-    const int rows_grid = std::max(1, std::min((cap + 7) / 8, 152 * 8));  // 8 warps (rows) per CTA
-    MOE_LAUNCH(k_gather_copy, dim3(rows_grid), dim3(256), 0, s, (const uint4*)X, vpr, k, T * k, sorted, meta,
-               (uint4*)Xs);
+    if (inv) {
+      if (k > 32) return cudaErrorInvalidValue;
+      constexpr int wpb = kGatherThreads / 32;
+      const int blocks = std::max(1, std::min((T + wpb - 1) / wpb, 152 * 32));  // one warp per token
+      MOE_LAUNCH(k_gather_scatter, dim3(blocks), dim3(kGatherThreads), 0, s, (const uint4*)X, vpr, T, k, T * k, inv,
+                 sorted, meta, (uint4*)Xs);
+    } else {
+      const int rows_grid = std::max(1, std::min((cap + 7) / 8, 152 * 8));  // 8 warps (rows) per CTA
+      MOE_LAUNCH(k_gather_copy, dim3(rows_grid), dim3(256), 0, s, (const uint4*)X, vpr, k, T * k, sorted, meta,
+                 (uint4*)Xs);
+    }
   } else {
     const int vpr = H / 8;
     MOE_LAUNCH(k_gather_quant, dim3(grid), dim3(128), 0, s, (const uint4*)X, vpr, k, T * k, sorted, meta, amax_bits, (uint2*)Xs);

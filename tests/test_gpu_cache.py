@@ -90,7 +90,8 @@ def test_cached_layer_matches_resident(moe, mode, name, slots, T):
 
 @pytest.mark.parametrize("name,slots,T,E,k", [("fine_decode", 20, 6, 64, 8), ("fine_decode", 10, 6, 64, 8),
                                               ("fp8_decode", 24, 2, 32, 8), ("mixtral_decode", 3, 5, 8, 2),
-                                              ("prefill", 12, 96, 16, 2)])  # 96 tokens: token-major GEMMs
+                                              ("prefill", 12, 96, 16, 2),  # 96 tokens: token-major GEMMs
+                                              ("prefill", 12, 4200, 16, 2)])  # 4200: token-order row gather
 def test_cached_layer_matches_oracle(moe, name, slots, T, E, k):
     """A sequence of batches with evictions (and, where slots < distinct experts, passes)
     against the CPU oracle."""

@@ -81,6 +81,26 @@ def test_bf16_token_major(moe, T, H, I, E, k):
     assert_parity(out.float().cpu().numpy(), _ref(L), "bf16", "")
 
 
+# From 4096 tokens on the rows are gathered token by token (each token row read once
+# and stored at its k sorted rows), below that row by row.  A token's output does not
+# depend on the other tokens of the batch, so the first 1000 tokens of a 4200-token batch
+# must come out bit for bit as a 1000-token batch of the same tokens computes them.
+@pytest.mark.parametrize("name,H,I,E,k", [("prefill", 256, 256, 16, 4), ("prefill", 512, 128, 8, 1),
+                                          ("tiny_f32", 64, 96, 8, 2)])
+def test_token_order_gather(moe, name, H, I, E, k):
+    L = _layer(name, T=4200, H=H, I=I, E=E, k=k)
+    sp = L["spec"]
+    opts = None if name == "tiny_f32" else {"orientation": 2}
+    full = _run(moe, L, opts)
+    kind = "f32" if name == "tiny_f32" else "bf16"
+    assert_parity(full.float().cpu().numpy(), _ref(L), kind, f"{name} T=4200")
+    d = {kk: (v.cuda() if isinstance(v, torch.Tensor) else v) for kk, v in L.items()}
+    part = moe.moe_forward(d["X"][:1000].contiguous(), d["Wr"], d["W13"], d["W2"], sp.k, sp.renorm, options=opts)
+    torch.cuda.synchronize()
+    assert moe.moe_get_status() == 0
+    assert torch.equal(full[:1000], part)
+
+
 @pytest.mark.parametrize("splits", [2, 3, 4])
 def test_bf16_split_k(moe, splits):
     L = _layer("fine_decode", T=5, H=512, I=384, E=16, k=4)
