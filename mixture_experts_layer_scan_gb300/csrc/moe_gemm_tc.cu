@@ -303,7 +303,37 @@ __device__ __forceinline__ void epi_tile(const TcDev& p, const Tile& d, uint32_t
           if (c0 + j < p.n_valid) dst[c0 + j] = v[j];
       }
     }
-  } else if constexpr (!SWAP && (EPI == TC_EPI_G2_BF16 || EPI == TC_EPI_G2_F32)) {
+  } else if constexpr (!SWAP && EPI == TC_EPI_G2_F32) {
+    // fp32 rows of Y: read in the 16x256b shape, thread t has two adjacent columns of
+    // rows t/4 and 8 + t/4 (of each 16-lane half of the warp's quadrant) per 8-column
+    // group; one exchange with the neighbouring thread leaves 4 adjacent columns of one
+    // row in each thread, so a store instruction writes 32 contiguous bytes of each of
+    // 16 rows instead of 16 bytes of each of 32
+    const int ln = lrow & 31;
+    const bool odd = (ln & 1) != 0;
+    const int ncols = 2 * p.wbox;
+    const int cofs = (ln & 2) * 2;  // first of the 4 columns this thread stores in a group
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int row = (lrow & ~31) + 16 * h + (ln >> 2) + (odd ? 8 : 0);
+      const int f = p.sorted[d.xrow + row];
+      float* dst = reinterpret_cast<float*>(p.out) + (size_t)(f < n_pairs ? f : 0) * p.H + (size_t)d.n * ncols + cofs;
+      for (int c0 = 0; c0 < ncols; c0 += 32) {
+        float v[16];
+        tmem_ld_16x256b_x4(tb + ((uint32_t)(16 * h) << 16) + (uint32_t)c0, v);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float s0 = odd ? v[4 * j] : v[4 * j + 2];  // the pair the neighbour stores
+          const float s1 = odd ? v[4 * j + 1] : v[4 * j + 3];
+          const float r0 = __shfl_xor_sync(0xffffffffu, s0, 1);
+          const float r1 = __shfl_xor_sync(0xffffffffu, s1, 1);
+          const float4 o = odd ? make_float4(r0 * scale, r1 * scale, v[4 * j + 2] * scale, v[4 * j + 3] * scale)
+                               : make_float4(v[4 * j] * scale, v[4 * j + 1] * scale, r0 * scale, r1 * scale);
+          if (f < n_pairs) *reinterpret_cast<float4*>(dst + c0 + 8 * j) = o;
+        }
+      }
+    }
+  } else if constexpr (!SWAP && EPI == TC_EPI_G2_BF16) {
     const int f = p.sorted[d.xrow + lrow];
     const int ncols = 2 * p.wbox;
     for (int c0 = 0; c0 < ncols; c0 += 16) {
@@ -311,20 +341,11 @@ __device__ __forceinline__ void epi_tile(const TcDev& p, const Tile& d, uint32_t
       tmem_ld16(tb + (uint32_t)c0, v);
       if (f < n_pairs) {
         const size_t o = (size_t)f * p.H + (size_t)d.n * ncols + c0;
-        if constexpr (EPI == TC_EPI_G2_BF16) {
-          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + o);
-          dst[0] = make_uint4(pack_bf16x2(v[0] * scale, v[1] * scale), pack_bf16x2(v[2] * scale, v[3] * scale),
-                              pack_bf16x2(v[4] * scale, v[5] * scale), pack_bf16x2(v[6] * scale, v[7] * scale));
-          dst[1] =
-              make_uint4(pack_bf16x2(v[8] * scale, v[9] * scale), pack_bf16x2(v[10] * scale, v[11] * scale),
-                         pack_bf16x2(v[12] * scale, v[13] * scale), pack_bf16x2(v[14] * scale, v[15] * scale));
-        } else {
-          float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + o);
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            dst[j] = make_float4(v[4 * j] * scale, v[4 * j + 1] * scale, v[4 * j + 2] * scale,
-                                 v[4 * j + 3] * scale);
-        }
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + o);
+        dst[0] = make_uint4(pack_bf16x2(v[0] * scale, v[1] * scale), pack_bf16x2(v[2] * scale, v[3] * scale),
+                            pack_bf16x2(v[4] * scale, v[5] * scale), pack_bf16x2(v[6] * scale, v[7] * scale));
+        dst[1] = make_uint4(pack_bf16x2(v[8] * scale, v[9] * scale), pack_bf16x2(v[10] * scale, v[11] * scale),
+                            pack_bf16x2(v[12] * scale, v[13] * scale), pack_bf16x2(v[14] * scale, v[15] * scale));
       }
     }
   }
