@@ -412,15 +412,21 @@ static int forward_steps(const Plan& pl, int steps, const void* hidden, const vo
 
   // 3. permutation
   if (o) record(o->stage_begin[MOE_STAGE_ALIGN], s);
-  MOE_TRY(launch_align(tid, T, topk, E, pl.B, sorted, eids, meta + META_NPP, nullptr, meta, st, s, skip_minus_one,
-                       pblk, fin, pl.fin ? E * (I / 128) : 0, inv));
+  // the permutation kernel also zeroes the counters of this call's later kernels: the split
+  // arrival counters (last-arriver sums) or the two FP8 amax words, so that no memset node
+  // breaks the chain of programmatically dependent launches
+  {
+    unsigned* zero_words = pl.fin ? fin : (pl.path == PATH_FP8 ? amax : nullptr);
+    const int n_zero = pl.fin ? E * (I / 128) : (pl.path == PATH_FP8 ? 2 : 0);
+    MOE_TRY(launch_align(tid, T, topk, E, pl.B, sorted, eids, meta + META_NPP, nullptr, meta, st, s, skip_minus_one,
+                         pblk, zero_words, n_zero, inv));
+  }
   if (o) record(o->stage_end[MOE_STAGE_ALIGN], s);
 
   // 4. activations: the fp32 path gathers rows into expert order here; the
   // tensor-core paths gather inside GEMM1 (FP8: quantise the input to e4m3 first)
   if (o) record(o->stage_begin[MOE_STAGE_GATHER], s);
   if (pl.path == PATH_FP8) {
-    MOE_TRY(cudaMemsetAsync(amax, 0, 2 * sizeof(unsigned), s));
     MOE_TRY(launch_amax_bf16(hidden, (size_t)T * H, amax, s));
     if (pl.gather_in_gemm)
       MOE_TRY(launch_quant_x(hidden, (size_t)T * H, amax, (uint8_t*)xs, s));

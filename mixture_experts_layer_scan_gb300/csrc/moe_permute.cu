@@ -583,13 +583,17 @@ cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int B, int32_t
   cfg.blockDim = dim3(kAlignThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  // programmatic dependent launch, like every kernel of the library: the CTAs launch
+  // while the top-k kernel drains and wait (griddepcontrol.wait) before reading its ids
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = csize;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, k_align, ids, T, k, E, B, sorted, eids, npp, counts, meta, status,
                             skip_minus_one ? 1 : 0, pblk, zero_words, n_zero, inv);
 }
