@@ -350,16 +350,16 @@ def run_ours(args, rank, world, dev):
             head["spec"] = sp
             head["clocks"] = sampler.summary() if sampler else None
             head["K"], head["W"] = K, W
-            # end to end through the C ABI with host buffers (moe_forward_host): the copy of
-            # the batch from pinned host memory, the layer and the copy of the output back to
+            # end to end through the C ABI with host buffers (moe_forward_host): the batch
+            # read from pinned host memory into the device, the layer, its output stored into
             # pinned host memory, every step, on the timed stream
             Xh = X.cpu().pin_memory()
             outh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
             Xd = torch.empty_like(X)
 
             def e2e_step():
-                moe.moe_forward_host(Xh, Wr, W13, W2, sp.k, sp.renorm, s13, s2, hidden_dev=Xd, out_dev=out,
-                                     out_host=outh, workspace=ws, options=base_opts, stream=stream, w_format=wfmt)
+                moe.moe_forward_host(Xh, Wr, W13, W2, sp.k, sp.renorm, s13, s2, hidden_dev=Xd, out_host=outh,
+                                     workspace=ws, options=base_opts, stream=stream, w_format=wfmt)
 
             for _ in range(W):
                 e2e_step()
@@ -368,7 +368,8 @@ def run_ours(args, rank, world, dev):
             e2e_ms = timed(e2e_step, ke, False) / ke
             e2e_ms = max_over_ranks(e2e_ms, world, dev)
             head["e2e"] = {"value": job_tokens_per_s(T, world, e2e_ms), "unit": "tokens/s",
-                           "api": "moe_forward_host (pinned host in, pinned host out, one stream)",
+                           "api": "moe_forward_host (pinned host batch read by a copy kernel, output stored "
+                                  "into pinned host memory by the layer, one stream)",
                            "h2d_bytes_per_step": X.numel() * X.element_size(),
                            "d2h_bytes_per_step": out.numel() * out.element_size()}
             head["cpu_layer"] = (L, sp)

@@ -263,23 +263,24 @@ MOE_API int moe_forward(const void* hidden, const void* router_w, const void* w1
                 const void* w2_scale, void* out, void* workspace, size_t workspace_bytes, const moe_options* opts,
                 moe_stream_t stream);
 
-/* The layer from host memory to host memory: on `stream`, in this order,
- *   1. hidden_host -> hidden_dev, T*H elements of act_dtype (cudaMemcpyAsync),
- *   2. moe_forward(hidden_dev, ..., out_dev, ...) exactly as above,
- *   3. out_dev -> out_host, T*H elements of act_dtype (cudaMemcpyAsync).
- * hidden_host and out_host are page-locked host memory (cudaHostAlloc, cudaMallocHost or
- * cudaHostRegister; MOE_ERR_ARG otherwise, since a pageable copy would not be
- * asynchronous); hidden_dev and out_dev are device staging buffers of T*H elements
- * (16-byte aligned), owned by the caller.  Every other argument is moe_forward's.  The
- * call returns once the work is enqueued: out_host holds the result when the work
- * enqueued on `stream` has completed (cudaStreamSynchronize, an event).  Errors: those
- * of moe_forward, MOE_ERR_ARG for a null or pageable host buffer, MOE_ERR_CUDA when a
- * copy cannot be enqueued.  T == 0 is a no-op. */
+/* The layer from host memory to host memory, on `stream`:
+ *   1. hidden_host -> hidden_dev, T*H elements of act_dtype, by a copy kernel that reads the
+ *      host memory directly (cudaMemcpyAsync when the byte count or an address is not a
+ *      multiple of 16),
+ *   2. moe_forward(hidden_dev, ..., out, ...) exactly as above, with `out` the device
+ *      address of out_host: the layer's last kernel stores the output into host memory.
+ * hidden_host and out_host are page-locked host memory that the device can address
+ * (cudaHostAlloc, cudaMallocHost or cudaHostRegister on a system with unified addressing;
+ * MOE_ERR_ARG otherwise); out_host 16-byte aligned (MOE_ERR_ALIGNMENT).  hidden_dev is a
+ * device staging buffer of T*H elements (16-byte aligned) owned by the caller.  Every
+ * other argument is moe_forward's.  The call returns once the work is enqueued: out_host
+ * holds the result when the work enqueued on `stream` has completed (cudaStreamSynchronize,
+ * an event).  Errors: those of moe_forward, MOE_ERR_ARG for a null, pageable or unmapped
+ * host buffer, MOE_ERR_CUDA when the copy cannot be enqueued.  T == 0 is a no-op. */
 MOE_API int moe_forward_host(const void* hidden_host, void* hidden_dev, const void* router_w, const void* w13,
                              const void* w2, int T, int H, int I, int E, int topk, int renorm, moe_dtype act_dtype,
-                             moe_dtype w_dtype, const void* w13_scale, const void* w2_scale, void* out_dev,
-                             void* out_host, void* workspace, size_t workspace_bytes, const moe_options* opts,
-                             moe_stream_t stream);
+                             moe_dtype w_dtype, const void* w13_scale, const void* w2_scale, void* out_host,
+                             void* workspace, size_t workspace_bytes, const moe_options* opts, moe_stream_t stream);
 
 /* Inverse rotary position embedding fused with per-head FP8 quantisation
  *   ("Mixture-of-Experts kernel engineering on Amazon SageMaker AI", section on

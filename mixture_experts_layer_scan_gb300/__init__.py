@@ -89,7 +89,7 @@ def _load():
     lib.moe_forward_noalloc.restype = i
     lib.moe_forward_noalloc.argtypes = [P, P, P, P, i, i, i, i, i, i, i, i, P, P, P, P, P]
     lib.moe_forward_host.restype = i
-    lib.moe_forward_host.argtypes = [P, P, P, P, P, i, i, i, i, i, i, i, i, P, P, P, P, P, sz, P, P]
+    lib.moe_forward_host.argtypes = [P, P, P, P, P, i, i, i, i, i, i, i, i, P, P, P, P, sz, P, P]
     lib.moe_get_status.restype = i
     lib.moe_get_status.argtypes = [P]
     lib.moe_forward_routed.restype = i
@@ -260,12 +260,12 @@ def moe_forward(hidden: torch.Tensor, router_w: torch.Tensor, w13: torch.Tensor,
 
 
 def moe_forward_host(hidden_host: torch.Tensor, router_w: torch.Tensor, w13: torch.Tensor, w2: torch.Tensor, topk: int,
-                     renorm: bool, w13_scale=None, w2_scale=None, hidden_dev=None, out_dev=None, out_host=None,
-                     workspace=None, options=None, stream=None, w_format=None):
-    """The layer from pinned host memory to pinned host memory (moe_forward_host): the copy of
-    hidden_host into the device staging buffer hidden_dev, the layer into out_dev and the copy of
-    out_dev into out_host, all enqueued on `stream`.  Returns out_host, complete once the stream's
-    work is.  hidden_host and out_host must be page-locked (Tensor.pin_memory())."""
+                     renorm: bool, w13_scale=None, w2_scale=None, hidden_dev=None, out_host=None, workspace=None,
+                     options=None, stream=None, w_format=None):
+    """The layer from pinned host memory to pinned host memory (moe_forward_host): a copy kernel
+    brings hidden_host into the device staging buffer hidden_dev, and the layer stores its output
+    straight into out_host, all on `stream`.  Returns out_host, complete once the stream's work is.
+    hidden_host and out_host must be page-locked (Tensor.pin_memory())."""
     T, H = hidden_host.shape
     E, twoI, H2 = w13.shape
     I = twoI // 2
@@ -278,10 +278,9 @@ def moe_forward_host(hidden_host: torch.Tensor, router_w: torch.Tensor, w13: tor
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     hidden_dev = torch.empty(hidden_host.shape, dtype=hidden_host.dtype, device=dev) if hidden_dev is None else hidden_dev
-    out_dev = torch.empty_like(hidden_dev) if out_dev is None else out_dev
     out_host = torch.empty(hidden_host.shape, dtype=hidden_host.dtype).pin_memory() if out_host is None else out_host
     _check(_lib.moe_forward_host(_p(hidden_host), _p(hidden_dev), _p(router_w), _p(w13), _p(w2), T, H, I, E, topk,
-                                 int(bool(renorm)), act, wdt, _p(w13_scale), _p(w2_scale), _p(out_dev), _p(out_host),
+                                 int(bool(renorm)), act, wdt, _p(w13_scale), _p(w2_scale), _p(out_host),
                                  _p(workspace), workspace.numel(), _opts(options), _stream(stream)),
            "moe_forward_host")
     return out_host

@@ -701,33 +701,43 @@ int moe_forward(const void* hidden, const void* router_w, const void* w13, const
                        reinterpret_cast<cudaStream_t>(stream));
 }
 
-static bool host_pinned(const void* p) {
+// Page-locked host memory and the address at which the device reaches it
+// (nullptr for anything else: pageable memory, device memory, unknown pointers).
+static void* host_mapped(const void* p) {
   cudaPointerAttributes a;
   if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
     cudaGetLastError();  // (not a sticky error: clear it)
-    return false;
+    return nullptr;
   }
-  return a.type == cudaMemoryTypeHost;
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
 }
 
 int moe_forward_host(const void* hidden_host, void* hidden_dev, const void* router_w, const void* w13, const void* w2,
                      int T, int H, int I, int E, int topk, int renorm, moe_dtype act_dtype, moe_dtype w_dtype,
-                     const void* w13_scale, const void* w2_scale, void* out_dev, void* out_host, void* workspace,
+                     const void* w13_scale, const void* w2_scale, void* out_host, void* workspace,
                      size_t workspace_bytes, const moe_options* opts, moe_stream_t stream) {
   Plan pl;
   int rc = make_plan(T, H, I, E, topk, act_dtype, w_dtype, opts, &pl);
   if (rc) return rc;
   if (T == 0) return MOE_OK;
-  if (!hidden_host || !out_host || !hidden_dev || !out_dev) return MOE_ERR_ARG;
-  if (!host_pinned(hidden_host) || !host_pinned(out_host)) return MOE_ERR_ARG;
+  if (!hidden_host || !out_host || !hidden_dev) return MOE_ERR_ARG;
+  void* in_mapped = host_mapped(hidden_host);
+  void* out_mapped = host_mapped(out_host);
+  if (!in_mapped || !out_mapped) return MOE_ERR_ARG;
+  if (misaligned(hidden_dev) || misaligned(out_mapped)) return MOE_ERR_ALIGNMENT;
   const size_t bytes = (size_t)T * H * (act_dtype == MOE_F32 ? 4 : 2);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(hidden_dev, hidden_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
-  rc = moe_forward(hidden_dev, router_w, w13, w2, T, H, I, E, topk, renorm, act_dtype, w_dtype, w13_scale, w2_scale,
-                   out_dev, workspace, workspace_bytes, opts, stream);
-  if (rc) return rc;
-  if (cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
-  return MOE_OK;
+  // the batch comes in through a copy kernel that reads the host memory directly: a
+  // kernel in the library's chain of programmatically dependent launches, where a
+  // copy-engine node would end the chain (sizes that are not whole 16-byte vectors
+  // take the copy engine)
+  const cudaError_t ce = (bytes % 16 == 0 && !misaligned(in_mapped))
+                             ? launch_copy_from_host(in_mapped, hidden_dev, bytes, num_sms(), s)
+                             : cudaMemcpyAsync(hidden_dev, hidden_host, bytes, cudaMemcpyHostToDevice, s);
+  if (ce != cudaSuccess) return MOE_ERR_CUDA;
+  // the layer's last kernel stores the output straight into the host buffer
+  return moe_forward(hidden_dev, router_w, w13, w2, T, H, I, E, topk, renorm, act_dtype, w_dtype, w13_scale, w2_scale,
+                     out_mapped, workspace, workspace_bytes, opts, stream);
 }
 
 int moe_forward_routed(const void* hidden, const float* topk_w, const int32_t* topk_ids, const void* w13,

@@ -41,6 +41,10 @@ cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int B, int32_t
                          int32_t* npp, int32_t* counts, int32_t* meta, int* status, cudaStream_t s,
                          bool skip_minus_one = false, int32_t* pblk = nullptr, unsigned* zero_words = nullptr,
                          int n_zero = 0, int32_t* inv = nullptr);
+// dst (device) = bytes of page-locked host memory read by the device at src (its device
+// address); a kernel launched like the library's others (bytes and both addresses 16-byte
+// multiples, else cudaErrorInvalidValue)
+cudaError_t launch_copy_from_host(const void* src, void* dst, size_t bytes, int sms, cudaStream_t s);
 // amax over n bf16 values -> *amax_bits (float bits, must be zeroed before)
 cudaError_t launch_amax_bf16(const void* X, size_t n, unsigned* amax_bits, cudaStream_t s);
 // Xs[r] = X[sorted[r]/k] (zero rows for the sentinel) for r < num_post_pad;

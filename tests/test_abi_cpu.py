@@ -126,14 +126,13 @@ def test_forward_argument_errors_before_launch(moe):
     assert lib.moe_align(fake, 4, 2, 8, 0, fake, fake, fake, None, None) == moe.MOE_ERR_ARG
     assert lib.moe_topk_from_logits(fake, 4, 8, 9, 1, fake, fake, None) == moe.MOE_ERR_ARG
     # host-to-host forward: a no-op at T = 0; null buffers and bad sizes before any copy
-    assert lib.moe_forward_host(None, None, None, None, None, 0, 256, 256, 8, 2, 1, 1, 1, None, None, None, None, None,
-                                0, None, None) == 0
-    for hh, hd, od, oh in ((None, fake, fake, fake), (fake, None, fake, fake), (fake, fake, None, fake),
-                           (fake, fake, fake, None)):
-        assert lib.moe_forward_host(hh, hd, fake, fake, fake, 4, 256, 256, 8, 2, 1, 1, 1, None, None, od, oh, ws,
-                                    1 << 30, None, None) == moe.MOE_ERR_ARG
-    assert lib.moe_forward_host(fake, fake, fake, fake, fake, 4, 256, 256, 2000, 2, 1, 1, 1, None, None, fake, fake,
-                                ws, 1 << 30, None, None) == moe.MOE_ERR_ARG
+    assert lib.moe_forward_host(None, None, None, None, None, 0, 256, 256, 8, 2, 1, 1, 1, None, None, None, None, 0,
+                                None, None) == 0
+    for hh, hd, oh in ((None, fake, fake), (fake, None, fake), (fake, fake, None)):
+        assert lib.moe_forward_host(hh, hd, fake, fake, fake, 4, 256, 256, 8, 2, 1, 1, 1, None, None, oh, ws, 1 << 30,
+                                    None, None) == moe.MOE_ERR_ARG
+    assert lib.moe_forward_host(fake, fake, fake, fake, fake, 4, 256, 256, 2000, 2, 1, 1, 1, None, None, fake, ws,
+                                1 << 30, None, None) == moe.MOE_ERR_ARG
 
 
 def test_int4_plans_and_argument_errors(moe):
