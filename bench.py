@@ -477,12 +477,19 @@ def run_offload(dev, steps=48, warm=8, slots=48, M=8, M_big=64, steps_big=12):
         torch.cuda.synchronize()
         return (time.perf_counter() - t0) / (len(xs) - n_warm) * 1e3
 
+    def median_of_3(fn):
+        # host-clock timings wander with the host (the cached call waits on its routing):
+        # three repetitions, the median reported
+        runs = sorted((fn() for _ in range(3)), key=lambda r: r[0] if isinstance(r, tuple) else r)
+        return runs[1]
+
     modes = {"overlap": moe.CACHE_COPY_OVERLAP, "serial": moe.CACHE_COPY_SERIAL, "copy_kernel": moe.CACHE_COPY_KERNEL}
-    res["resident_ms_per_call"] = run_resident(small, warm, M)
+    res["timing"] += ", median of 3 repetitions"
+    res["resident_ms_per_call"] = median_of_3(lambda: run_resident(small, warm, M))
     res["resident_tokens_per_s"] = M / (res["resident_ms_per_call"] * 1e-3)
     for name, mode in modes.items():
         try:
-            ms, d = run_cached(mode, small, warm, M)
+            ms, d = median_of_3(lambda: run_cached(mode, small, warm, M))
         except moe.MoeError as e:
             res[f"cached_{name}"] = {"unavailable": str(e)}
             continue
@@ -490,8 +497,8 @@ def run_offload(dev, steps=48, warm=8, slots=48, M=8, M_big=64, steps_big=12):
         res[f"cached_{name}"] = {"ms_per_call": ms, "tokens_per_s": M / (ms * 1e-3),
                                  "hit_rate": d["hits"] / max(1, distinct), "misses_per_call": d["misses"] / steps,
                                  "h2d_bytes_per_call": d["bytes_h2d"] / steps}
-    ms, d = run_cached(moe.CACHE_COPY_OVERLAP, big, 2, M_big)
-    rb = run_resident(big, 2, M_big)
+    ms, d = median_of_3(lambda: run_cached(moe.CACHE_COPY_OVERLAP, big, 2, M_big))
+    rb = median_of_3(lambda: run_resident(big, 2, M_big))
     res[f"fine_decode_M{M_big}"] = {"cached_ms_per_call": ms, "resident_ms_per_call": rb,
                                     "cached_tokens_per_s": M_big / (ms * 1e-3), "passes_per_call": d["passes"] / steps_big,
                                     "misses_per_call": d["misses"] / steps_big,
