@@ -111,6 +111,39 @@ static int choose_splits(long base_tiles, int kb_total, int forced, int split_pe
   return best;
 }
 
+// K splits of swap-AB GEMM2 (no reduction kernel: the combine sums the splits).  The
+// waves of (expert, tile, split) units share HBM: a wave of n < SMs units streams each
+// unit at min(kSmStreamCap, SMs / n) times a full wave's per-unit rate, so a last,
+// partial wave -- or a single wave of a few large tiles -- costs less than a full one.
+// Step time in K-block units of a full wave:
+//   sum over waves of ceil(kb_total / s) / min(kSmStreamCap, SMs / units in the wave) + 1.
+// (Measured on the decode layers: one 128-tile wave of whole rows beats 7 or 8 splits,
+// while 32 tiles want about 4.)  The tile count is the upper bound min(E, T*k) of active
+// experts, which is exact for one token and near certain from 4E pairs on; in between
+// (4 tokens of top-2 over 8 experts activate about 5.5) a plan trusting it leaves SMs
+// idle, so those batches keep the wave count alone.
+constexpr double kSmStreamCap = 1.25;
+static int choose_splits_shared(long base_tiles, int kb_total, int forced) {
+  if (forced > 0) return std::max(1, std::min(forced, kb_total));
+  int best = 1;
+  double best_t = -1.0;
+  for (int s = 1; s <= 16 && s <= std::max(1, kb_total / 2); ++s) {
+    const int kbs = (kb_total + s - 1) / s;
+    const int se = (kb_total + kbs - 1) / kbs;
+    if (se != s) continue;
+    double t = 0.0;
+    for (long left = base_tiles * s; left > 0; left -= kPlanSms) {
+      const long n = std::min<long>(left, kPlanSms);
+      t += kbs / std::min(kSmStreamCap, (double)kPlanSms / (double)n) + 1.0;
+    }
+    if (best_t < 0.0 || t < best_t - 1e-9) {
+      best_t = t;
+      best = s;
+    }
+  }
+  return best;
+}
+
 static int check_shape(int T, int H, int I, int E, int topk) {
   if (T < 0 || H < 1 || I < 1 || E < 1 || E > 1024 || topk < 1 || topk > E || topk > 32) return MOE_ERR_ARG;
   const long long n = (long long)T * topk;
@@ -161,7 +194,10 @@ static int make_plan(int T, int H, int I, int E, int topk, moe_dtype act, moe_dt
       p.s1 = choose_splits(act_upper * (I / 128), kbt1, forced, 8);
       p.kb1 = (kbt1 + p.s1 - 1) / p.s1;
       p.s1 = (kbt1 + p.kb1 - 1) / p.kb1;
-      p.s2 = choose_splits(act_upper * ((H + 255) / 256), kbt2, forced, 0);
+      // (INT4 GEMMs are bound by the MMA rate, not by a shared HBM stream: wave counts only)
+      const bool active_known = T == 1 || n >= 4L * E;
+      p.s2 = (p.path != PATH_W4 && active_known) ? choose_splits_shared(act_upper * ((H + 255) / 256), kbt2, forced)
+                                                 : choose_splits(act_upper * ((H + 255) / 256), kbt2, forced, 0);
       p.kb2 = (kbt2 + p.s2 - 1) / p.s2;
       p.s2 = (kbt2 + p.kb2 - 1) / p.kb2;
       p.y_bf16 = false;
