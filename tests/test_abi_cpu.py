@@ -90,6 +90,22 @@ def test_plan_info(moe):
     assert moe.moe_plan_info(64, 256, 512, 8, 2, moe.MOE_F32, moe.MOE_F32)["orientation"] == 0
 
 
+@pytest.mark.parametrize("T,H,I,E,k,w,s2", [
+    (1, 4096, 14336, 8, 2, "bf16", 4),     # exactly k experts: 32 whole tiles want about 4 splits
+    (16, 4096, 14336, 8, 2, "bf16", 1),    # every expert active: one 128-tile wave of whole rows
+    (64, 4096, 14336, 8, 2, "bf16", 1),
+    (4, 4096, 14336, 8, 2, "bf16", 7),     # about 5.5 of 8 experts active: wave counts alone
+    (1, 4096, 8192, 64, 8, "e4m3", 1),     # exactly 8 experts x 16 tiles
+    (8, 2048, 768, 128, 8, "bf16", 2),     # few active experts of many: wave counts alone
+    (16, 4096, 14336, 8, 2, "int4", 7),    # INT4 is bound by the MMA rate: wave counts alone
+])
+def test_gemm2_split_plans(moe, T, H, I, E, k, w, s2):
+    """GEMM2's K splits: the shared-bandwidth model where the active-expert count is known
+    (one token, or at least 4E pairs), the wave count elsewhere and for INT4."""
+    wdt = {"bf16": moe.MOE_BF16, "e4m3": moe.MOE_E4M3, "int4": moe.MOE_INT4}[w]
+    assert moe.moe_plan_info(T, H, I, E, k, moe.MOE_BF16, wdt)["splits_gemm2"] == s2
+
+
 def test_align_capacity(moe):
     assert moe.moe_align_capacity(64, 8, 128, 16) == (512 + 128 * 15, (512 + 128 * 15) // 16)
     assert moe.moe_align_capacity(1, 2, 8, 16) == (2 + 2 * 15, 32 // 16)
