@@ -311,11 +311,17 @@ static cudaError_t launch_router(const void* X, const void* Wr, int T, int H, in
     g.K = H;
     g.W = Wr;
     g.w_rows_per_expert = E;
-    g.wbox = ((E + 15) / 16 * 16) / 2;
+    // experts in nt column tiles of N = epad / nt when the token tiles alone would leave
+    // SMs idle (N a multiple of 16, each of the tile's two weight boxes a multiple of 8 rows)
+    const int epad = (E + 15) / 16 * 16;
+    const int row_tiles = (T + 127) / 128;
+    int nt = 1;
+    while (nt < 4 && epad % (32 * nt) == 0 && 2 * nt * row_tiles <= sms) nt *= 2;
+    g.wbox = epad / (2 * nt);
     g.w_pair_off = g.wbox;
-    g.w_tile_rows = 0;
+    g.w_tile_rows = 2 * g.wbox;
     g.xbox = 128;
-    g.n_tiles = 1;
+    g.n_tiles = nt;
     g.splits = 1;
     g.kb_per_split = H * 2 / 128;
     g.cap = T;

@@ -89,7 +89,7 @@ struct Tile {
 template <bool SWAP, int EPI>
 __device__ __forceinline__ int tile_count(const TcDev& p) {
   if constexpr (EPI == TC_EPI_LOGITS)
-    return (p.T + 127) / 128;
+    return (p.T + 127) / 128 * p.n_tiles;
   else if constexpr (SWAP)
     return p.meta[META_NACT] * p.n_tiles * p.splits;
   else
@@ -100,16 +100,18 @@ template <bool SWAP, int EPI>
 __device__ __forceinline__ Tile tile_at(const TcDev& p, int t) {
   Tile d;
   if constexpr (EPI == TC_EPI_LOGITS) {
-    // router: 128 consecutive (unsorted) tokens against all experts
-    d.n = 0;
+    // router: 128 consecutive (unsorted) tokens against the experts of column tile n
+    // (2 wbox experts from n * w_tile_rows; the column tiles of a token tile are adjacent
+    // in t, so its second read of the tokens comes from L2)
+    d.n = t % p.n_tiles;
     d.s = 0;
     d.e = 0;
-    d.xrow = t * 128;
+    d.xrow = (t / p.n_tiles) * 128;
     d.ntok = 128;
     d.npad = 128;
     d.kb0 = 0;
     d.kb1 = p.kb_total;
-    d.wr0 = 0;
+    d.wr0 = d.n * p.w_tile_rows;
     return d;
   } else if constexpr (SWAP) {
     const int per_e = p.n_tiles * p.splits;
@@ -293,14 +295,15 @@ __device__ __forceinline__ void epi_tile(const TcDev& p, const Tile& d, uint32_t
   } else if constexpr (EPI == TC_EPI_LOGITS) {
     const int row = d.xrow + lrow;
     const int ncols = 2 * p.wbox;
+    const int col0 = d.n * ncols;  // first expert of this column tile
     for (int c0 = 0; c0 < ncols; c0 += 16) {
       float v[16];
       tmem_ld16(tb + (uint32_t)c0, v);
       if (row < p.T) {
-        float* dst = reinterpret_cast<float*>(p.out) + (size_t)row * p.n_valid;
+        float* dst = reinterpret_cast<float*>(p.out) + (size_t)row * p.n_valid + col0;
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-          if (c0 + j < p.n_valid) dst[c0 + j] = v[j];
+          if (col0 + c0 + j < p.n_valid) dst[c0 + j] = v[j];
       }
     }
   } else if constexpr (!SWAP && EPI == TC_EPI_G2_F32) {
@@ -1661,7 +1664,7 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s) {
 
   long upper;
   if (a.epi == TC_EPI_LOGITS)
-    upper = (a.T + 127) / 128;
+    upper = (long)(a.T + 127) / 128 * a.n_tiles;
   else if (a.swap)
     upper = (long)std::min(a.E, a.T * a.k) * a.n_tiles * a.splits;
   else
