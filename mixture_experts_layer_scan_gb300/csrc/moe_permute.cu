@@ -20,7 +20,6 @@ namespace {
 
 constexpr int kAlignThreads = 1024;
 constexpr int kAlignWarps = kAlignThreads / 32;
-constexpr int kAlignCached = 8;  // batches of 32 ids per warp kept in registers across both passes
 constexpr int kGatherThreads = 64;  // two warps (tokens) per CTA: short batches spread over SMs
 
 // Exclusive scan over blockDim.x (= 1024) values, one per thread; returns the
@@ -91,35 +90,9 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
   for (int i = threadIdx.x; i < kAlignWarps * E; i += blockDim.x) wc[i] = 0;
   __syncthreads();
 
-  // The warp's first kAlignCached batches of 32 ids are read once, all loads in flight
-  // together, and kept in registers for both passes (every loop bound is the same in
-  // all lanes of the warp); later batches are read in each pass.
-  bool bad = false;
-  const int iters = (end - beg + 31) / 32;
-  int ev[kAlignCached];
-#pragma unroll
-  for (int it = 0; it < kAlignCached; ++it) {
-    const int f = beg + 32 * it + lane;
-    int e = -1;
-    if (it < iters && f < end) {
-      e = ids[f];
-      // -1 marks a pair another pass handles (skip_minus_one): dropped without a flag
-      if (e < 0 || e >= E) { bad = bad || !(skip_minus_one && e == -1); e = -1; }
-    }
-    ev[it] = e;
-  }
-
   // pass 1: per-warp histogram
-#pragma unroll
-  for (int it = 0; it < kAlignCached; ++it) {
-    if (it < iters) {
-      const int e = ev[it];
-      const unsigned grp = __match_any_sync(0xffffffffu, e);
-      if (e >= 0 && lane == __ffs(grp) - 1) wc[warp * E + e] += __popc(grp);
-      __syncwarp();
-    }
-  }
-  for (int base = beg + 32 * kAlignCached; base < end; base += 32) {
+  bool bad = false;
+  for (int base = beg; base < end; base += 32) {
     const int f = base + lane;
     int e = -1;
     if (f < end) {
@@ -207,24 +180,7 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
   }
 
   // pass 2: stable scatter
-#pragma unroll
-  for (int it = 0; it < kAlignCached; ++it) {
-    if (it < iters) {
-      const int f = beg + 32 * it + lane;
-      const int e = ev[it];
-      const unsigned grp = __match_any_sync(0xffffffffu, e);
-      int slot = 0;
-      if (e >= 0) slot = off[e] + cbase[e] + wc[warp * E + e] + __popc(grp & ((1u << lane) - 1u));
-      __syncwarp();
-      if (e >= 0) {
-        sorted[slot] = f;
-        if (lane == __ffs(grp) - 1) wc[warp * E + e] += __popc(grp);
-      }
-      if (inv && f < end) inv[f] = e >= 0 ? slot : -1;  // pair -> sorted row (-1: left out)
-      __syncwarp();
-    }
-  }
-  for (int base = beg + 32 * kAlignCached; base < end; base += 32) {
+  for (int base = beg; base < end; base += 32) {
     const int f = base + lane;
     int e = -1;
     if (f < end) {
