@@ -449,6 +449,14 @@ static int forward_steps(const Plan& pl, int steps, const void* hidden, const vo
     MOE_TRY(launch_topk(logits, T, E_router, topk, renorm != 0, tw, tid, s));
     if (o) record(o->stage_end[MOE_STAGE_ROUTE], s);
   }
+  // routing leaves HBM idle: when every expert is almost surely active (T*k at least
+  // 8 E pairs), each swap-AB GEMM1 CTA prefetches its first tile's first weights into L2
+  // while the routing runs (a hint: a wrong guess costs only idle bandwidth).  Otherwise
+  // the row gather lets GEMM1 launch only once the permutation is complete, and GEMM1
+  // streams its first weight stages into shared memory while the gather runs.
+  const bool g1_prefetch = pl.swap && !gate && (long)T * topk >= 8L * E;
+  const bool g1_early = pl.swap && pl.path != PATH_W4 && !pl.gather_in_gemm && !inv && !gate && !g1_prefetch;
+
   if (!(steps & (STEPS_EXPERTS | STEPS_COMBINE))) return MOE_OK;
   if (!(steps & STEPS_EXPERTS)) goto combine_step;
 
@@ -473,10 +481,10 @@ static int forward_steps(const Plan& pl, int steps, const void* hidden, const vo
     if (pl.gather_in_gemm)
       MOE_TRY(launch_quant_x(hidden, (size_t)T * H, amax, (uint8_t*)xs, s));
     else
-      MOE_TRY(launch_gather(hidden, T, H, topk, 2, 1, amax, sorted, nullptr, meta, cap, xs, s));
+      MOE_TRY(launch_gather(hidden, T, H, topk, 2, 1, amax, sorted, nullptr, meta, cap, xs, g1_early, s));
   } else if (!pl.gather_in_gemm) {
     MOE_TRY(launch_gather(hidden, T, H, topk, pl.path == PATH_F32 ? 4 : 2, 0, nullptr, sorted, inv, meta, cap, xs,
-                          s));
+                          g1_early, s));
   }
   if (o) record(o->stage_end[MOE_STAGE_GATHER], s);
 
@@ -531,13 +539,12 @@ static int forward_steps(const Plan& pl, int steps, const void* hidden, const vo
     g1.a_amax = amax;
     g1.amax_out = amax + 1;
     g1.ready = gate ? gate->ready13 : nullptr;
-    // routing leaves HBM idle: when every expert is almost surely active (T*k at least
-    // 8 E pairs), each GEMM1 CTA prefetches its first tile's first weights into L2,
-    // about 64 MB over the grid (a hint: a wrong guess costs only idle bandwidth)
-    if (pl.swap && !gate && (long)T * topk >= 8L * E) {
+    // the routing-phase L2 prefetch: about 64 MB over the grid
+    if (g1_prefetch) {
       const long kb_bytes = 2L * 128 * 128;  // both 128-row boxes of one K block
       g1.prefetch_kb = (int)std::max<long>(1, (64L << 20) / (kb_bytes * std::max(1, sms)));
     }
+    g1.early = g1_early;
     void* aint_lo = pl.act_split ? (void*)((uint16_t*)aint + (size_t)cap * I) : nullptr;
     if (pl.s1 > 1) {
       g1.epi = TC_EPI_G1_PART;

@@ -50,10 +50,12 @@ cudaError_t launch_amax_bf16(const void* X, size_t n, unsigned* amax_bits, cudaS
 // Xs[r] = X[sorted[r]/k] (zero rows for the sentinel) for r < num_post_pad;
 // mode 0: copy elements of elem_bytes, token by token through inv when it is given
 // (launch_align's inverse map; k <= 32: every token row read once), else row by row;
-// mode 1: bf16 -> e4m3 with scale amax/448 (inv unused)
+// mode 1: bf16 -> e4m3 with scale amax/448 (inv unused).
+// late (row-by-row copy and mode 1): let dependents launch only after this kernel's own
+// dependency wait, so the permutation is complete when the next kernel starts.
 cudaError_t launch_gather(const void* X, int T, int H, int k, int elem_bytes, int mode, const unsigned* amax_bits,
                           const int32_t* sorted, const int32_t* inv, const int32_t* meta, int cap, void* Xs,
-                          cudaStream_t s);
+                          bool late, cudaStream_t s);
 // split-K reduction of the GEMM1 partials P[split][pair][2I] + scale + SiLU(gate)*up
 // into sorted rows (row r holds pair sorted[r]).
 //   out_mode 0: bf16 A_int   1: fp32 A (+ amax into amax_bits)

@@ -285,8 +285,14 @@ __global__ void __launch_bounds__(kGatherThreads) k_gather_scatter(const uint4* 
 // batches, whose token rows stay in L2, this spreads the copies over the most warps.
 __global__ void __launch_bounds__(256) k_gather_copy(const uint4* __restrict__ X, int vec_per_row, int k,
                                                      int n_pairs, const int32_t* __restrict__ sorted,
-                                                     const int32_t* __restrict__ meta, uint4* __restrict__ Xs) {
-  pdl_enter();
+                                                     const int32_t* __restrict__ meta, uint4* __restrict__ Xs,
+                                                     int late) {
+  // late: dependents launch only once the permutation is complete (after this kernel's own
+  // dependency wait), so GEMM1 may read its tile list and stream weights before its wait;
+  // otherwise they launch at once (GEMM1 then prefetches guessed weights into L2 meanwhile)
+  if (!late) pdl_launch_dependents();
+  pdl_wait();
+  if (late) pdl_launch_dependents();
   // one warp per row; each lane has kGatherUnroll 16-byte loads in flight before its stores
   constexpr int kGatherUnroll = 8;
   const int npp = meta[META_NPP];
@@ -316,8 +322,10 @@ __global__ void __launch_bounds__(256) k_gather_copy(const uint4* __restrict__ X
 // Gather + dynamic per-tensor e4m3 quantisation: code = e4m3(x / s), s = amax/448.
 __global__ void k_gather_quant(const uint4* __restrict__ X, int vec_per_row /* 8 bf16 each */, int k, int n_pairs,
                                const int32_t* __restrict__ sorted, const int32_t* __restrict__ meta,
-                               const unsigned* __restrict__ amax_bits, uint2* __restrict__ Xq) {
-  pdl_enter();
+                               const unsigned* __restrict__ amax_bits, uint2* __restrict__ Xq, int late) {
+  if (!late) pdl_launch_dependents();  // (late: as in k_gather_copy)
+  pdl_wait();
+  if (late) pdl_launch_dependents();
   const int npp = meta[META_NPP];
   const float s = e4m3_scale_from_amax(__uint_as_float(*amax_bits));
   for (int r = blockIdx.x; r < npp; r += gridDim.x) {
@@ -605,7 +613,7 @@ cudaError_t launch_amax_bf16(const void* X, size_t n, unsigned* amax_bits, cudaS
 
 cudaError_t launch_gather(const void* X, int T, int H, int k, int elem_bytes, int mode, const unsigned* amax_bits,
                           const int32_t* sorted, const int32_t* inv, const int32_t* meta, int cap, void* Xs,
-                          cudaStream_t s) {
+                          bool late, cudaStream_t s) {
   const int grid = cap < 152 * 8 ? (cap > 0 ? cap : 1) : 152 * 8;
   if (mode == 0) {
     const int vpr = H * elem_bytes / 16;
@@ -618,11 +626,12 @@ cudaError_t launch_gather(const void* X, int T, int H, int k, int elem_bytes, in
     } else {
       const int rows_grid = std::max(1, std::min((cap + 7) / 8, 152 * 8));  // 8 warps (rows) per CTA
       MOE_LAUNCH(k_gather_copy, dim3(rows_grid), dim3(256), 0, s, (const uint4*)X, vpr, k, T * k, sorted, meta,
-                 (uint4*)Xs);
+                 (uint4*)Xs, late ? 1 : 0);
     }
   } else {
     const int vpr = H / 8;
-    MOE_LAUNCH(k_gather_quant, dim3(grid), dim3(128), 0, s, (const uint4*)X, vpr, k, T * k, sorted, meta, amax_bits, (uint2*)Xs);
+    MOE_LAUNCH(k_gather_quant, dim3(grid), dim3(128), 0, s, (const uint4*)X, vpr, k, T * k, sorted, meta, amax_bits,
+               (uint2*)Xs, late ? 1 : 0);
   }
   return cudaGetLastError();
 }
