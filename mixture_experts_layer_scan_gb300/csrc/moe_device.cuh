@@ -177,6 +177,15 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity, u
   }
 }
 
+// Untiled bulk copy global -> shared (the CTA's own shared memory), completion
+// counted in bytes on an mbarrier.  dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t smem_dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // TMA (tiled 2-D bulk tensor copy global -> shared, completion on an mbarrier)
 // ---------------------------------------------------------------------------
