@@ -215,6 +215,96 @@ __global__ void __launch_bounds__(kAlignThreads, 1)
   }
 }
 
+// The same permutation for batches of at most 32 pairs (decode), by one warp: each
+// lane holds one pair, warp match gives every pair's expert group, its size and the
+// pair's rank inside it (lower flat index first: the same stable order), and the group
+// leaders -- the active experts -- find their padded offsets by comparing expert ids
+// over the warp and write their own block map entries and sentinel rows.  The leaders'
+// (expert, offset, count) sorted by expert give every expert's offset and count.  No
+// block barrier and no second read of the ids:
+// the general kernel's phases cost about 0.5 us each at this size.  Outputs equal the
+// general kernel's (pblk is not produced here).
+constexpr int kAlignSmallThreads = 128;
+
+__global__ void __launch_bounds__(kAlignSmallThreads)
+    k_align_small(const int32_t* __restrict__ ids, int n, int E, int B, int32_t* __restrict__ sorted,
+                  int32_t* __restrict__ eids, int32_t* __restrict__ npp_out, int32_t* __restrict__ counts_out,
+                  int32_t* __restrict__ meta, int* status, int skip_minus_one, unsigned* __restrict__ zero_words,
+                  int n_zero, int32_t* __restrict__ inv) {
+  pdl_enter();
+  for (int i = threadIdx.x; i < n_zero; i += blockDim.x) zero_words[i] = 0u;
+  if (threadIdx.x >= 32) return;
+  __shared__ int s_e[32], s_off[32], s_c[32];  // active experts in ascending order
+  const int lane = threadIdx.x;
+  int e = -1;
+  if (lane < n) {
+    e = ids[lane];
+    if (e < 0 || e >= E) {
+      if (!(skip_minus_one && e == -1)) report(status, MOE_ERR_DEVICE_INDEX);
+      e = -1;
+    }
+  }
+  const unsigned grp = __match_any_sync(0xffffffffu, e);
+  const int c = __popc(grp);
+  const bool leader = e >= 0 && lane == __ffs(grp) - 1;
+  const unsigned leaders = __ballot_sync(0xffffffffu, leader);
+  const int pad = (c + B - 1) / B * B;
+  // experts below mine among the active ones, and their padded rows
+  int below = 0, off = 0;
+  for (int j = 0; j < 32; ++j) {
+    const int ej = __shfl_sync(0xffffffffu, e, j);
+    const int pj = __shfl_sync(0xffffffffu, pad, j);
+    if (((leaders >> j) & 1u) && ej < e) {
+      ++below;
+      off += pj;
+    }
+  }
+  int total = leader ? pad : 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+  const int nact = __popc(leaders);
+  if (leader) {
+    s_e[below] = e;
+    s_off[below] = off;
+    s_c[below] = c;
+    if (meta) meta[meta_active(E) + below] = e;
+  }
+  if (e >= 0) {
+    const int slot = off + __popc(grp & ((1u << lane) - 1u));
+    sorted[slot] = lane;
+    if (inv) inv[lane] = slot;
+  } else if (inv && lane < n) {
+    inv[lane] = -1;
+  }
+  // block -> expert map and sentinel rows: each active expert's leader writes its own run
+  if (leader) {
+    for (int b = off / B; b < (off + pad) / B; ++b) eids[b] = e;
+    for (int q = off + c; q < off + pad; ++q) sorted[q] = n;
+  }
+  __syncwarp();
+  // every expert's offset and count: those of the first active expert at or above it
+  // (lane x visits x, x + 32, ...: the active index lo only moves forward)
+  int lo = 0;
+  for (int x = lane; x < E; x += 32) {
+    while (lo < nact && s_e[lo] < x) ++lo;
+    const int cnt = (lo < nact && s_e[lo] == x) ? s_c[lo] : 0;
+    if (meta) {
+      meta[meta_offsets(E) + x] = lo < nact ? s_off[lo] : total;
+      meta[meta_counts(E) + x] = cnt;
+    }
+    if (counts_out) counts_out[x] = cnt;
+  }
+  if (lane == 0) {
+    *npp_out = total;
+    if (meta) {
+      meta[META_NPP] = total;
+      meta[META_NBLK] = total / B;
+      meta[META_NACT] = nact;
+      meta[meta_offsets(E) + E] = total;
+    }
+  }
+}
+
 // amax over n bf16 values (bit pattern of a non-negative float, atomicMax on
 // the bits is order independent).
 __global__ void k_amax_bf16(const uint16_t* __restrict__ X, size_t n, unsigned* amax_bits) {
@@ -574,6 +664,11 @@ cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int B, int32_t
                          bool skip_minus_one, int32_t* pblk, unsigned* zero_words, int n_zero, int32_t* inv) {
   if (pblk && B != 128) return cudaErrorInvalidValue;
   if (n_zero > 0 && !zero_words) return cudaErrorInvalidValue;
+  if ((long)T * k <= 32 && !pblk) {
+    MOE_LAUNCH(k_align_small, dim3(1), dim3(kAlignSmallThreads), 0, s, ids, T * k, E, B, sorted, eids, npp, counts,
+               meta, status, skip_minus_one ? 1 : 0, zero_words, n_zero, inv);
+    return cudaGetLastError();
+  }
   const size_t smem = (size_t)(kAlignWarps * E + 4 * E + 1 + 33) * sizeof(int);
   static bool configured[64] = {};
   int dev = 0;

@@ -82,7 +82,10 @@ def _random_ids(T, k, E, seed, skew=False):
     return np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
 
 
-@pytest.mark.parametrize("T,k,E,B", [(1, 1, 1, 1), (1, 2, 8, 16), (37, 2, 8, 16), (64, 8, 128, 16), (100, 3, 5, 4),
+# (up to 32 pairs go to a single-warp kernel: the first rows of the list)
+@pytest.mark.parametrize("T,k,E,B", [(1, 1, 1, 1), (1, 2, 8, 16), (1, 8, 128, 16), (4, 8, 128, 16), (3, 8, 1024, 16),
+                                     (16, 2, 8, 16), (2, 3, 7, 1), (5, 6, 40, 128), (4, 8, 64, 1000), (3, 10, 33, 16),
+                                     (37, 2, 8, 16), (64, 8, 128, 16), (100, 3, 5, 4),
                                      (257, 8, 64, 128), (1000, 6, 1024, 16), (8192, 8, 64, 128), (333, 7, 9, 1024)])
 def test_align_bit_exact(moe, T, k, E, B):
     ids = _random_ids(T, k, E, T + 31 * E, skew=(T % 2 == 0))
@@ -95,6 +98,24 @@ def test_align_bit_exact(moe, T, k, E, B):
     assert np.array_equal(s.cpu().numpy()[:n], rs)
     assert np.array_equal(ex.cpu().numpy()[: n // B], rex)
     assert np.array_equal(counts.cpu().numpy(), rcounts)
+
+
+@pytest.mark.parametrize("T,k", [(3, 8), (512, 8)])
+def test_align_drops_and_flags_bad_ids(moe, T, k):
+    ids = _random_ids(T, k, 64, 11)
+    bad = ids.copy()
+    bad[1, 2] = 64
+    bad[2, 0] = -2
+    s, ex, npp, counts = moe.moe_align(torch.from_numpy(bad).cuda(), 64, 16)
+    assert moe.moe_get_status() == moe.MOE_ERR_DEVICE_INDEX
+    assert moe.moe_get_status() == 0
+    keep = (bad >= 0) & (bad < 64)
+    rcounts = np.bincount(bad[keep], minlength=64)
+    assert np.array_equal(counts.cpu().numpy(), rcounts)
+    n = int(npp.item())
+    rows = s.cpu().numpy()[:n]
+    flat = np.flatnonzero(keep.reshape(-1))
+    assert np.array_equal(np.sort(rows[rows < T * k]), flat)  # every kept pair once, no dropped one
 
 
 def test_align_is_deterministic_and_flags_bad_ids(moe):
