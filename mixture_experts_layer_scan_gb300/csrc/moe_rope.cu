@@ -13,14 +13,16 @@
 //     y_{half+i} = x_{half+i} c_i - x_i s_i            (rotation by -angle: the inverse)
 //     y_j        = x_j                                 R <= j < D (not rotated)
 //   scale[t][h] = max_j |y_j| / 448 (1 when that is 0)
-//   Q[t][h][j]  = e4m3(y_j * r), r = 1 / scale[t][h] (one fp32 division per
-//                 vector), round to nearest even, saturating
+//   Q[t][h][j]  = e4m3(y_j * r), r = 1 / scale[t][h] (one correctly rounded fp32
+//                 reciprocal per vector), round to nearest even, saturating
 // Products, sums and the reciprocal are separate fp32 roundings (no fused
 // multiply-add), so the codes are reproducible in plain fp32 arithmetic.
 //
-// Layouts with 16-byte granularity go to a kernel where a group of lanes shares
-// a vector and moves 8 elements per access (below); others to one warp per
-// vector with 4-byte accesses.  HBM bound: 3 bytes per element plus 4 per scale.
+// Layouts with 16-byte granularity go to kernels where a group of lanes shares
+// a vector and moves 8 elements per access: loads into registers on a persistent
+// grid, or -- long vectors from 4 MB of input -- a shared-memory ring filled by
+// bulk copies (below); others to one warp per vector with 4-byte accesses.  HBM
+// bound: 3 bytes per element plus 4 per scale.
 #include <algorithm>
 #include <climits>
 
