@@ -126,6 +126,20 @@ def test_swap_ab_identity_both_orientations(moe):
     assert rel_err(a, b, "swap-AB vs token-major") <= TOL["bf16"]
 
 
+# Pre-gathered swap-AB batches (more than 32 tokens) with fewer than 8 pairs per expert:
+# the row gather lets GEMM1 launch only after its own dependency wait and GEMM1 streams
+# its first weight stages before it waits (bf16, with and without K splits, and FP8,
+# whose gather also quantises).
+@pytest.mark.parametrize("name,T,H,I,E,k", [("mixtral_decode", 40, 256, 384, 64, 4),
+                                            ("fine_decode", 48, 512, 256, 128, 8),
+                                            ("fp8_decode", 40, 256, 256, 64, 4)])
+def test_gemm1_streams_during_gather(moe, name, T, H, I, E, k):
+    assert T * k < 8 * E and T > 32
+    L = _layer(name, T=T, H=H, I=I, E=E, k=k)
+    out = _run(moe, L, {"orientation": 1})
+    assert_parity(out.float().cpu().numpy(), _ref(L), "e4m3" if name == "fp8_decode" else "bf16", "")
+
+
 @pytest.mark.parametrize("T,orient", [(1, 1), (16, 1), (64, 1), (130, 2), (7, 2)])
 def test_fp8_path(moe, T, orient):
     L = _layer("fp8_decode", T=T, H=256, I=256, E=8, k=4)
