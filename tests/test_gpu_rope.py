@@ -1,8 +1,8 @@
 """GPU parity of the inverse rotary embedding + per-head e4m3 quantisation kernel against
 the oracle: codes and scales bit for bit (both sides decide every code in the same fp32
 arithmetic), over rotated / partly rotated / unrotated heads, head sizes up to 1024,
-zero vectors, the first and last table positions, the shared-memory staged form of the
-kernel on odd layouts, and the full-size prefill layout.
+zero vectors, the first and last table positions, the persistent and shared-memory staged
+forms of the kernel on odd large layouts, and the full-size prefill layout.
 """
 import numpy as np
 import pytest
@@ -50,22 +50,24 @@ def test_zero_vectors_and_table_edges(moe):
     _check(moe, d)
 
 
-# From 4 MB of input the kernel stages chunks of consecutive vectors (and their tokens'
-# table rows) through shared memory: head counts that do not divide a chunk, a chunk
-# per token and less, partly rotated heads, and a ragged last chunk.
+# Large inputs: long vectors (32 lanes each) from 4 MB go through the kernel that stages
+# chunks of consecutive vectors and their tokens' table rows in shared memory (head counts
+# that do not divide a chunk, partly rotated heads, a ragged last chunk); short vectors
+# through the persistent register kernel (odd head counts, one head per token).
 @pytest.mark.parametrize("T,heads,D,R", [(5000, 7, 128, 128), (300, 40, 200, 64), (20000, 1, 128, 96),
                                          (1100, 9, 576, 64)])
-def test_inv_rope_fp8_staged_bit_exact(moe, T, heads, D, R):
+def test_inv_rope_fp8_large_bit_exact(moe, T, heads, D, R):
     d = make_rope_inputs(rope_spec("gqa_decode", T=T, heads=heads, head_dim=D, rot_dim=R, max_pos=4096))
     assert T * heads * D * 2 >= 4 << 20
     _check(moe, d)
 
 
-def test_staged_position_outside_table_is_flagged(moe):
-    d = make_rope_inputs(rope_spec("gqa_decode", T=5000, heads=7, max_pos=4096))
+@pytest.mark.parametrize("T,heads,D,R", [(5000, 7, 128, 128), (1100, 9, 576, 64)])
+def test_large_position_outside_table_is_flagged(moe, T, heads, D, R):
+    d = make_rope_inputs(rope_spec("gqa_decode", T=T, heads=heads, head_dim=D, rot_dim=R, max_pos=4096))
     pos = d["pos"].clone()
-    pos[4321] = -1
-    moe.moe_inv_rope_fp8_quant(d["x"].cuda(), pos.cuda(), d["cos_sin"].cuda(), 128)
+    pos[T - 679] = -1
+    moe.moe_inv_rope_fp8_quant(d["x"].cuda(), pos.cuda(), d["cos_sin"].cuda(), R)
     assert moe.moe_get_status() == moe.MOE_ERR_DEVICE_INDEX
     assert moe.moe_get_status() == 0
 
