@@ -80,6 +80,68 @@ __device__ __forceinline__ void router_block(const TIn* __restrict__ X, const TI
   cta_sync();  // red is free again
 }
 
+// The same logits for TT tokens and EB experts (e0 .. e0+EB-1, < E) per block, with
+// the arithmetic of router_block for every logit: lane-sequential fma over its
+// 16-byte vectors, the fixed butterfly, warp sums in warp order.  Inputs stay in
+// registers as raw 16-byte vectors and are widened inside the fma loop.
+// red: shared scratch of kRouterWarps * TT * EB floats.
+__device__ __forceinline__ float router_elem(const uint4& u, int q, const __nv_bfloat16*) {
+  const uint32_t w = q < 2 ? u.x : q < 4 ? u.y : q < 6 ? u.z : u.w;
+  return bf16_bits_to_f32((q & 1) ? (w >> 16) : (w & 0xffffu));
+}
+__device__ __forceinline__ float router_elem(const uint4& u, int q, const float*) {
+  return __uint_as_float(q == 0 ? u.x : q == 1 ? u.y : q == 2 ? u.z : u.w);
+}
+
+template <typename TIn, int TT, int EB>
+__device__ __forceinline__ void router_tile(const TIn* __restrict__ X, const TIn* __restrict__ Wr, int T, int H,
+                                            int E, int t0, int e0, float* __restrict__ logits, float* red) {
+  constexpr int V = 16 / sizeof(TIn);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nt = min(TT, T - t0), ne = min(EB, E - e0);
+  float acc[EB][TT];
+#pragma unroll
+  for (int c = 0; c < EB; ++c)
+#pragma unroll
+    for (int b = 0; b < TT; ++b) acc[c][b] = 0.0f;
+  for (int h = (warp * 32 + lane) * V; h < H; h += kRouterWarps * 32 * V) {
+    // every row is loaded (rows past the batch or the experts re-read the last one)
+    uint4 wr[EB], xr[TT];
+#pragma unroll
+    for (int c = 0; c < EB; ++c) wr[c] = *reinterpret_cast<const uint4*>(Wr + (size_t)(e0 + min(c, ne - 1)) * H + h);
+#pragma unroll
+    for (int b = 0; b < TT; ++b) xr[b] = *reinterpret_cast<const uint4*>(X + (size_t)(t0 + min(b, nt - 1)) * H + h);
+#pragma unroll
+    for (int q = 0; q < V; ++q) {
+#pragma unroll
+      for (int c = 0; c < EB; ++c) {
+        const float w = router_elem(wr[c], q, X);
+#pragma unroll
+        for (int b = 0; b < TT; ++b) acc[c][b] = fmaf(w, router_elem(xr[b], q, X), acc[c][b]);
+      }
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < EB; ++c)
+#pragma unroll
+    for (int b = 0; b < TT; ++b) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) acc[c][b] += __shfl_xor_sync(0xffffffffu, acc[c][b], off);
+      if (lane == 0) red[(warp * EB + c) * TT + b] = acc[c][b];
+    }
+  cta_sync();
+  if ((int)threadIdx.x < EB * TT) {
+    const int c = threadIdx.x / TT, b = threadIdx.x % TT;
+    if (c < ne && b < nt) {
+      float sum = 0.0f;
+#pragma unroll
+      for (int w8 = 0; w8 < kRouterWarps; ++w8) sum += red[(w8 * EB + c) * TT + b];
+      logits[(size_t)(t0 + b) * E + e0 + c] = sum;
+    }
+  }
+  cta_sync();  // red is free again
+}
+
 constexpr int kTopkCache = 8;  // logits per lane kept in registers by the top-k
 
 // (value, index) order of the ranking: larger value first, lower index on ties.
