@@ -305,6 +305,108 @@ __global__ void __launch_bounds__(kAlignSmallThreads)
   }
 }
 
+// The same permutation for 33 to 1024 pairs by one CTA, one pair per thread (pair f
+// in thread f): warp match gives each pair's rank inside its warp and the warp's
+// count of its expert (wc[warp][e], also added into the expert's total); a pair's
+// stable slot is its expert's offset plus the counts of the lower warps plus its
+// rank.  One warp scans the padded counts into offsets; every expert's thread then
+// writes its block-map entries and sentinel rows.  Three block barriers (the general
+// kernel has about a dozen).  Outputs equal the general kernel's (pblk not produced).
+__global__ void __launch_bounds__(kAlignThreads, 1)
+    k_align_mid(const int32_t* __restrict__ ids, int n, int E, int B, int32_t* __restrict__ sorted,
+                int32_t* __restrict__ eids, int32_t* __restrict__ npp_out, int32_t* __restrict__ counts_out,
+                int32_t* __restrict__ meta, int* status, int skip_minus_one, unsigned* __restrict__ zero_words,
+                int n_zero, int32_t* __restrict__ inv) {
+  pdl_enter();
+  for (int i = threadIdx.x; i < n_zero; i += blockDim.x) zero_words[i] = 0u;
+  extern __shared__ int sm[];
+  int* wc = sm;            // [kAlignWarps][E] counts of each expert in each warp
+  int* cnt = wc + kAlignWarps * E;  // [E]
+  int* off = cnt + E;      // [E + 1]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < kAlignWarps * E; i += blockDim.x) wc[i] = 0;
+  for (int i = threadIdx.x; i < E; i += blockDim.x) cnt[i] = 0;
+  const int f = threadIdx.x;
+  int e = -1;
+  if (f < n) {
+    e = ids[f];
+    if (e < 0 || e >= E) {
+      if (!(skip_minus_one && e == -1)) report(status, MOE_ERR_DEVICE_INDEX);
+      e = -1;
+    }
+  }
+  __syncthreads();
+  const unsigned grp = __match_any_sync(0xffffffffu, e);
+  const int rank = __popc(grp & ((1u << lane) - 1u));
+  if (e >= 0 && lane == __ffs(grp) - 1) {
+    wc[warp * E + e] = __popc(grp);
+    atomicAdd(&cnt[e], __popc(grp));  // (a total: the order of the additions does not matter)
+  }
+  __syncthreads();
+  int below = 0;  // pairs of my expert in lower warps
+  if (e >= 0)
+    for (int w = 0; w < warp; ++w) below += wc[w * E + e];
+  if (warp == 0) {
+    // offsets: lane l scans experts [l*per, l*per + per) after a warp scan of the lane sums
+    const int per = (E + 31) / 32, x0 = min(E, lane * per), x1 = min(E, x0 + per);
+    int lp = 0, la = 0;
+    for (int x = x0; x < x1; ++x) {
+      const int c = cnt[x];
+      lp += (c + B - 1) / B * B;
+      la += c > 0 ? 1 : 0;
+    }
+    int ip = lp, ia = la;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int up = __shfl_up_sync(0xffffffffu, ip, o), ua = __shfl_up_sync(0xffffffffu, ia, o);
+      if (lane >= o) {
+        ip += up;
+        ia += ua;
+      }
+    }
+    const int total = __shfl_sync(0xffffffffu, ip, 31), nact = __shfl_sync(0xffffffffu, ia, 31);
+    int rp = ip - lp, ra = ia - la;
+    for (int x = x0; x < x1; ++x) {
+      const int c = cnt[x];
+      off[x] = rp;
+      if (meta) {
+        meta[meta_offsets(E) + x] = rp;
+        meta[meta_counts(E) + x] = c;
+        if (c > 0) meta[meta_active(E) + ra] = x;
+      }
+      if (counts_out) counts_out[x] = c;
+      ra += c > 0 ? 1 : 0;
+      rp += (c + B - 1) / B * B;
+    }
+    if (lane == 0) {
+      off[E] = total;
+      *npp_out = total;
+      if (meta) {
+        meta[META_NPP] = total;
+        meta[META_NBLK] = total / B;
+        meta[META_NACT] = nact;
+        meta[meta_offsets(E) + E] = total;
+      }
+    }
+  }
+  __syncthreads();
+  if (e >= 0) {
+    const int slot = off[e] + below + rank;
+    sorted[slot] = f;
+    if (inv) inv[f] = slot;
+  } else if (inv && f < n) {
+    inv[f] = -1;
+  }
+  // block map and sentinel rows, one expert per thread
+  for (int x = threadIdx.x; x < E; x += blockDim.x) {
+    const int c = cnt[x];
+    if (c == 0) continue;
+    const int o = off[x], pad = (c + B - 1) / B * B;
+    for (int b = o / B; b < (o + pad) / B; ++b) eids[b] = x;
+    for (int q = o + c; q < o + pad; ++q) sorted[q] = n;
+  }
+}
+
 // amax over n bf16 values (bit pattern of a non-negative float, atomicMax on
 // the bits is order independent).
 __global__ void k_amax_bf16(const uint16_t* __restrict__ X, size_t n, unsigned* amax_bits) {
@@ -667,6 +769,20 @@ cudaError_t launch_align(const int32_t* ids, int T, int k, int E, int B, int32_t
   if ((long)T * k <= 32 && !pblk) {
     MOE_LAUNCH(k_align_small, dim3(1), dim3(kAlignSmallThreads), 0, s, ids, T * k, E, B, sorted, eids, npp, counts,
                meta, status, skip_minus_one ? 1 : 0, zero_words, n_zero, inv);
+    return cudaGetLastError();
+  }
+  if ((long)T * k <= kAlignThreads && !pblk) {
+    static bool mid_configured[64] = {};
+    int mdev = 0;
+    cudaGetDevice(&mdev);
+    if (mdev < 0 || mdev >= 64 || !mid_configured[mdev]) {
+      cudaError_t e = cudaFuncSetAttribute(k_align_mid, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+      if (e != cudaSuccess) return e;
+      if (mdev >= 0 && mdev < 64) mid_configured[mdev] = true;
+    }
+    const size_t msmem = (size_t)(kAlignWarps * E + 2 * E + 1) * sizeof(int);
+    MOE_LAUNCH(k_align_mid, dim3(1), dim3(kAlignThreads), msmem, s, ids, T * k, E, B, sorted, eids, npp, counts, meta,
+               status, skip_minus_one ? 1 : 0, zero_words, n_zero, inv);
     return cudaGetLastError();
   }
   const size_t smem = (size_t)(kAlignWarps * E + 4 * E + 1 + 33) * sizeof(int);

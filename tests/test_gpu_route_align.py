@@ -82,10 +82,12 @@ def _random_ids(T, k, E, seed, skew=False):
     return np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
 
 
-# (up to 32 pairs go to a single-warp kernel: the first rows of the list)
+# (up to 32 pairs go to a single-warp kernel, up to 1024 to a one-pair-per-thread kernel,
+# more to the block-wide kernel: the list covers all three and their boundaries)
 @pytest.mark.parametrize("T,k,E,B", [(1, 1, 1, 1), (1, 2, 8, 16), (1, 8, 128, 16), (4, 8, 128, 16), (3, 8, 1024, 16),
                                      (16, 2, 8, 16), (2, 3, 7, 1), (5, 6, 40, 128), (4, 8, 64, 1000), (3, 10, 33, 16),
-                                     (37, 2, 8, 16), (64, 8, 128, 16), (100, 3, 5, 4),
+                                     (37, 2, 8, 16), (64, 8, 128, 16), (100, 3, 5, 4), (128, 8, 128, 16),
+                                     (33, 1, 1024, 16), (40, 8, 1024, 1), (17, 3, 7, 1000), (129, 8, 64, 16),
                                      (257, 8, 64, 128), (1000, 6, 1024, 16), (8192, 8, 64, 128), (333, 7, 9, 1024)])
 def test_align_bit_exact(moe, T, k, E, B):
     ids = _random_ids(T, k, E, T + 31 * E, skew=(T % 2 == 0))
@@ -100,7 +102,7 @@ def test_align_bit_exact(moe, T, k, E, B):
     assert np.array_equal(counts.cpu().numpy(), rcounts)
 
 
-@pytest.mark.parametrize("T,k", [(3, 8), (512, 8)])
+@pytest.mark.parametrize("T,k", [(3, 8), (64, 8), (512, 8)])
 def test_align_drops_and_flags_bad_ids(moe, T, k):
     ids = _random_ids(T, k, 64, 11)
     bad = ids.copy()
