@@ -40,6 +40,34 @@ def test_topk_from_logits_bit_exact(moe, T, E, k, renorm):
     np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=1e-5, atol=1e-7)
 
 
+def test_topk_special_values(moe):
+    """Ranking by value, lower expert index on equal values: -0 and +0 are equal, -inf
+    logits rank (last), NaN logits never rank; when fewer than k experts rank, the
+    remaining picks are expert 0 with weight 0 (renormalised weights)."""
+    E, k = 64, 8
+    lg = np.random.default_rng(5).standard_normal((3, E)).astype(np.float32)
+    lg[0] = -(np.abs(lg[0]) + 1.0)          # every other value below -1
+    lg[0, [3, 9, 40]] = 9.0                 # equal top values
+    lg[0, 17], lg[0, 5] = 8.0, 8.0
+    lg[0, 20], lg[0, 12] = np.float32(-0.0), np.float32(0.0)  # -0 and +0 tie: picks 6 and 7
+    lg[1, :] = -np.inf
+    lg[1, [7, 33]] = [1.0, 2.0]
+    lg[2, :] = np.nan
+    lg[2, [4, 44, 60, 2, 31]] = [0.5, 0.25, 0.5, -1.0, 3.0]
+    w, ids = moe.moe_topk_from_logits(torch.from_numpy(lg).cuda(), k, True)
+    ids, w = ids.cpu().numpy(), w.cpu().numpy()
+    for t in range(3):
+        v = lg[t].astype(np.float64)
+        ranked = sorted([e for e in range(E) if not np.isnan(v[e])], key=lambda e: (-v[e], e))[:k]
+        want = ranked + [0] * (k - len(ranked))
+        assert list(ids[t]) == want, (t, list(ids[t]), want)
+        vals = np.array([v[e] for e in ranked] + [-np.inf] * (k - len(ranked)))
+        ex = np.exp(vals - vals[0])
+        np.testing.assert_allclose(w[t], ex / ex.sum(), rtol=1e-5, atol=1e-7)
+    # -0 and +0 tie: the lower index (12) comes first
+    assert list(ids[0]).index(12) < list(ids[0]).index(20)
+
+
 @pytest.mark.parametrize("name,T", [("tiny_f32", 64), ("mixtral_decode", 64), ("fine_decode", 64),
                                     ("fp8_decode", 64), ("prefill", 8192), ("prefill_hot", 8192)])
 def test_route_matches_oracle(moe, name, T):
