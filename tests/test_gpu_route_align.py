@@ -85,11 +85,14 @@ def test_route_matches_oracle(moe, name, T):
 
 
 @pytest.mark.parametrize("T,H,E,k", [(256, 256, 40, 6), (300, 384, 256, 8), (1000, 128, 8, 2), (255, 256, 64, 8),
-                                     (257, 512, 16, 4), (512, 256, 64, 8), (2000, 256, 96, 8), (4864, 256, 64, 8)])
+                                     (257, 512, 16, 4), (512, 256, 64, 8), (2000, 256, 96, 8), (4864, 256, 64, 8),
+                                     (40, 256, 33, 4), (77, 384, 9, 2), (200, 256, 130, 8), (32, 256, 5, 2),
+                                     (31, 256, 7, 2)])
 def test_route_tensor_core_and_cuda_core_paths(moe, T, H, E, k):
     """T >= 256 bf16 batches take the tcgen05 logits GEMM (E in the N slot, masked to E; split into 2 or 4
     column tiles when the 128-token tiles would leave SMs idle: 512 x 64, 4864 x 64 and 300 x 256 take 4,
-    2000 x 96 and the 8192-token prefill layers take 2); shorter ones the CUDA cores."""
+    2000 x 96 and the 8192-token prefill layers take 2); shorter ones the CUDA cores, from 32 tokens with
+    four experts per CTA (expert counts that are not a multiple of 4 included), below with one."""
     sp = spec("prefill", T=T, H=H, E=E, k=k)
     L = make_layer(sp, weights=False)
     make_tie_free(L)
