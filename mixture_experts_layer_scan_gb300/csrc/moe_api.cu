@@ -545,6 +545,9 @@ static int forward_steps(const Plan& pl, int steps, const void* hidden, const vo
       g1.prefetch_kb = (int)std::max<long>(1, (64L << 20) / (kb_bytes * std::max(1, sms)));
     }
     g1.early = g1_early;
+    // swap-AB GEMM2 may claim its tiles past the first wave from a counter that GEMM1 zeroes
+    int* g2_claim = (pl.swap && pl.path != PATH_W4 && !gate) ? reinterpret_cast<int*>(ws + pl.o_misc + 128) : nullptr;
+    g1.zero_word = g2_claim;
     void* aint_lo = pl.act_split ? (void*)((uint16_t*)aint + (size_t)cap * I) : nullptr;
     if (pl.s1 > 1) {
       g1.epi = TC_EPI_G1_PART;
@@ -599,6 +602,7 @@ static int forward_steps(const Plan& pl, int steps, const void* hidden, const vo
     // its dependents launch only after its own dependency wait: the permutation
     // metadata is complete by then, so GEMM2 may stream weights early.
     g2.early = true;
+    g2.claim = g2_claim;
     if (o) record(o->stage_begin[MOE_STAGE_GEMM2], s);
     MOE_TRY(launch_gemm_tc(g2, s));
     if (o) record(o->stage_end[MOE_STAGE_GEMM2], s);

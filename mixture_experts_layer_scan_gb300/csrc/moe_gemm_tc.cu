@@ -41,6 +41,8 @@ namespace {
 
 constexpr int kTcThreads = 192;
 constexpr int kMaxStages = 8;
+constexpr int kTileQueue = 8;   // claimed-tile slots between the producer and the other roles
+constexpr int kClaimMinWaves = 4;  // claim tiles only from this many waves of them
 constexpr uint32_t kTmemCols = 512;  // all of tensor memory: accumulator buffers
 
 struct TcDev {
@@ -70,6 +72,8 @@ struct TcDev {
   void* out_fin_lo;
   const unsigned* ready;  // nullable: expert e's weights are streamed once ready[e] == want[e]
   const unsigned* want;
+  int* claim;             // nullable: tiles past the first wave may be claimed from this counter
+  int* zero_word;         // nullable: set to 0 after the dependency wait (the next GEMM's counter)
   const int32_t* sorted;
   const int32_t* eids;
   const int32_t* meta;
@@ -369,12 +373,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t bar_exit = bar_drain + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + p.bar_off + 8 * (2 * kMaxStages + 6));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // claimed tiles: the producer publishes each tile index (or the end) in a ring of
+  // kTileQueue slots read by the MMA warp and the four epilogue warps
+  const uint32_t bar_tq_full = bar_full + 8 * (2 * kMaxStages + 6) + 16;
+  const uint32_t bar_tq_empty = bar_tq_full + 8 * kTileQueue;
+  volatile int* tq = reinterpret_cast<volatile int*>(smem + p.bar_off + 8 * (2 * kMaxStages + 6) + 16 + 16 * kTileQueue);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int q = 0; q < kTileQueue; ++q) {
+      mbar_init(bar_tq_full + 8 * q, 1);
+      mbar_init(bar_tq_empty + 8 * q, 1 + 4);  // the MMA warp and the four epilogue warps
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_tfull + 8 * b, 1);
@@ -422,6 +435,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // metadata is complete) and for the router GEMM (which reads none).
   if (!p.early) pdl_wait();
   const int ntiles = tile_count<SWAP, EPI>(p);
+  // Tiles past each CTA's first are claimed from a counter when there are at least
+  // kClaimMinWaves waves of them: SMs that stream faster then take more tiles (FP8 decode
+  // at 16 tokens, 5.8 waves: 886 against 910 us).  With fewer waves the static schedule
+  // measured faster (fine-grained decode at 32 and 64 tokens, 2.1-2.7 waves).
+  const bool claim = p.claim != nullptr && ntiles >= kClaimMinWaves * (int)gridDim.x;
   constexpr int KBLK = FP8 ? 128 : 64;  // elements per 128-byte K block
 
   if (warp == 0) {
@@ -462,12 +480,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     pre = __shfl_sync(0xffffffffu, pre, 0);
     pdl_wait();
+    if (p.zero_word && blockIdx.x == 0 && lane == 0) *p.zero_word = 0;
     const int n_pairs = p.T * p.k;
     const int npp = (EPI == TC_EPI_LOGITS) ? 0 : p.meta[META_NPP];
     int stage = 0;
     uint32_t phase = 0, issued = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+    for (int i = 0, t = blockIdx.x; ok; ++i) {
+      if (claim) {
+        // the first tile is blockIdx.x (its weights may already be on their way)
+        if (i > 0) {
+          int c = 0;
+          if (lane == 0) c = atomicAdd(p.claim, 1);
+          t = (int)gridDim.x + __shfl_sync(0xffffffffu, c, 0);
+        }
+        const int slot = i % kTileQueue;
+        if (i >= kTileQueue &&
+            !mbar_wait_all(bar_tq_empty + 8 * slot, ((uint32_t)(i / kTileQueue) & 1u) ^ 1u, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          tq[slot] = t;
+          mbar_arrive(bar_tq_full + 8 * slot);
+        }
+        __syncwarp();
+      } else if (i > 0) {
+        t += gridDim.x;
+      }
+      if (t >= ntiles) break;
       const Tile d = tile_at<SWAP, EPI>(p, t);
       // expert cache: this expert's weights may still be on their way into its slot
       if (p.ready && !wait_word_all(p.ready + d.e, p.want[d.e], abort_flag, p.status)) {
@@ -545,7 +586,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
     bool ok = true, any = false;
-    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+    for (int i = 0, t = blockIdx.x; ok; ++i) {
+      if (claim) {
+        const int slot = i % kTileQueue;
+        if (!mbar_wait_all(bar_tq_full + 8 * slot, (uint32_t)(i / kTileQueue) & 1u, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        t = tq[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_tq_empty + 8 * slot);
+      } else if (i > 0) {
+        t += gridDim.x;
+      }
+      if (t >= ntiles) break;
       const Tile d = tile_at<SWAP, EPI>(p, t);
       // (stacked hi/lo: the B rows are the xbox hi rows, then the lo rows, all in one MMA)
       const int N = SWAP ? (p.stack_lo ? p.xbox + d.npad : d.npad) : 2 * p.wbox;
@@ -621,7 +675,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     const int n_pairs = p.T * p.k;
-    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    for (int i = 0, t = blockIdx.x;; ++i) {
+      if (claim) {
+        const int slot = i % kTileQueue;
+        const bool okq = mbar_wait_all(bar_tq_full + 8 * slot, (uint32_t)(i / kTileQueue) & 1u, abort_flag, p.status);
+        if (epi_any(!okq)) break;
+        t = tq[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_tq_empty + 8 * slot);
+      } else if (i > 0) {
+        t += gridDim.x;
+      }
+      if (t >= ntiles) break;
       const Tile d = tile_at<SWAP, EPI>(p, t);
       const bool ok = mbar_wait_all(bar_tfull + 8 * acc, acc_phase, abort_flag, p.status);
       if (epi_any(!ok)) break;
@@ -1625,6 +1690,8 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s) {
   p.out = a.out;
   p.gather = a.gather ? 1 : 0;
   p.early = a.early ? 1 : 0;
+  p.claim = a.claim;
+  p.zero_word = a.zero_word;
   p.n_valid = a.n_valid;
   p.out_lo = a.out_lo;
   p.x_lo_rows = a.x_lo_rows;
@@ -1642,7 +1709,7 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s) {
 
   p.w_bytes = (uint32_t)(2 * a.wbox * 128);
   p.stage_bytes = p.w_bytes + (uint32_t)(a.xbox * 128) * (a.x_lo_rows ? 2u : 1u);
-  const uint32_t bar_bytes = 8 * (2 * kMaxStages + 6) + 16;
+  const uint32_t bar_bytes = 8 * (2 * kMaxStages + 6) + 16 + 16 * kTileQueue + 4 * kTileQueue;
   const uint32_t budget = 227 * 1024 - 1024 - bar_bytes;
   int stages = (int)(budget / p.stage_bytes);
   if (stages > kMaxStages) stages = kMaxStages;

@@ -143,6 +143,10 @@ struct TcGemmArgs {
   // ready[e] == want[e] (words written by the cache's copy stream after each copy); nullable
   const unsigned* ready;
   const unsigned* want;
+  // swap-AB k_gemm_tc: tiles past the first wave may be claimed from *claim (zeroed each call
+  // by the preceding GEMM through zero_word, after its dependency wait); nullable
+  int* claim;
+  int* zero_word;
 };
 cudaError_t launch_gemm_tc(const TcGemmArgs& a, cudaStream_t s);
 
