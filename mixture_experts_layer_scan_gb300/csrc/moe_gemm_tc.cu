@@ -432,7 +432,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // dependents launch early, so nothing written by an earlier kernel may be
   // read before pdl_wait() -- except when the host sets `early`: for GEMM2
   // (launched only after GEMM1 has itself passed its wait, so the permutation
-  // metadata is complete) and for the router GEMM (which reads none).
+  // metadata is complete), for a GEMM1 behind a row gather that lets its
+  // dependents launch only after its own wait (the same guarantee), and for the
+  // router GEMM (which reads none).
   if (!p.early) pdl_wait();
   const int ntiles = tile_count<SWAP, EPI>(p);
   // Tiles past each CTA's first are claimed from a counter when there are at least
